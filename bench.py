@@ -1,0 +1,305 @@
+#!/usr/bin/env python3
+"""Decode throughput of the routed sparse-MoE stack on GB300.
+
+One step = one batch of B tokens through every MoE layer of the workload
+(router -> top-k -> slot lookup -> int4 dequant gate/up + SwiGLU -> down +
+weighted combine + sigmoid-gated shared expert -> renormalisation), through
+the C ABI (moe_forward_decode_stack) with inputs resident in HBM.
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle on the
+host cores on the same workload instead (each step: one token through one
+layer, which is 1/n_layers of a token of the metric's unit).
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MoE-stack decode tok/s; expert-weight HBM GB/s as fraction of GB300 peak"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2048)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="35b", choices=["35b", "80b", "stress"])
+    ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--bits", type=int, default=0)
+    ap.add_argument("--cpu-samples", type=int, default=64, help="(token, layer) samples of the oracle baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d.get("hbm_gbs", FALLBACK_HBM_GBS)), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def workload_desc(w, B, bits):
+    return (f"{w.name} decode stack: {w.n_layers} MoE layers, hidden {w.hidden}, {w.n_experts} experts top-{w.top_k}, "
+            f"expert inter {w.inter}, shared inter {w.shared_inter}, int{bits} group-64 affine, batch {B}"
+            + (", Zipf(1.1) router bias" if w.zipf_s else "") + ", renormalised per layer, all experts resident")
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region
+# --------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.device = device
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "20"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                try:
+                    rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+                except ValueError:
+                    pass
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [r[0] for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[2]) if v.lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------
+# the CPU oracle (cpu_baseline leg and --impl reference)
+# --------------------------------------------------------------------------
+def oracle_samples(w, bits, n_samples, threads):
+    """(token, layer) samples with their routed experts drawn beforehand (untimed):
+    token = a renormalised N(0,1) vector, the distribution of a layer input."""
+    import oracle
+    samples = []
+    for i in range(n_samples):
+        layer = i % w.n_layers
+        x = oracle.renorm(synth.tokens(w.seed, 900000 + i, 1, w.hidden)[0])
+        wr, wsg, beta = synth.layer_inputs(w, layer)
+        lay = oracle.Layer(w.hidden, w.n_experts, w.top_k, w.inter, w.shared_inter, wr, wsg, {}, router_bias=beta,
+                           shared=synth.expert(w.seed, layer, synth.SHARED, w.hidden, w.shared_inter, bits, w.sigma))
+        _, idx, _, _ = lay.route(x)
+        samples.append((layer, x, lay, [int(e) for e in idx]))
+    with cf.ThreadPoolExecutor(threads) as ex:
+        for (layer, x, lay, idx) in samples:
+            ex_arrays = dict(zip(idx, ex.map(lambda e: synth.expert(w.seed, layer, e, w.hidden, w.inter, bits,
+                                                                    w.sigma), idx)))
+            lay.set_experts(ex_arrays)
+    return samples
+
+
+def time_oracle(samples, n_steps, threads):
+    """Run n_steps (token, layer) oracle evaluations over `threads` host threads."""
+    def run(i):
+        _, x, lay, _ = samples[i % len(samples)]
+        lay.token(x)
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(threads) as ex:
+        list(ex.map(run, range(n_steps)))
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, bits, n_samples):
+    threads = os.cpu_count() or 1
+    samples = oracle_samples(w, bits, min(n_samples, 32), threads)
+    secs = time_oracle(samples, n_samples, threads)
+    return {"value": (n_samples / w.n_layers) / secs, "unit": "tok/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n_samples} (token, layer) evaluations of the fp64 scalar oracle (one token through one "
+                      f"of the {w.n_layers} layers each, inputs renormalised N(0,1)), split over {threads} host "
+                      f"threads; {secs:.1f} s wall"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    w = synth.CONFIGS[args.config]
+    bits = args.bits or w.bits
+    threads = os.cpu_count() or 1
+    samples = oracle_samples(w, bits, 32, threads)
+    time_oracle(samples, max(args.warmup, 1), threads)
+    secs = time_oracle(samples, args.steps, threads)
+    value = (args.steps / w.n_layers) / secs
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(w, 1, bits), "step": "one token through one layer (1/n_layers token)"},
+        "cpu_baseline": {"value": value, "unit": "tok/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{args.steps} (token, layer) oracle evaluations over {threads} host threads"},
+        "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
+# our path
+# --------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+
+    import int4_expert_streaming_gb300 as moe
+    from int4_expert_streaming_gb300 import workload
+
+    rank, world, local = dist_env()
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")  # replicas: host-side barrier and max only
+        pg = dist
+    torch.cuda.set_device(local)
+    w = synth.CONFIGS[args.config]
+    bits = args.bits or w.bits
+    B = args.batch
+    L, H, k = w.n_layers, w.hidden, w.top_k
+    moe.build()
+    ctx = workload.create_loaded(w, bits, max_batch=B)
+    try:
+        n_ring = 256
+        X = torch.from_numpy(np.stack([synth.tokens(w.seed, s, B, H) for s in range(n_ring)])).cuda()
+        y = torch.empty((B, H), device="cuda")
+        st = torch.cuda.current_stream()
+        # expert bytes actually read per step: (distinct routed experts + shared) x blob bytes, per layer
+        blob = moe.moe_blob_bytes(H, w.inter, bits)
+        sblob = moe.moe_blob_bytes(H, w.shared_inter, bits) if w.shared_inter else 0
+        it = torch.empty((L, B, k), dtype=torch.int32, device="cuda")
+        uniq = []
+        for s in range(min(n_ring, 32)):
+            moe.moe_forward_decode_stack(ctx, 0, L, X[s], B, y, 1e-6, None, it, None, st)
+            idx = it.cpu().numpy()
+            uniq.append(sum(len(np.unique(idx[l])) for l in range(L)))
+        expert_bytes = float(np.mean(uniq)) * blob + L * sblob
+        router_bytes = L * w.n_experts * H * 2
+        for s in range(args.warmup):
+            moe.moe_forward_decode_stack(ctx, 0, L, X[s % n_ring], B, y, 1e-6, None, None, None, st)
+        torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+        l0 = moe.moe_launch_count(ctx)
+        clk = ClockSampler(local)
+        clk.start()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(st)
+        for s in range(args.steps):
+            moe.moe_forward_decode_stack(ctx, 0, L, X[s % n_ring], B, y, 1e-6, None, None, None, st)
+        e1.record(st)
+        torch.cuda.synchronize()
+        clocks = clk.stop()
+        launches = moe.moe_launch_count(ctx) - l0
+        ms = e0.elapsed_time(e1)
+        if pg:
+            t = torch.tensor([ms])
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            ms = float(t.item())
+            pg.barrier()
+        secs = ms / 1e3
+        value = args.steps * B * world / secs
+        gbs = expert_bytes * args.steps / secs / 1e9
+        peak, peak_kind = peaks()
+        # end to end through the public API with host buffers: pinned H2D of the
+        # step's tokens, the stack, D2H of the step's output, every step
+        e2e = None
+        if not args.no_e2e:
+            xh = torch.from_numpy(np.stack([synth.tokens(w.seed, s, B, H) for s in range(n_ring)])).pin_memory()
+            yh = torch.empty((B, H)).pin_memory()
+            xd = torch.empty((B, H), device="cuda")
+            n_e2e = min(args.steps, 512)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for s in range(n_e2e):
+                xd.copy_(xh[s % n_ring], non_blocking=True)
+                moe.moe_forward_decode_stack(ctx, 0, L, xd, B, y, 1e-6, None, None, None, st)
+                yh.copy_(y, non_blocking=True)
+                st.synchronize()
+            e2e_s = time.perf_counter() - t0
+            e2e = {"value": n_e2e * B * world / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": B * H * 4,
+                   "d2h_bytes_per_step": B * H * 4, "steps": n_e2e}
+        line = {
+            "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": workload_desc(w, B, bits), "batch": B, "layers": L, "bits": bits,
+                       "parallelism": "replicas" if world > 1 else "single-gpu",
+                       "l2": f"inputs larger than L2: {expert_bytes / 1e6:.1f} MB of expert weights per step"},
+            "expert_gbs": gbs, "hbm_frac": gbs / peak,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                         "peak_kind": peak_kind, "traffic": None,
+                         "kernel": "decode stack (one forward_decode_stack call per step)",
+                         "bytes_per_launch": expert_bytes, "router_bytes_per_launch": router_bytes},
+            "gpu_launches": int(launches),
+            "clocks": clocks,
+            "e2e": e2e,
+        }
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w, bits, args.cpu_samples)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+    finally:
+        moe.moe_destroy(ctx)
+        if pg:
+            pg.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,256 @@
+/*
+ * moe.h -- C ABI of libmoe.so: the routed sparse-MoE layer with expert
+ * streaming, for one NVIDIA GB300 (sm_103a).
+ *
+ * What the layer computes (the Swiftlet pages describe the system; they give
+ * no formulas, the readings below are this library's):
+ *   For each token x (fp32, length hidden) of one MoE layer:
+ *     l      = W_r x + beta                    router logits, W_r bf16 [E x H]
+ *     idx    = top-k of l (descending, ties -> lower expert id)
+ *     w_i    = softmax over the k chosen logits (norm_topk = 1)
+ *     E_e(x) = D_e (silu(G_e x) * (U_e x))     SwiGLU expert, int4/int8 weights
+ *     y      = sum_i w_i E_{idx_i}(x) + sigmoid(w_sg . x) * S(x)
+ *   S is the always-resident shared expert.  Each expert matrix is MLX affine
+ *   group-quantised: w = scale * q + bias per 64 consecutive columns of a row,
+ *   scale and bias fp16.
+ *   [Swiftlet article (linlog.top), "Why MoE architectures can be streamed":
+ *    512 routed experts choose 10 per token (80B), 256 choose 8 (35B), plus
+ *    one shared expert; README translation (news.paixiangai.cn), "How it
+ *    works" and "Relation to TurboFieldfare": MLX affine int4/int8 group
+ *    quantisation computed on the GPU, byte-addressed kernels with 64-bit
+ *    offsets, a cooperative SIMD-group GEMV fast path.]
+ *
+ * Expert storage: every routed expert is one fixed-stride blob, so fetching
+ * an expert is one contiguous copy [article, section 2 "Fixed-stride pread
+ * reads"].  A bounded per-layer slot pool in HBM caches experts and evicts by
+ * use count with recency as the tie-break [article, section 3 "Expert cache
+ * pool and LFU+LRU eviction"; README, "How it works": "LFU plus recency"].
+ * Misses are copied from a pinned host store on a side stream.
+ *
+ * Blob layout v1 (little-endian; offsets in bytes, rows x cols per matrix):
+ *   gate.q  [inter  x hidden*bits/32] u32   element c of a row in word
+ *   up.q    [inter  x hidden*bits/32] u32     c/(32/bits), bit (c%(32/bits))*bits
+ *   down.q  [hidden x inter*bits/32]  u32     (low bits first)
+ *   gate.sb [inter  x hidden/64] u32     low half fp16 scale, high half fp16 bias
+ *   up.sb   [inter  x hidden/64] u32
+ *   down.sb [hidden x inter/64]  u32
+ *   zero padding up to stride = round_up(bytes, 4096).
+ *
+ * Conventions.
+ *   - Every call returns MOE_OK (0) or a negative MOE_E* code; moe_last_error()
+ *     gives the message of the last failure on that context (or of a failed
+ *     moe_create when ctx is NULL, per host thread).
+ *   - Pointers named *_dev are device pointers owned by the caller (fp32 /
+ *     int32, contiguous, row-major).  Pointers named *_host are host memory
+ *     owned by the caller and only read during the call.
+ *   - `stream` is the caller's cudaStream_t (NULL = legacy default stream).
+ *   - The library owns the context, the HBM slot pool, the pinned host store,
+ *     its side stream and all scratch.  One host thread per context.
+ *   - A CUDA error poisons the context: later calls return MOE_ESTATE.
+ *   - All-resident contexts (pool_slots == n_experts) never synchronise the
+ *     host in forward calls; streaming contexts synchronise once per layer
+ *     call to read the routing result.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_OK 0
+#define MOE_EINVAL -1   /* invalid argument or shape; no GPU work was issued */
+#define MOE_ENOMEM -2   /* device, pinned or host allocation failed */
+#define MOE_ECUDA -3    /* a CUDA call failed; the context is poisoned */
+#define MOE_EPOOL -4    /* a call needs more distinct experts than the pool has slots */
+#define MOE_ETIMEOUT -5 /* a bounded host or device wait ran out */
+#define MOE_ESTATE -6   /* wrong call order, unloaded layer, or poisoned context */
+
+#define MOE_EVICT_LFU_RECENCY 0 /* victim = min (use count, last use, slot) */
+#define MOE_EVICT_LRU 1         /* victim = min (last use, slot) */
+
+/* fault_flags: host-side fault injection for tests (0 in production). */
+#define MOE_FAULT_PINNED_ALLOC 0x1u /* pretend the pinned store allocation failed */
+#define MOE_FAULT_MISS_COPY 0x2u    /* fail the fault_arg-th miss copy (0-based), without issuing it */
+#define MOE_FAULT_WAIT_TIMEOUT 0x4u /* treat the next host wait as timed out */
+
+typedef struct moe_ctx moe_ctx;
+
+typedef struct {
+    int32_t n_layers;     /* MoE layers held by the context (>= 1) */
+    int32_t hidden;       /* H, multiple of 256 */
+    int32_t n_experts;    /* E routed experts per layer, 1..1024 */
+    int32_t top_k;        /* k, 1..min(E, 16) */
+    int32_t inter;        /* I, expert intermediate size, multiple of 64 */
+    int32_t shared_inter; /* shared expert intermediate, multiple of 64 (0 = no shared expert) */
+    int32_t bits;         /* 4 or 8 */
+    int32_t group_size;   /* 64 only */
+    int32_t pool_slots;   /* slots per layer; == n_experts => all resident, no host sync */
+    int32_t norm_topk;    /* 1 = renormalise the k weights (softmax over chosen), 0 = full softmax */
+    int32_t policy;       /* MOE_EVICT_LFU_RECENCY or MOE_EVICT_LRU */
+    int32_t device;       /* CUDA device ordinal */
+    int32_t max_batch;    /* largest B of a decode call, 1..64 */
+    int32_t max_tokens;   /* largest T of a prefill call (0 = no prefill) */
+    uint32_t fault_flags; /* MOE_FAULT_* (tests only) */
+    int32_t fault_arg;
+    int32_t timeout_ms;   /* bound on every host wait (<= 0: 10000) */
+} moe_config;
+
+typedef struct {
+    uint64_t hits;      /* expert lookups served from the pool */
+    uint64_t misses;    /* lookups that needed a host->HBM copy */
+    uint64_t evictions; /* misses that displaced a resident expert */
+    uint64_t h2d_bytes; /* bytes copied for misses */
+    double h2d_ms;      /* device time of those copies (CUDA events) */
+    int32_t resident;   /* experts currently resident */
+    int32_t calls;      /* forward calls that routed through this layer */
+} moe_pool_stats_t;
+
+/* ------------------------------------------------------------------ */
+/* blobs                                                                */
+/* ------------------------------------------------------------------ */
+
+/* Packed bytes of one expert (before padding) and its fixed stride. 0 on bad shape. */
+size_t moe_blob_bytes(int32_t hidden, int32_t inter, int32_t bits);
+size_t moe_blob_stride(int32_t hidden, int32_t inter, int32_t bits);
+
+/*
+ * Pack one expert's quantised tensors into its blob (host only, pure).
+ * q_*_host: one code per byte, values < 2^bits; gate/up [inter x hidden],
+ * down [hidden x inter].  sb_*_host: fp16 bit patterns, (scale, bias) pairs
+ * per 64-column group, [rows x cols/64 x 2].  blob_host must hold
+ * moe_blob_stride() bytes; padding is zeroed.
+ * Errors: MOE_EINVAL for bad shape, short buffer or an out-of-range code.
+ */
+int moe_pack_expert(int32_t hidden, int32_t inter, int32_t bits, const uint8_t* q_gate_host,
+                    const uint16_t* sb_gate_host, const uint8_t* q_up_host, const uint16_t* sb_up_host,
+                    const uint8_t* q_down_host, const uint16_t* sb_down_host, void* blob_host, size_t blob_bytes);
+
+/* ------------------------------------------------------------------ */
+/* context                                                              */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Validate cfg, allocate the HBM slot pool (n_layers x pool_slots x stride,
+ * 64-bit offsets), the device directory, scratch and, when streaming, the
+ * pinned host store (n_layers x n_experts x stride) and the side stream.
+ * Errors: MOE_EINVAL (bad config, nothing allocated), MOE_ENOMEM, MOE_ECUDA.
+ */
+int moe_create(const moe_config* cfg, moe_ctx** out);
+
+/* Synchronise the library's streams and free everything.  NULL is ignored. */
+void moe_destroy(moe_ctx* ctx);
+
+/*
+ * Load one layer (call once per layer before its first forward).  Copies:
+ *   blobs_host      [n_experts x stride] routed expert blobs (stride as returned
+ *                   by moe_blob_stride for (hidden, inter, bits))
+ *   shared_blob_host one blob of the shared expert (stride for shared_inter),
+ *                   NULL iff shared_inter == 0
+ *   router_w_host   bf16 bits [n_experts x hidden]
+ *   shared_gate_host bf16 bits [hidden] (NULL iff shared_inter == 0)
+ *   router_bias_host fp32 [n_experts] or NULL (= zeros)
+ * All-resident: blobs go straight to their HBM slots (slot = expert id).
+ * Streaming: blobs go to the pinned store; the layer's pool starts empty.
+ * Synchronous (returns when the copies are done).
+ */
+int moe_load_experts(moe_ctx* ctx, int32_t layer, const void* blobs_host, size_t stride,
+                     const void* shared_blob_host, const uint16_t* router_w_host,
+                     const uint16_t* shared_gate_host, const float* router_bias_host);
+
+/* Replace one layer's router bias (fp32 [n_experts], host).  Ordered on `stream`. */
+int moe_set_router_bias(moe_ctx* ctx, int32_t layer, const float* router_bias_host, void* stream);
+
+/* ------------------------------------------------------------------ */
+/* forward                                                              */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Decode: one layer for B tokens (1 <= B <= max_batch).
+ *   x_dev   fp32 [B x hidden] in, y_dev fp32 [B x hidden] out (may not alias x).
+ *   topk_idx_dev int32 [B x top_k] / topk_w_dev fp32 [B x top_k]: the chosen
+ *   experts in descending-logit order and their weights, or NULL.
+ * Asynchronous on `stream` when all experts are resident; otherwise it reads
+ * the routing back once, fetches missed blobs on the side stream and orders
+ * `stream` after them.  Errors: MOE_EINVAL, MOE_ESTATE (layer not loaded),
+ * MOE_EPOOL, MOE_ETIMEOUT, MOE_ECUDA.
+ */
+int moe_forward_decode(moe_ctx* ctx, int32_t layer, const float* x_dev, int32_t B, float* y_dev,
+                       int32_t* topk_idx_dev, float* topk_w_dev, void* stream);
+
+/*
+ * Decode through consecutive layers layer0 .. layer0+n_layers-1 for B tokens:
+ *   y_l = MoE_l(x_l);  x_{l+1} = y_l / sqrt(mean(y_l^2) + renorm_eps)
+ * (the renormalisation stands in for the attention/norm layers that sit
+ * between MoE layers in the full model).  y_dev receives y of the last layer.
+ * Optional traces (NULL to skip), all device, for every layer l of the call:
+ *   x_trace_dev fp32 [n_layers x B x hidden]   layer inputs x_l
+ *   idx_trace_dev int32 [n_layers x B x top_k] chosen experts
+ *   y_trace_dev fp32 [n_layers x B x hidden]   layer outputs y_l
+ * All-resident contexts run the whole stack as one persistent kernel.
+ */
+int moe_forward_decode_stack(moe_ctx* ctx, int32_t layer0, int32_t n_layers, const float* x_dev, int32_t B,
+                             float* y_dev, float renorm_eps, float* x_trace_dev, int32_t* idx_trace_dev,
+                             float* y_trace_dev, void* stream);
+
+/*
+ * Prefill: one layer for T tokens (1 <= T <= max_tokens), all experts of the
+ * layer resident.  Tokens are sorted per expert and the experts run as a
+ * grouped GEMM on the tensor cores: weights dequantised to bf16
+ * (bf16(fp32 fma(scale, q, bias))), activations rounded to bf16, fp32
+ * accumulation, SwiGLU output rounded to bf16 before the down projection.
+ * Routing is computed exactly as in decode (fp32 x).
+ *   x_dev fp32 [T x hidden], y_dev fp32 [T x hidden],
+ *   topk_idx_dev int32 [T x top_k] / topk_w_dev fp32 [T x top_k] or NULL.
+ */
+int moe_forward_prefill(moe_ctx* ctx, int32_t layer, const float* x_dev, int32_t T, float* y_dev,
+                        int32_t* topk_idx_dev, float* topk_w_dev, void* stream);
+
+/* ------------------------------------------------------------------ */
+/* pool introspection                                                   */
+/* ------------------------------------------------------------------ */
+
+/* Counters of one layer, or the sum over layers (layer = -1).  Synchronises. */
+int moe_pool_stats(moe_ctx* ctx, int32_t layer, moe_pool_stats_t* out);
+
+/*
+ * Streaming contexts: copy the pool event trace, oldest first, as rows of six
+ * int32 (call number of that layer, layer, expert, kind 0 = HIT / 1 = MISS,
+ * slot, evicted expert or -1), at most `cap` rows into buf_host; *n_out = rows
+ * available in total.  All-resident contexts record no trace (*n_out = 0):
+ * every lookup is a hit in slot = expert id.
+ */
+int moe_pool_trace(moe_ctx* ctx, int32_t* buf_host, size_t cap, size_t* n_out);
+
+/* Number of CUDA kernels this context has launched so far (all entry points). */
+int moe_launch_count(moe_ctx* ctx, uint64_t* out);
+
+const char* moe_last_error(moe_ctx* ctx);
+
+/* ------------------------------------------------------------------ */
+/* the slot-pool policy on its own (host only; used by the context)      */
+/* ------------------------------------------------------------------ */
+
+typedef struct moe_slotpool moe_slotpool;
+
+int moe_slotpool_create(int32_t slots, int32_t n_experts, int32_t policy, moe_slotpool** out);
+void moe_slotpool_destroy(moe_slotpool* p);
+
+/*
+ * One request of distinct expert ids, ascending (req_host[n]).  Hits update
+ * use count and recency; each miss takes the lowest free slot or evicts the
+ * policy's victim among slots not requested in this call.  events_host
+ * receives n rows of (expert, kind 0 = HIT / 1 = MISS, slot, evicted or -1)
+ * in ascending expert order.  Returns n, or MOE_EPOOL if n > slots,
+ * MOE_EINVAL if req is not ascending and in range.
+ */
+int moe_slotpool_request(moe_slotpool* p, const int32_t* req_host, int32_t n, int32_t* events_host);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

@@ -1,0 +1,616 @@
+// api.cu -- the C ABI of libmoe.so (see include/moe.h): context, expert store,
+// HBM slot pool, miss engine and the forward entry points.
+//
+// Data layout in HBM (64-bit offsets throughout, the "byte-addressed kernels
+// with 64-bit offsets" of the Swiftlet README, "Relation to TurboFieldfare"):
+//   pool        [n_layers][pool_slots][stride] routed expert blobs
+//   shared_pool [n_layers][shared_stride]      shared expert blobs
+//   router_w    [n_layers][E][H] bf16, router_bias [n_layers][E] fp32,
+//   shared_gate [n_layers][H] bf16
+//   dir         [n_layers][E] blob address of each resident expert, NULL if not
+// Streaming contexts keep the full store in pinned host memory
+//   store       [n_layers][E][stride]
+// and fetch a missed expert with one cudaMemcpyAsync of one stride on a side
+// stream -- the CUDA counterpart of Swiftlet's one pread per expert from the
+// fixed-stride container (article section 2; explainer "Flujo de Inferencia"
+// steps 3-6).  The compute stream waits on an event recorded after the copies,
+// which is this library's explicit hazard management between slot refills and
+// the kernels that read them.
+#include <algorithm>
+#include <chrono>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "moe_internal.h"
+#include "stack.h"
+
+int32_t moe_slotpool_resident(const moe_slotpool* p);
+
+namespace {
+
+thread_local std::string g_create_error;
+
+struct LayerStats {
+    uint64_t hits = 0, misses = 0, evictions = 0, h2d_bytes = 0;
+    double h2d_ms = 0.0;
+    int32_t calls = 0;
+};
+
+}  // namespace
+
+struct moe_ctx {
+    moe_config cfg{};
+    moe::Shapes sh{};
+    size_t stride = 0, shared_stride = 0;
+    bool resident = false, poisoned = false;
+    std::string err;
+
+    // device
+    uint8_t* pool = nullptr;
+    uint8_t* shared_pool = nullptr;
+    uint16_t* router_w = nullptr;
+    float* router_bias = nullptr;
+    uint16_t* shared_gate = nullptr;
+    const uint8_t** dir = nullptr;
+    unsigned long long* hits_dev = nullptr;
+    float* logits = nullptr;
+    float* sigma = nullptr;
+    int32_t* idx = nullptr;
+    float* w = nullptr;
+    float* h = nullptr;
+    float* xbuf = nullptr;  // [2][max_batch][H]
+    float* ybuf = nullptr;  // [max_batch][H]
+    void* disp_mem = nullptr;
+    moe::Dispatch disp{};
+    moe::StackScratch stack{};
+
+    // host
+    uint8_t* store = nullptr;
+    const uint8_t** dir_host = nullptr;
+    int32_t* idx_host = nullptr;
+    std::vector<uint8_t> loaded;
+    std::vector<moe_slotpool*> pools;
+    std::vector<LayerStats> stats;
+    std::vector<int32_t> trace;
+    cudaStream_t side = nullptr;
+    cudaEvent_t ev_idx = nullptr, ev_copy0 = nullptr, ev_copy1 = nullptr;
+    int pending_timing_layer = -1;
+    int64_t miss_copies = 0;
+    bool fault_timeout_armed = false;
+    uint64_t launches = 0;
+};
+
+namespace {
+
+int fail(moe_ctx* c, int code, const char* fmt, ...) __attribute__((format(printf, 3, 4)));
+
+int fail(moe_ctx* c, int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    if (c) {
+        c->err = buf;
+        if (code == MOE_ECUDA) c->poisoned = true;
+    } else {
+        g_create_error = buf;
+    }
+    return code;
+}
+
+#define CUDA_TRY(ctx, expr)                                                                          \
+    do {                                                                                             \
+        cudaError_t e_ = (expr);                                                                     \
+        if (e_ != cudaSuccess)                                                                       \
+            return fail((ctx), MOE_ECUDA, "%s failed: %s (%s:%d)", #expr, cudaGetErrorString(e_), \
+                        __FILE__, __LINE__);                                                         \
+    } while (0)
+
+int timeout_ms(const moe_ctx* c) { return c->cfg.timeout_ms > 0 ? c->cfg.timeout_ms : 10000; }
+
+// Bounded host wait on an event: polls cudaEventQuery until the deadline.
+int wait_event(moe_ctx* c, cudaEvent_t ev) {
+    if (c->fault_timeout_armed) {
+        c->fault_timeout_armed = false;
+        return fail(c, MOE_ETIMEOUT, "host wait timed out (injected)");
+    }
+    const auto deadline = std::chrono::steady_clock::now() + std::chrono::milliseconds(timeout_ms(c));
+    for (;;) {
+        cudaError_t e = cudaEventQuery(ev);
+        if (e == cudaSuccess) return MOE_OK;
+        if (e != cudaErrorNotReady)
+            return fail(c, MOE_ECUDA, "cudaEventQuery failed: %s", cudaGetErrorString(e));
+        if (std::chrono::steady_clock::now() > deadline)
+            return fail(c, MOE_ETIMEOUT, "host wait exceeded %d ms", timeout_ms(c));
+        std::this_thread::yield();
+    }
+}
+
+int check_config(const moe_config* g) {
+    if (!g) return fail(nullptr, MOE_EINVAL, "cfg is NULL");
+    if (g->n_layers < 1) return fail(nullptr, MOE_EINVAL, "n_layers must be >= 1");
+    if (g->hidden < 256 || g->hidden % 256) return fail(nullptr, MOE_EINVAL, "hidden must be a multiple of 256");
+    if (g->n_experts < 1 || g->n_experts > 1024) return fail(nullptr, MOE_EINVAL, "n_experts must be in 1..1024");
+    if (g->top_k < 1 || g->top_k > 16 || g->top_k > g->n_experts)
+        return fail(nullptr, MOE_EINVAL, "top_k must be in 1..min(16, n_experts)");
+    if (g->inter < 64 || g->inter % 64) return fail(nullptr, MOE_EINVAL, "inter must be a positive multiple of 64");
+    if (g->shared_inter < 0 || g->shared_inter % 64)
+        return fail(nullptr, MOE_EINVAL, "shared_inter must be a multiple of 64");
+    if (g->bits != 4 && g->bits != 8) return fail(nullptr, MOE_EINVAL, "bits must be 4 or 8");
+    if (g->group_size != 64) return fail(nullptr, MOE_EINVAL, "group_size must be 64");
+    if (g->pool_slots < g->top_k || g->pool_slots > g->n_experts)
+        return fail(nullptr, MOE_EINVAL, "pool_slots must be in top_k..n_experts");
+    if (g->policy != MOE_EVICT_LFU_RECENCY && g->policy != MOE_EVICT_LRU)
+        return fail(nullptr, MOE_EINVAL, "unknown eviction policy");
+    if (g->max_batch < 1 || g->max_batch > 64) return fail(nullptr, MOE_EINVAL, "max_batch must be in 1..64");
+    if (g->max_tokens < 0 || g->max_tokens > (1 << 20)) return fail(nullptr, MOE_EINVAL, "max_tokens out of range");
+    return MOE_OK;
+}
+
+template <class T>
+int dev_alloc(moe_ctx* c, T** p, size_t n, const char* what) {
+    if (n == 0) n = 1;
+    cudaError_t e = cudaMalloc(reinterpret_cast<void**>(p), n * sizeof(T));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(c, MOE_ENOMEM, "cudaMalloc(%s, %zu bytes) failed: %s", what, n * sizeof(T),
+                    cudaGetErrorString(e));
+    }
+    return MOE_OK;
+}
+
+int check_layer(moe_ctx* c, int32_t layer) {
+    if (c->poisoned) return fail(c, MOE_ESTATE, "context poisoned by an earlier CUDA error");
+    if (layer < 0 || layer >= c->cfg.n_layers) return fail(c, MOE_EINVAL, "layer %d out of range", layer);
+    if (!c->loaded[layer]) return fail(c, MOE_ESTATE, "layer %d has not been loaded", layer);
+    return MOE_OK;
+}
+
+const uint8_t* shared_blob(moe_ctx* c, int layer) {
+    return c->cfg.shared_inter > 0 ? c->shared_pool + (size_t)layer * c->shared_stride : nullptr;
+}
+
+// Account the device time of the previous call's miss copies (already complete
+// once the compute stream has passed the point the host just waited for).
+void harvest_copy_timing(moe_ctx* c) {
+    if (c->pending_timing_layer < 0) return;
+    float ms = 0.0f;
+    if (cudaEventElapsedTime(&ms, c->ev_copy0, c->ev_copy1) == cudaSuccess)
+        c->stats[c->pending_timing_layer].h2d_ms += ms;
+    else
+        cudaGetLastError();
+    c->pending_timing_layer = -1;
+}
+
+// Streaming: read back the routing, run the pool policy, fetch misses.
+int resolve_pool(moe_ctx* c, int layer, int B, cudaStream_t st) {
+    const int k = c->cfg.top_k, E = c->cfg.n_experts;
+    CUDA_TRY(c, cudaMemcpyAsync(c->idx_host, c->idx, sizeof(int32_t) * B * k, cudaMemcpyDeviceToHost, st));
+    CUDA_TRY(c, cudaEventRecord(c->ev_idx, st));
+    int rc = wait_event(c, c->ev_idx);
+    if (rc) return rc;
+    harvest_copy_timing(c);
+    std::vector<int32_t> req(c->idx_host, c->idx_host + B * k);
+    std::sort(req.begin(), req.end());
+    req.erase(std::unique(req.begin(), req.end()), req.end());
+    std::vector<int32_t> ev(4 * req.size());
+    rc = moe_slotpool_request(c->pools[layer], req.data(), (int32_t)req.size(), ev.data());
+    if (rc < 0)
+        return fail(c, rc, "slot pool request of %zu experts failed (pool has %d slots)", req.size(),
+                    c->cfg.pool_slots);
+    LayerStats& S = c->stats[layer];
+    const int64_t call_no = S.calls;
+    const uint8_t** dirh = c->dir_host + (size_t)layer * E;
+    bool any_miss = false;
+    for (size_t i = 0; i < req.size(); ++i) {
+        const int32_t e = ev[4 * i], kind = ev[4 * i + 1], slot = ev[4 * i + 2], evicted = ev[4 * i + 3];
+        c->trace.insert(c->trace.end(), {(int32_t)call_no, layer, e, kind, slot, evicted});
+        if (kind == 0) {
+            S.hits++;
+            continue;
+        }
+        S.misses++;
+        if (evicted >= 0) {
+            S.evictions++;
+            dirh[evicted] = nullptr;
+        }
+        uint8_t* dst = c->pool + ((size_t)layer * c->cfg.pool_slots + slot) * c->stride;
+        const uint8_t* src = c->store + ((size_t)layer * E + e) * c->stride;
+        if (!any_miss) {
+            CUDA_TRY(c, cudaEventRecord(c->ev_copy0, c->side));
+            any_miss = true;
+        }
+        if ((c->cfg.fault_flags & MOE_FAULT_MISS_COPY) && c->miss_copies == c->cfg.fault_arg) {
+            c->miss_copies++;
+            return fail(c, MOE_ECUDA, "miss copy %d failed (injected)", c->cfg.fault_arg);
+        }
+        c->miss_copies++;
+        CUDA_TRY(c, cudaMemcpyAsync(dst, src, c->stride, cudaMemcpyHostToDevice, c->side));
+        S.h2d_bytes += c->stride;
+        dirh[e] = dst;
+    }
+    if (any_miss) {
+        CUDA_TRY(c, cudaEventRecord(c->ev_copy1, c->side));
+        CUDA_TRY(c, cudaStreamWaitEvent(st, c->ev_copy1, 0));
+        c->pending_timing_layer = layer;
+    }
+    CUDA_TRY(c, cudaMemcpyAsync(c->dir + (size_t)layer * E, dirh, sizeof(void*) * E, cudaMemcpyHostToDevice, st));
+    return MOE_OK;
+}
+
+int decode_layer(moe_ctx* c, int layer, const float* x, int B, float* y, int32_t* uidx, float* uw,
+                 cudaStream_t st) {
+    const moe::Shapes& s = c->sh;
+    const int E = c->cfg.n_experts;
+    const uint16_t* wr = c->router_w + (size_t)layer * E * c->cfg.hidden;
+    const float* bias = c->router_bias + (size_t)layer * E;
+    const uint16_t* wsg = c->cfg.shared_inter > 0 ? c->shared_gate + (size_t)layer * c->cfg.hidden : nullptr;
+    const uint8_t* const* dir = c->dir + (size_t)layer * E;
+    CUDA_TRY(c, moe::launch_router(s, wr, bias, x, B, c->logits, st));
+    c->launches += c->resident ? 4 : 5;
+    if (c->resident) {
+        CUDA_TRY(c, moe::launch_route_dispatch(s, 3, c->logits, x, wsg, B, c->idx, c->w, c->sigma, uidx, uw, dir,
+                                               shared_blob(c, layer), c->disp, c->hits_dev + layer, st));
+    } else {
+        CUDA_TRY(c, moe::launch_route_dispatch(s, 1, c->logits, x, wsg, B, c->idx, c->w, c->sigma, uidx, uw, dir,
+                                               shared_blob(c, layer), c->disp, nullptr, st));
+        int rc = resolve_pool(c, layer, B, st);
+        if (rc) return rc;
+        CUDA_TRY(c, moe::launch_route_dispatch(s, 2, c->logits, x, wsg, B, c->idx, c->w, c->sigma, nullptr,
+                                               nullptr, dir, shared_blob(c, layer), c->disp, nullptr, st));
+    }
+    CUDA_TRY(c, moe::launch_gateup(s, c->disp, x, c->h, B, st));
+    CUDA_TRY(c, moe::launch_down(s, c->disp, c->h, y, B, st));
+    c->stats[layer].calls++;
+    return MOE_OK;
+}
+
+}  // namespace
+
+// ===========================================================================
+// C ABI
+// ===========================================================================
+
+extern "C" const char* moe_last_error(moe_ctx* ctx) {
+    return ctx ? ctx->err.c_str() : g_create_error.c_str();
+}
+
+extern "C" void moe_destroy(moe_ctx* c) {
+    if (!c) return;
+    if (c->cfg.device >= 0) cudaSetDevice(c->cfg.device);
+    if (c->side) cudaStreamSynchronize(c->side);
+    cudaDeviceSynchronize();
+    cudaFree(c->pool);
+    cudaFree(c->shared_pool);
+    cudaFree(c->router_w);
+    cudaFree(c->router_bias);
+    cudaFree(c->shared_gate);
+    cudaFree(c->dir);
+    cudaFree(c->hits_dev);
+    cudaFree(c->logits);
+    cudaFree(c->sigma);
+    cudaFree(c->idx);
+    cudaFree(c->w);
+    cudaFree(c->h);
+    cudaFree(c->xbuf);
+    cudaFree(c->ybuf);
+    cudaFree(c->disp_mem);
+    moe::stack_free(c->stack);
+    if (c->store) cudaFreeHost(c->store);
+    if (c->dir_host) cudaFreeHost(c->dir_host);
+    if (c->idx_host) cudaFreeHost(c->idx_host);
+    for (auto* p : c->pools) moe_slotpool_destroy(p);
+    if (c->side) cudaStreamDestroy(c->side);
+    if (c->ev_idx) cudaEventDestroy(c->ev_idx);
+    if (c->ev_copy0) cudaEventDestroy(c->ev_copy0);
+    if (c->ev_copy1) cudaEventDestroy(c->ev_copy1);
+    cudaGetLastError();
+    delete c;
+}
+
+extern "C" int moe_create(const moe_config* cfg, moe_ctx** out) {
+    if (!out) return fail(nullptr, MOE_EINVAL, "out is NULL");
+    *out = nullptr;
+    int rc = check_config(cfg);
+    if (rc) return rc;
+    moe_ctx* c = new (std::nothrow) moe_ctx;
+    if (!c) return fail(nullptr, MOE_ENOMEM, "host allocation failed");
+    c->cfg = *cfg;
+    const moe_config& g = c->cfg;
+    c->resident = g.pool_slots == g.n_experts;
+    c->stride = moe_blob_stride(g.hidden, g.inter, g.bits);
+    c->shared_stride = g.shared_inter > 0 ? moe_blob_stride(g.hidden, g.shared_inter, g.bits) : 0;
+    c->fault_timeout_armed = (g.fault_flags & MOE_FAULT_WAIT_TIMEOUT) != 0;
+    const int L = g.n_layers, E = g.n_experts, H = g.hidden, Bm = g.max_batch, k = g.top_k;
+    moe::Shapes& s = c->sh;
+    s.hidden = H, s.n_experts = E, s.top_k = k, s.inter = g.inter, s.shared_inter = g.shared_inter;
+    s.bits = g.bits, s.norm_topk = g.norm_topk ? 1 : 0;
+    s.max_act = std::min(E, Bm * k) + 1;
+    s.max_pairs = Bm * (k + 1);
+    s.h_stride = std::max(g.inter, g.shared_inter);
+    c->loaded.assign(L, 0);
+    c->stats.assign(L, LayerStats{});
+
+    auto bail = [&](int code) {
+        std::string msg = c->err;
+        moe_destroy(c);
+        g_create_error = msg;
+        return code;
+    };
+    if (cudaSetDevice(g.device) != cudaSuccess) {
+        cudaGetLastError();
+        c->err = "cudaSetDevice failed";
+        return bail(MOE_ECUDA);
+    }
+    if ((rc = dev_alloc(c, &c->pool, (size_t)L * g.pool_slots * c->stride, "slot pool")) ||
+        (rc = dev_alloc(c, &c->shared_pool, (size_t)L * c->shared_stride, "shared pool")) ||
+        (rc = dev_alloc(c, &c->router_w, (size_t)L * E * H, "router weights")) ||
+        (rc = dev_alloc(c, &c->router_bias, (size_t)L * E, "router bias")) ||
+        (rc = dev_alloc(c, &c->shared_gate, (size_t)L * H, "shared gate")) ||
+        (rc = dev_alloc(c, &c->dir, (size_t)L * E, "directory")) ||
+        (rc = dev_alloc(c, &c->hits_dev, (size_t)L, "hit counters")) ||
+        (rc = dev_alloc(c, &c->logits, (size_t)Bm * E, "logits")) ||
+        (rc = dev_alloc(c, &c->sigma, (size_t)Bm, "sigma")) ||
+        (rc = dev_alloc(c, &c->idx, (size_t)Bm * k, "idx")) || (rc = dev_alloc(c, &c->w, (size_t)Bm * k, "w")) ||
+        (rc = dev_alloc(c, &c->h, (size_t)s.max_pairs * s.h_stride, "h")) ||
+        (rc = dev_alloc(c, &c->xbuf, (size_t)2 * Bm * H, "xbuf")) ||
+        (rc = dev_alloc(c, &c->ybuf, (size_t)Bm * H, "ybuf")))
+        return bail(rc);
+    // dispatch scratch in one allocation
+    {
+        const size_t A = s.max_act, P = s.max_pairs;
+        const size_t bytes = 16 + A * 4 + A * 8 + (A + 1) * 4 + P * 4 + P * 4 + 16 + 64;
+        if ((rc = dev_alloc(c, reinterpret_cast<uint8_t**>(&c->disp_mem), bytes, "dispatch"))) return bail(rc);
+        uint8_t* p = static_cast<uint8_t*>(c->disp_mem);
+        auto take = [&](size_t n) {
+            uint8_t* q = p;
+            p += (n + 15) / 16 * 16;
+            return q;
+        };
+        c->disp.n_act = reinterpret_cast<int32_t*>(take(4));
+        c->disp.status = reinterpret_cast<int32_t*>(take(4));
+        c->disp.act_blob = reinterpret_cast<const uint8_t**>(take(A * 8));
+        c->disp.act_expert = reinterpret_cast<int32_t*>(take(A * 4));
+        c->disp.act_off = reinterpret_cast<int32_t*>(take((A + 1) * 4));
+        c->disp.pair_token = reinterpret_cast<int32_t*>(take(P * 4));
+        c->disp.pair_w = reinterpret_cast<float*>(take(P * 4));
+        if (cudaMemset(c->disp_mem, 0, bytes) != cudaSuccess) {
+            c->err = "cudaMemset failed";
+            return bail(MOE_ECUDA);
+        }
+    }
+    if (cudaMemset(c->dir, 0, sizeof(void*) * (size_t)L * E) != cudaSuccess ||
+        cudaMemset(c->hits_dev, 0, sizeof(unsigned long long) * L) != cudaSuccess ||
+        cudaMemset(c->router_bias, 0, sizeof(float) * (size_t)L * E) != cudaSuccess) {
+        c->err = "cudaMemset failed";
+        return bail(MOE_ECUDA);
+    }
+    if (c->resident) {
+        rc = moe::stack_alloc(c->stack, s, L, Bm, c->err);
+        if (rc) return bail(rc);
+    } else {
+        if (g.fault_flags & MOE_FAULT_PINNED_ALLOC) {
+            c->err = "pinned store allocation failed (injected)";
+            return bail(MOE_ENOMEM);
+        }
+        const size_t store_bytes = (size_t)L * E * c->stride;
+        if (cudaHostAlloc(reinterpret_cast<void**>(&c->store), store_bytes, cudaHostAllocDefault) != cudaSuccess) {
+            cudaGetLastError();
+            c->store = nullptr;
+            char buf[160];
+            snprintf(buf, sizeof buf, "cudaHostAlloc of the %zu-byte pinned store failed", store_bytes);
+            c->err = buf;
+            return bail(MOE_ENOMEM);
+        }
+        if (cudaHostAlloc(reinterpret_cast<void**>(&c->dir_host), sizeof(void*) * (size_t)L * E,
+                          cudaHostAllocDefault) != cudaSuccess ||
+            cudaHostAlloc(reinterpret_cast<void**>(&c->idx_host), sizeof(int32_t) * Bm * k, cudaHostAllocDefault) !=
+                cudaSuccess) {
+            cudaGetLastError();
+            c->err = "cudaHostAlloc failed";
+            return bail(MOE_ENOMEM);
+        }
+        std::memset(c->dir_host, 0, sizeof(void*) * (size_t)L * E);
+        c->pools.assign(L, nullptr);
+        for (int l = 0; l < L; ++l)
+            if ((rc = moe_slotpool_create(g.pool_slots, E, g.policy, &c->pools[l]))) {
+                c->err = "slot pool creation failed";
+                return bail(rc);
+            }
+        if (cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking) != cudaSuccess) {
+            c->err = "cudaStreamCreate failed";
+            return bail(MOE_ECUDA);
+        }
+    }
+    if (cudaEventCreateWithFlags(&c->ev_idx, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreate(&c->ev_copy0) != cudaSuccess || cudaEventCreate(&c->ev_copy1) != cudaSuccess) {
+        c->err = "cudaEventCreate failed";
+        return bail(MOE_ECUDA);
+    }
+    *out = c;
+    return MOE_OK;
+}
+
+extern "C" int moe_load_experts(moe_ctx* c, int32_t layer, const void* blobs, size_t stride,
+                                const void* shared_blob_host, const uint16_t* router_w_host,
+                                const uint16_t* shared_gate_host, const float* router_bias_host) {
+    if (!c) return fail(nullptr, MOE_EINVAL, "ctx is NULL");
+    if (c->poisoned) return fail(c, MOE_ESTATE, "context poisoned by an earlier CUDA error");
+    const moe_config& g = c->cfg;
+    if (layer < 0 || layer >= g.n_layers) return fail(c, MOE_EINVAL, "layer %d out of range", layer);
+    if (!blobs || !router_w_host) return fail(c, MOE_EINVAL, "blobs and router weights are required");
+    if (stride != c->stride) return fail(c, MOE_EINVAL, "stride %zu != expected %zu", stride, c->stride);
+    if ((g.shared_inter > 0) != (shared_blob_host != nullptr) || (g.shared_inter > 0) != (shared_gate_host != nullptr))
+        return fail(c, MOE_EINVAL, "shared blob and shared gate are required iff shared_inter > 0");
+    CUDA_TRY(c, cudaSetDevice(g.device));
+    const int E = g.n_experts, H = g.hidden;
+    const size_t layer_bytes = (size_t)E * c->stride;
+    if (c->resident) {
+        CUDA_TRY(c, cudaMemcpy(c->pool + (size_t)layer * layer_bytes, blobs, layer_bytes, cudaMemcpyHostToDevice));
+        std::vector<const uint8_t*> d(E);
+        for (int e = 0; e < E; ++e) d[e] = c->pool + ((size_t)layer * E + e) * c->stride;
+        CUDA_TRY(c, cudaMemcpy(c->dir + (size_t)layer * E, d.data(), sizeof(void*) * E, cudaMemcpyHostToDevice));
+    } else {
+        std::memcpy(c->store + (size_t)layer * layer_bytes, blobs, layer_bytes);
+    }
+    if (g.shared_inter > 0) {
+        CUDA_TRY(c, cudaMemcpy(c->shared_pool + (size_t)layer * c->shared_stride, shared_blob_host, c->shared_stride,
+                               cudaMemcpyHostToDevice));
+        CUDA_TRY(c, cudaMemcpy(c->shared_gate + (size_t)layer * H, shared_gate_host, sizeof(uint16_t) * H,
+                               cudaMemcpyHostToDevice));
+    }
+    CUDA_TRY(c, cudaMemcpy(c->router_w + (size_t)layer * E * H, router_w_host, sizeof(uint16_t) * (size_t)E * H,
+                           cudaMemcpyHostToDevice));
+    if (router_bias_host)
+        CUDA_TRY(c, cudaMemcpy(c->router_bias + (size_t)layer * E, router_bias_host, sizeof(float) * E,
+                               cudaMemcpyHostToDevice));
+    else
+        CUDA_TRY(c, cudaMemset(c->router_bias + (size_t)layer * E, 0, sizeof(float) * E));
+    c->loaded[layer] = 1;
+    return MOE_OK;
+}
+
+extern "C" int moe_set_router_bias(moe_ctx* c, int32_t layer, const float* bias_host, void* stream) {
+    if (!c) return fail(nullptr, MOE_EINVAL, "ctx is NULL");
+    int rc = check_layer(c, layer);
+    if (rc) return rc;
+    if (!bias_host) return fail(c, MOE_EINVAL, "bias is NULL");
+    CUDA_TRY(c, cudaMemcpyAsync(c->router_bias + (size_t)layer * c->cfg.n_experts, bias_host,
+                                sizeof(float) * c->cfg.n_experts, cudaMemcpyHostToDevice,
+                                static_cast<cudaStream_t>(stream)));
+    return MOE_OK;
+}
+
+extern "C" int moe_forward_decode(moe_ctx* c, int32_t layer, const float* x, int32_t B, float* y,
+                                  int32_t* topk_idx, float* topk_w, void* stream) {
+    if (!c) return fail(nullptr, MOE_EINVAL, "ctx is NULL");
+    int rc = check_layer(c, layer);
+    if (rc) return rc;
+    if (!x || !y || x == y) return fail(c, MOE_EINVAL, "x and y must be distinct device buffers");
+    if (B < 1 || B > c->cfg.max_batch) return fail(c, MOE_EINVAL, "B=%d outside 1..max_batch", B);
+    CUDA_TRY(c, cudaSetDevice(c->cfg.device));
+    return decode_layer(c, layer, x, B, y, topk_idx, topk_w, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int moe_forward_decode_stack(moe_ctx* c, int32_t layer0, int32_t n, const float* x, int32_t B,
+                                        float* y, float eps, float* x_trace, int32_t* idx_trace, float* y_trace,
+                                        void* stream) {
+    if (!c) return fail(nullptr, MOE_EINVAL, "ctx is NULL");
+    if (n < 1 || layer0 < 0 || layer0 + n > c->cfg.n_layers)
+        return fail(c, MOE_EINVAL, "layers %d..%d out of range", layer0, layer0 + n - 1);
+    for (int l = layer0; l < layer0 + n; ++l) {
+        int rc = check_layer(c, l);
+        if (rc) return rc;
+    }
+    if (!x || !y || x == y) return fail(c, MOE_EINVAL, "x and y must be distinct device buffers");
+    if (B < 1 || B > c->cfg.max_batch) return fail(c, MOE_EINVAL, "B=%d outside 1..max_batch", B);
+    if (!(eps > 0.0f)) return fail(c, MOE_EINVAL, "renorm_eps must be > 0");
+    CUDA_TRY(c, cudaSetDevice(c->cfg.device));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int H = c->cfg.hidden, k = c->cfg.top_k;
+    const size_t tok = (size_t)B * H;
+    if (c->resident && moe::stack_supported(c->sh, B)) {
+        moe::StackArgs a{};
+        a.layer0 = layer0;
+        a.n_layers = n;
+        a.B = B;
+        a.eps = eps;
+        a.x = x;
+        a.y = y;
+        a.x_trace = x_trace;
+        a.idx_trace = idx_trace;
+        a.y_trace = y_trace;
+        a.router_w = c->router_w;
+        a.router_bias = c->router_bias;
+        a.shared_gate = c->cfg.shared_inter > 0 ? c->shared_gate : nullptr;
+        a.dir = c->dir;
+        a.shared_pool = c->cfg.shared_inter > 0 ? c->shared_pool : nullptr;
+        a.shared_stride = c->shared_stride;
+        cudaError_t e = moe::launch_stack(c->sh, c->stack, a, st);
+        if (e != cudaSuccess) return fail(c, MOE_ECUDA, "decode stack launch failed: %s", cudaGetErrorString(e));
+        for (int l = layer0; l < layer0 + n; ++l) c->stats[l].calls++;
+        c->launches += 1;
+        return MOE_OK;
+    }
+    const float* xin = x;
+    for (int l = layer0; l < layer0 + n; ++l) {
+        const int i = l - layer0;
+        if (x_trace) {
+            CUDA_TRY(c, cudaMemcpyAsync(x_trace + i * tok, xin, tok * sizeof(float), cudaMemcpyDeviceToDevice, st));
+        }
+        float* yl = (l == layer0 + n - 1) ? y : (y_trace ? y_trace + i * tok : c->ybuf);
+        int rc = decode_layer(c, l, xin, B, yl, idx_trace ? idx_trace + (size_t)i * B * k : nullptr, nullptr, st);
+        if (rc) return rc;
+        if (l == layer0 + n - 1) {
+            if (y_trace) {
+                CUDA_TRY(c, cudaMemcpyAsync(y_trace + i * tok, y, tok * sizeof(float), cudaMemcpyDeviceToDevice, st));
+            }
+            break;
+        }
+        float* xn = c->xbuf + (size_t)(i & 1) * c->cfg.max_batch * H;
+        CUDA_TRY(c, moe::launch_renorm(yl, xn, B, H, eps, st));
+        c->launches += 1;
+        xin = xn;
+    }
+    return MOE_OK;
+}
+
+extern "C" int moe_forward_prefill(moe_ctx* c, int32_t layer, const float* x, int32_t T, float* y,
+                                   int32_t* topk_idx, float* topk_w, void* stream) {
+    if (!c) return fail(nullptr, MOE_EINVAL, "ctx is NULL");
+    int rc = check_layer(c, layer);
+    if (rc) return rc;
+    (void)x, (void)T, (void)y, (void)topk_idx, (void)topk_w, (void)stream;
+    return fail(c, MOE_ESTATE, "prefill is not available in this build");
+}
+
+extern "C" int moe_pool_stats(moe_ctx* c, int32_t layer, moe_pool_stats_t* out) {
+    if (!c || !out) return fail(c, MOE_EINVAL, "NULL argument");
+    const moe_config& g = c->cfg;
+    if (layer < -1 || layer >= g.n_layers) return fail(c, MOE_EINVAL, "layer %d out of range", layer);
+    std::memset(out, 0, sizeof *out);
+    std::vector<unsigned long long> hits(g.n_layers, 0);
+    if (c->resident && !c->poisoned) {
+        CUDA_TRY(c, cudaSetDevice(g.device));
+        CUDA_TRY(c, cudaDeviceSynchronize());
+        CUDA_TRY(c, cudaMemcpy(hits.data(), c->hits_dev, sizeof(unsigned long long) * g.n_layers,
+                               cudaMemcpyDeviceToHost));
+    }
+    if (!c->resident && c->side && !c->poisoned) {
+        CUDA_TRY(c, cudaStreamSynchronize(c->side));
+        harvest_copy_timing(c);
+    }
+    for (int l = 0; l < g.n_layers; ++l) {
+        if (layer >= 0 && l != layer) continue;
+        const LayerStats& S = c->stats[l];
+        out->hits += c->resident ? hits[l] : S.hits;
+        out->misses += S.misses;
+        out->evictions += S.evictions;
+        out->h2d_bytes += S.h2d_bytes;
+        out->h2d_ms += S.h2d_ms;
+        out->calls += S.calls;
+        out->resident += c->resident ? (c->loaded[l] ? g.n_experts : 0) : moe_slotpool_resident(c->pools[l]);
+    }
+    return MOE_OK;
+}
+
+extern "C" int moe_launch_count(moe_ctx* c, uint64_t* out) {
+    if (!c || !out) return fail(c, MOE_EINVAL, "NULL argument");
+    *out = c->launches;
+    return MOE_OK;
+}
+
+extern "C" int moe_pool_trace(moe_ctx* c, int32_t* buf, size_t cap, size_t* n_out) {
+    if (!c || !n_out) return fail(c, MOE_EINVAL, "NULL argument");
+    const size_t rows = c->trace.size() / 6;
+    *n_out = rows;
+    if (buf) std::memcpy(buf, c->trace.data(), sizeof(int32_t) * 6 * std::min(rows, cap));
+    return MOE_OK;
+}

@@ -1,0 +1,62 @@
+// moe_internal.h -- shared between the host runtime and the CUDA kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// Byte offsets of the six sections of one blob (layout v1, see moe.h).
+struct BlobLayout {
+    uint64_t gate_q, up_q, down_q, gate_sb, up_sb, down_sb, bytes;
+};
+
+__host__ __device__ inline BlobLayout blob_layout(int hidden, int rows, int bits) {
+    BlobLayout L;
+    uint64_t q = (uint64_t)rows * hidden * bits / 8;
+    uint64_t sb = (uint64_t)rows * (hidden / 64) * 4;
+    L.gate_q = 0;
+    L.up_q = q;
+    L.down_q = 2 * q;
+    L.gate_sb = 3 * q;
+    L.up_sb = 3 * q + sb;
+    L.down_sb = 3 * q + 2 * sb;
+    L.bytes = 3 * q + 3 * sb;
+    return L;
+}
+
+// Device-side routing/dispatch scratch of one decode call.  "Active experts"
+// are the distinct routed experts chosen by any token of the call (ascending
+// id) followed by the shared expert; each owns a contiguous run of "pairs"
+// (token, weight), tokens ascending within the run.
+struct Dispatch {
+    int32_t* n_act;        // [1]  routed active + 1 (shared)
+    int32_t* act_expert;   // [max_act] expert id, -1 = shared
+    const uint8_t** act_blob;  // [max_act] blob base address in HBM
+    int32_t* act_off;      // [max_act + 1] first pair of each active expert
+    int32_t* pair_token;   // [max_pairs]
+    float* pair_w;         // [max_pairs] routing weight (sigmoid gate for the shared expert)
+    int32_t* status;       // [1] device error word (0 = ok, 1 = routed to a non-resident expert)
+};
+
+struct Shapes {
+    int hidden, n_experts, top_k, inter, shared_inter, bits, norm_topk;
+    int max_act, max_pairs, h_stride;  // h_stride = max(inter, shared_inter)
+};
+
+// kernels (decode_kernels.cu)
+cudaError_t launch_router(const Shapes& s, const uint16_t* w_r, const float* bias, const float* x, int B,
+                          float* logits, cudaStream_t st);
+// mode bit 1 = top-k, bit 2 = dispatch
+cudaError_t launch_route_dispatch(const Shapes& s, int mode, const float* logits, const float* x,
+                                  const uint16_t* shared_gate_w, int B, int32_t* idx, float* w, float* sigma,
+                                  int32_t* user_idx, float* user_w, const uint8_t* const* dir_layer,
+                                  const uint8_t* shared_blob, Dispatch d, unsigned long long* hit_counter,
+                                  cudaStream_t st);
+cudaError_t launch_gateup(const Shapes& s, Dispatch d, const float* x, float* h, int B, cudaStream_t st);
+cudaError_t launch_down(const Shapes& s, Dispatch d, const float* h, float* y, int B, cudaStream_t st);
+cudaError_t launch_renorm(const float* y, float* x_next, int B, int hidden, float eps, cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,63 @@
+"""Load the seeded synthetic workloads (package ``synth``) into a context
+through the C ABI: draw and quantise each expert, pack it with
+``moe_pack_expert`` and hand whole layers to ``moe_load_experts``."""
+from __future__ import annotations
+
+import concurrent.futures as cf
+import os
+
+import numpy as np
+
+import synth
+
+from . import make_config, moe_blob_stride, moe_create, moe_load_experts, moe_pack_expert
+
+
+def _threads(n=None):
+    return n or max(1, os.cpu_count() or 1)
+
+
+def layer_blobs(w: "synth.Workload", layer: int, bits: int | None = None, threads: int | None = None,
+                out: np.ndarray | None = None):
+    """Packed routed blobs [E*stride] (uint8), the shared blob, router weights
+    (bf16 bits), shared-gate weights (bf16 bits) and router bias (fp32 or None)."""
+    bits = bits or w.bits
+    stride = moe_blob_stride(w.hidden, w.inter, bits)
+    E = w.n_experts
+    blobs = out if out is not None else np.empty(E * stride, np.uint8)
+    assert blobs.nbytes >= E * stride
+
+    def one(e):
+        d = synth.expert(w.seed, layer, e, w.hidden, w.inter, bits, w.sigma)
+        moe_pack_expert(w.hidden, w.inter, bits, d, out=blobs[e * stride:(e + 1) * stride])
+
+    with cf.ThreadPoolExecutor(_threads(threads)) as ex:
+        list(ex.map(one, range(E)))
+    shared = None
+    if w.shared_inter > 0:
+        shared = moe_pack_expert(w.hidden, w.shared_inter, bits,
+                                 synth.expert(w.seed, layer, synth.SHARED, w.hidden, w.shared_inter, bits, w.sigma))
+    wr, wsg, beta = synth.layer_inputs(w, layer)
+    return blobs[:E * stride], shared, wr, wsg, beta
+
+
+def config_for(w: "synth.Workload", bits: int | None = None, max_batch: int = 1, max_tokens: int = 0,
+               pool_slots: int | None = None, n_layers: int | None = None, **kw):
+    return make_config(n_layers or w.n_layers, w.hidden, w.n_experts, w.top_k, w.inter, w.shared_inter,
+                       bits=bits or w.bits,
+                       pool_slots=pool_slots if pool_slots is not None else (w.pool_slots or w.n_experts),
+                       max_batch=max_batch, max_tokens=max_tokens, **kw)
+
+
+def create_loaded(w: "synth.Workload", bits: int | None = None, max_batch: int = 1, max_tokens: int = 0,
+                  pool_slots: int | None = None, layers=None, threads: int | None = None, **kw):
+    """Create a context for workload w and load every layer (or `layers`)."""
+    bits = bits or w.bits
+    cfg = config_for(w, bits, max_batch, max_tokens, pool_slots, **kw)
+    ctx = moe_create(cfg)
+    stride = moe_blob_stride(w.hidden, w.inter, bits)
+    buf = np.empty(w.n_experts * stride, np.uint8)
+    for layer in (range(cfg.n_layers) if layers is None else layers):
+        blobs, shared, wr, wsg, beta = layer_blobs(w, layer, bits, threads, out=buf)
+        moe_load_experts(ctx, layer, blobs, stride, shared, wr, wsg, beta)
+    return ctx

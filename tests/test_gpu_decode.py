@@ -1,0 +1,231 @@
+"""Decode parity: the CUDA path through the C ABI against the CPU oracle on the
+tiny workload and its variants (batch sizes, int8, full-softmax weights, Zipf
+router bias, multi-layer stacks, streaming slot pool)."""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from _common import assert_close, oracle_layer, seed_with_gap
+
+torch = pytest.importorskip("torch")
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+import int4_expert_streaming_gb300 as moe  # noqa: E402
+from int4_expert_streaming_gb300 import workload  # noqa: E402
+
+TINY = synth.CONFIGS["tiny"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    moe.build()
+    moe.load_library()
+
+
+def _ctx(w, **kw):
+    return workload.create_loaded(w, **kw)
+
+
+def _decode(ctx, w, x_np, layer=0):
+    B = x_np.shape[0]
+    x = torch.from_numpy(x_np).cuda()
+    y = torch.empty_like(x)
+    idx = torch.empty((B, w.top_k), dtype=torch.int32, device="cuda")
+    wt = torch.empty((B, w.top_k), dtype=torch.float32, device="cuda")
+    moe.moe_forward_decode(ctx, layer, x, B, y, idx, wt, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    return y.cpu().numpy(), idx.cpu().numpy(), wt.cpu().numpy()
+
+
+def _check_layer(w, x_np, y, idx, wt, layer=0, norm_topk=True, orc=None):
+    orc = orc or oracle_layer(w, layer, norm_topk=norm_topk)
+    ref = orc.tokens(x_np)
+    assert np.array_equal(idx, ref["idx"]), (idx, ref["idx"])
+    np.testing.assert_allclose(wt, ref["w"], rtol=2e-6, atol=1e-7)
+    return assert_close(y, ref["y"])
+
+
+@pytest.mark.parametrize("B", [1, 3, 8])
+def test_tiny_decode_matches_oracle(B):
+    w = seed_with_gap(TINY, B)
+    ctx = _ctx(w, max_batch=B)
+    try:
+        x = synth.tokens(w.seed, 0, B, w.hidden)
+        _check_layer(w, x, *_decode(ctx, w, x))
+    finally:
+        moe.moe_destroy(ctx)
+
+
+def test_tiny_decode_max_batch_64_all_experts_active():
+    w = TINY
+    ctx = _ctx(w, max_batch=64)
+    try:
+        x = synth.tokens(w.seed, 1, 64, w.hidden)
+        y, idx, wt = _decode(ctx, w, x)
+        assert len(np.unique(idx)) == w.n_experts  # every expert is routed to by someone
+        _check_layer(w, x, y, idx, wt)
+    finally:
+        moe.moe_destroy(ctx)
+
+
+def test_tiny_decode_int8():
+    w = dataclasses.replace(seed_with_gap(TINY, 4), bits=8)
+    ctx = _ctx(w, max_batch=4)
+    try:
+        x = synth.tokens(w.seed, 0, 4, w.hidden)
+        _check_layer(w, x, *_decode(ctx, w, x))
+    finally:
+        moe.moe_destroy(ctx)
+
+
+def test_tiny_decode_full_softmax_weights():
+    w = seed_with_gap(TINY, 2)
+    ctx = _ctx(w, max_batch=2, norm_topk=False)
+    try:
+        x = synth.tokens(w.seed, 0, 2, w.hidden)
+        _check_layer(w, x, *_decode(ctx, w, x), norm_topk=False)
+    finally:
+        moe.moe_destroy(ctx)
+
+
+def test_tiny_decode_with_zipf_router_bias_and_wider_shapes():
+    """E = 64, k = 10, Zipf(1.1) bias, router weights ~ N(0, 1/H) (the 80B
+    recipe at tiny width), hidden 512, intermediate 192 (three groups)."""
+    w = dataclasses.replace(TINY, n_experts=64, top_k=10, hidden=512, inter=192, shared_inter=64,
+                            router_sigma=1.0 / np.sqrt(512), zipf_s=1.1)
+    w = seed_with_gap(w, 5)
+    ctx = _ctx(w, max_batch=5)
+    try:
+        x = synth.tokens(w.seed, 0, 5, w.hidden)
+        _check_layer(w, x, *_decode(ctx, w, x))
+    finally:
+        moe.moe_destroy(ctx)
+
+
+def test_tiny_stack_layer_by_layer():
+    """Three-layer stack with renormalisation: each layer checked against the
+    oracle fed the GPU's own layer input; the renormalisation checked too."""
+    w = dataclasses.replace(TINY, n_layers=3)
+    B = 4
+    ctx = _ctx(w, max_batch=B)
+    try:
+        x = torch.from_numpy(synth.tokens(w.seed, 0, B, w.hidden)).cuda()
+        y = torch.empty_like(x)
+        xt = torch.empty((3, B, w.hidden), device="cuda")
+        yt = torch.empty((3, B, w.hidden), device="cuda")
+        it = torch.empty((3, B, w.top_k), dtype=torch.int32, device="cuda")
+        moe.moe_forward_decode_stack(ctx, 0, 3, x, B, y, 1e-6, xt, it, yt, torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        xt, yt, it = xt.cpu().numpy(), yt.cpu().numpy(), it.cpu().numpy()
+        assert np.array_equal(xt[0], x.cpu().numpy())
+        assert np.array_equal(yt[2], y.cpu().numpy())
+        for l in range(3):
+            orc = oracle_layer(w, l)
+            ref = orc.tokens(xt[l])
+            assert np.array_equal(it[l], ref["idx"]), l
+            assert_close(yt[l], ref["y"], what=f"y layer {l}")
+            if l + 1 < 3:
+                assert_close(xt[l + 1], oracle.renorm(yt[l]), rel_l2=1e-6, max_abs_frac=1e-6, what="renorm")
+    finally:
+        moe.moe_destroy(ctx)
+
+
+def test_streaming_pool_trace_and_placement_invariance():
+    """A pool of 4 slots for 16 experts: the pool events equal the oracle pool
+    simulator replayed on the GPU's routing, and every output is bitwise equal
+    to the all-resident context's (an expert's answer does not depend on
+    whether it came from the pool or was just fetched from the host store)."""
+    w = TINY
+    B, steps = 2, 12
+    res = _ctx(w, max_batch=B)
+    st = _ctx(w, max_batch=B, pool_slots=4)
+    sim = oracle.PoolSim(4, w.n_experts)
+    try:
+        for step in range(steps):
+            x = synth.tokens(w.seed, 100 + step, B, w.hidden)
+            y0, i0, w0 = _decode(res, w, x)
+            y1, i1, w1 = _decode(st, w, x)
+            assert np.array_equal(i0, i1) and np.array_equal(y0, y1) and np.array_equal(w0, w1)
+            want = sim.request(i1.reshape(-1))
+            tr = moe.moe_pool_trace(st)
+            got = [tuple(r[2:]) for r in tr if r[0] == step]
+            assert got == want, step
+        s = moe.moe_pool_stats(st, 0)
+        tr = moe.moe_pool_trace(st)
+        assert s["hits"] == int((tr[:, 3] == 0).sum()) and s["misses"] == int((tr[:, 3] == 1).sum())
+        assert s["h2d_bytes"] == s["misses"] * moe.moe_blob_stride(w.hidden, w.inter, w.bits)
+        assert s["resident"] == 4 and s["calls"] == steps and s["evictions"] > 0
+        rs = moe.moe_pool_stats(res, 0)
+        assert rs["resident"] == w.n_experts and rs["misses"] == 0 and rs["hits"] == s["hits"] + s["misses"]
+    finally:
+        moe.moe_destroy(res)
+        moe.moe_destroy(st)
+
+
+def test_streaming_stack_matches_resident_stack():
+    w = dataclasses.replace(TINY, n_layers=2)
+    B = 3
+    res = _ctx(w, max_batch=B)
+    st = _ctx(w, max_batch=B, pool_slots=6, policy=moe.MOE_EVICT_LRU)
+    try:
+        for step in range(4):
+            x = torch.from_numpy(synth.tokens(w.seed, 7 + step, B, w.hidden)).cuda()
+            ya, yb = torch.empty_like(x), torch.empty_like(x)
+            moe.moe_forward_decode_stack(res, 0, 2, x, B, ya)
+            moe.moe_forward_decode_stack(st, 0, 2, x, B, yb)
+            torch.cuda.synchronize()
+            assert torch.equal(ya, yb)
+        assert moe.moe_pool_stats(st)["misses"] > 0
+    finally:
+        moe.moe_destroy(res)
+        moe.moe_destroy(st)
+
+
+def test_decode_argument_errors():
+    w = dataclasses.replace(TINY, n_layers=2)
+    ctx = workload.create_loaded(w, max_batch=2, layers=[0])
+    try:
+        x = torch.zeros((2, w.hidden), device="cuda")
+        y = torch.zeros_like(x)
+        for args, code in [((0, x, 0, y), moe.MOE_EINVAL), ((0, x, 3, y), moe.MOE_EINVAL),
+                           ((5, x, 1, y), moe.MOE_EINVAL), ((1, x, 1, y), moe.MOE_ESTATE),
+                           ((0, x, 1, x), moe.MOE_EINVAL)]:
+            with pytest.raises(moe.MoeError) as e:
+                moe.moe_forward_decode(ctx, *args)
+            assert e.value.code == code, args
+        moe.moe_forward_decode(ctx, 0, x, 2, y)  # still usable
+        torch.cuda.synchronize()
+    finally:
+        moe.moe_destroy(ctx)
+
+
+def test_injected_faults_fail_cleanly():
+    w = TINY
+    with pytest.raises(moe.MoeError) as e:
+        workload.create_loaded(w, pool_slots=4, fault_flags=moe.MOE_FAULT_PINNED_ALLOC)
+    assert e.value.code == moe.MOE_ENOMEM
+    x = torch.from_numpy(synth.tokens(w.seed, 0, 1, w.hidden)).cuda()
+    y = torch.empty_like(x)
+    ctx = workload.create_loaded(w, pool_slots=4, fault_flags=moe.MOE_FAULT_WAIT_TIMEOUT)
+    try:
+        with pytest.raises(moe.MoeError) as e:
+            moe.moe_forward_decode(ctx, 0, x, 1, y)
+        assert e.value.code == moe.MOE_ETIMEOUT
+        moe.moe_forward_decode(ctx, 0, x, 1, y)  # the timeout is not sticky
+        torch.cuda.synchronize()
+    finally:
+        moe.moe_destroy(ctx)
+    ctx = workload.create_loaded(w, pool_slots=4, fault_flags=moe.MOE_FAULT_MISS_COPY, fault_arg=1)
+    try:
+        with pytest.raises(moe.MoeError) as e:
+            moe.moe_forward_decode(ctx, 0, x, 1, y)
+        assert e.value.code == moe.MOE_ECUDA
+        with pytest.raises(moe.MoeError) as e:
+            moe.moe_forward_decode(ctx, 0, x, 1, y)
+        assert e.value.code == moe.MOE_ESTATE  # poisoned
+    finally:
+        moe.moe_destroy(ctx)
