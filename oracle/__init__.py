@@ -155,9 +155,12 @@ def shared_gate(w_sg: np.ndarray, x: np.ndarray) -> float:
 
 
 def renorm(y: np.ndarray, eps: float = 1e-6) -> np.ndarray:
+    """Row-wise (last axis) x = y / sqrt(mean(y^2) + eps)."""
     y = np.ascontiguousarray(y, np.float32)
     x = np.empty_like(y)
-    _load().orc_renorm(_p(y), y.shape[-1], eps, _p(x))
+    rows_y, rows_x = y.reshape(-1, y.shape[-1]), x.reshape(-1, y.shape[-1])
+    for r in range(rows_y.shape[0]):
+        _load().orc_renorm(_p(rows_y[r]), y.shape[-1], eps, _p(rows_x[r]))
     return x
 
 
