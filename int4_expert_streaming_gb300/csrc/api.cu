@@ -68,6 +68,7 @@ struct moe_ctx {
     float* ybuf = nullptr;  // [max_batch][H]
     void* disp_mem = nullptr;
     moe::Dispatch disp{};
+    moe::TokenDigits xd{};
     moe::StackScratch stack{};
 
     // host
@@ -141,6 +142,8 @@ int check_config(const moe_config* g) {
     if (g->top_k < 1 || g->top_k > 16 || g->top_k > g->n_experts)
         return fail(nullptr, MOE_EINVAL, "top_k must be in 1..min(16, n_experts)");
     if (g->inter < 64 || g->inter % 64) return fail(nullptr, MOE_EINVAL, "inter must be a positive multiple of 64");
+    if (g->inter * g->bits > 4096 || g->shared_inter * g->bits > 4096)
+        return fail(nullptr, MOE_EINVAL, "inter * bits must be <= 4096 (inter <= 1024 for int4, <= 512 for int8)");
     if (g->shared_inter < 0 || g->shared_inter % 64)
         return fail(nullptr, MOE_EINVAL, "shared_inter must be a multiple of 64");
     if (g->bits != 4 && g->bits != 8) return fail(nullptr, MOE_EINVAL, "bits must be 4 or 8");
@@ -257,16 +260,16 @@ int decode_layer(moe_ctx* c, int layer, const float* x, int B, float* y, int32_t
     c->launches += c->resident ? 4 : 5;
     if (c->resident) {
         CUDA_TRY(c, moe::launch_route_dispatch(s, 3, c->logits, x, wsg, B, c->idx, c->w, c->sigma, uidx, uw, dir,
-                                               shared_blob(c, layer), c->disp, c->hits_dev + layer, st));
+                                               shared_blob(c, layer), c->disp, c->xd, c->hits_dev + layer, st));
     } else {
         CUDA_TRY(c, moe::launch_route_dispatch(s, 1, c->logits, x, wsg, B, c->idx, c->w, c->sigma, uidx, uw, dir,
-                                               shared_blob(c, layer), c->disp, nullptr, st));
+                                               shared_blob(c, layer), c->disp, c->xd, nullptr, st));
         int rc = resolve_pool(c, layer, B, st);
         if (rc) return rc;
         CUDA_TRY(c, moe::launch_route_dispatch(s, 2, c->logits, x, wsg, B, c->idx, c->w, c->sigma, nullptr,
-                                               nullptr, dir, shared_blob(c, layer), c->disp, nullptr, st));
+                                               nullptr, dir, shared_blob(c, layer), c->disp, c->xd, nullptr, st));
     }
-    CUDA_TRY(c, moe::launch_gateup(s, c->disp, x, c->h, B, st));
+    CUDA_TRY(c, moe::launch_gateup(s, c->disp, c->xd, c->h, B, st));
     CUDA_TRY(c, moe::launch_down(s, c->disp, c->h, y, B, st));
     c->stats[layer].calls++;
     return MOE_OK;
@@ -302,6 +305,9 @@ extern "C" void moe_destroy(moe_ctx* c) {
     cudaFree(c->xbuf);
     cudaFree(c->ybuf);
     cudaFree(c->disp_mem);
+    cudaFree(c->xd.words);
+    cudaFree(c->xd.sums);
+    cudaFree(c->xd.exps);
     moe::stack_free(c->stack);
     if (c->store) cudaFreeHost(c->store);
     if (c->dir_host) cudaFreeHost(c->dir_host);
@@ -361,7 +367,10 @@ extern "C" int moe_create(const moe_config* cfg, moe_ctx** out) {
         (rc = dev_alloc(c, &c->idx, (size_t)Bm * k, "idx")) || (rc = dev_alloc(c, &c->w, (size_t)Bm * k, "w")) ||
         (rc = dev_alloc(c, &c->h, (size_t)s.max_pairs * s.h_stride, "h")) ||
         (rc = dev_alloc(c, &c->xbuf, (size_t)2 * Bm * H, "xbuf")) ||
-        (rc = dev_alloc(c, &c->ybuf, (size_t)Bm * H, "ybuf")))
+        (rc = dev_alloc(c, &c->ybuf, (size_t)Bm * H, "ybuf")) ||
+        (rc = dev_alloc(c, &c->xd.words, (size_t)Bm * H * 3 / 4, "token digits")) ||
+        (rc = dev_alloc(c, &c->xd.sums, (size_t)Bm * H / 16, "token digit sums")) ||
+        (rc = dev_alloc(c, &c->xd.exps, (size_t)Bm, "token exponents")))
         return bail(rc);
     // dispatch scratch in one allocation
     {
@@ -393,7 +402,7 @@ extern "C" int moe_create(const moe_config* cfg, moe_ctx** out) {
         return bail(MOE_ECUDA);
     }
     if (c->resident) {
-        rc = moe::stack_alloc(c->stack, s, L, Bm, c->err);
+        rc = moe::stack_alloc(c->stack, s, L, Bm, g.device, c->err);
         if (rc) return bail(rc);
     } else {
         if (g.fault_flags & MOE_FAULT_PINNED_ALLOC) {
@@ -516,7 +525,12 @@ extern "C" int moe_forward_decode_stack(moe_ctx* c, int32_t layer0, int32_t n, c
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int H = c->cfg.hidden, k = c->cfg.top_k;
     const size_t tok = (size_t)B * H;
-    if (c->resident && moe::stack_supported(c->sh, B)) {
+    if (c->resident && moe::stack_last_status(c->stack))
+        return fail(c, MOE_ETIMEOUT, "a device-side wait of an earlier decode-stack launch ran out (status %d)",
+                    moe::stack_last_status(c->stack)) == MOE_ETIMEOUT
+                   ? (c->poisoned = true, MOE_ETIMEOUT)
+                   : MOE_ETIMEOUT;
+    if (c->resident && moe::stack_supported(c->sh, c->stack, B)) {
         moe::StackArgs a{};
         a.layer0 = layer0;
         a.n_layers = n;

@@ -4,7 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/moe.h"
+#include "moe.h"
 
 namespace moe {
 
@@ -46,6 +46,14 @@ struct Shapes {
     int max_act, max_pairs, h_stride;  // h_stride = max(inter, shared_inter)
 };
 
+// Block-fixed-point digits of the decode tokens (see gemv.cuh), written by the
+// top-k kernel and read by the gate/up kernel.
+struct TokenDigits {
+    uint32_t* words;  // [max_batch][hidden/cols_per_chunk][digit words per chunk]
+    int32_t* sums;    // [max_batch][hidden/cols_per_chunk]
+    int32_t* exps;    // [max_batch]
+};
+
 // kernels (decode_kernels.cu)
 cudaError_t launch_router(const Shapes& s, const uint16_t* w_r, const float* bias, const float* x, int B,
                           float* logits, cudaStream_t st);
@@ -53,9 +61,9 @@ cudaError_t launch_router(const Shapes& s, const uint16_t* w_r, const float* bia
 cudaError_t launch_route_dispatch(const Shapes& s, int mode, const float* logits, const float* x,
                                   const uint16_t* shared_gate_w, int B, int32_t* idx, float* w, float* sigma,
                                   int32_t* user_idx, float* user_w, const uint8_t* const* dir_layer,
-                                  const uint8_t* shared_blob, Dispatch d, unsigned long long* hit_counter,
-                                  cudaStream_t st);
-cudaError_t launch_gateup(const Shapes& s, Dispatch d, const float* x, float* h, int B, cudaStream_t st);
+                                  const uint8_t* shared_blob, Dispatch d, TokenDigits xd,
+                                  unsigned long long* hit_counter, cudaStream_t st);
+cudaError_t launch_gateup(const Shapes& s, Dispatch d, TokenDigits xd, float* h, int B, cudaStream_t st);
 cudaError_t launch_down(const Shapes& s, Dispatch d, const float* h, float* y, int B, cudaStream_t st);
 cudaError_t launch_renorm(const float* y, float* x_next, int B, int hidden, float eps, cudaStream_t st);
 

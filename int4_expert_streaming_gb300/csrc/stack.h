@@ -8,7 +8,16 @@
 namespace moe {
 
 struct StackScratch {
-    void* mem = nullptr;
+    unsigned long long* lg_ll = nullptr;  // logits {value, epoch} words [2][8][E]
+    unsigned long long* h_ll = nullptr;   // SwiGLU outputs [2][hp][h_stride]
+    unsigned long long* y_ll = nullptr;   // layer outputs [2][8][H]
+    unsigned* sync = nullptr;             // [1] CTAs finished, [2] epoch base
+    int* status = nullptr;                // device status word (0 = ok)
+    int* status_host = nullptr;           // pinned, mapped: status of the last finished launch
+    int* status_host_dev = nullptr;       // device alias of status_host
+    int grid = 0;                         // CTAs of the cooperative launch
+    int max_smem = 0;                     // opt-in shared memory per CTA
+    int hp = 0;                           // pairs per parity of h_ll
 };
 
 struct StackArgs {
@@ -27,9 +36,12 @@ struct StackArgs {
     size_t shared_stride;
 };
 
-int stack_alloc(StackScratch& s, const Shapes& sh, int n_layers, int max_batch, std::string& err);
+int stack_alloc(StackScratch& s, const Shapes& sh, int n_layers, int max_batch, int device, std::string& err);
 void stack_free(StackScratch& s);
-bool stack_supported(const Shapes& sh, int B);
+bool stack_supported(const Shapes& sh, const StackScratch& s, int B);
+// Status of the last finished launch (read from mapped host memory, no sync):
+// 0 = ok, otherwise a device-side wait ran out.
+int stack_last_status(const StackScratch& s);
 cudaError_t launch_stack(const Shapes& sh, StackScratch& s, const StackArgs& a, cudaStream_t st);
 
 }  // namespace moe

@@ -229,3 +229,83 @@ def test_injected_faults_fail_cleanly():
         assert e.value.code == moe.MOE_ESTATE  # poisoned
     finally:
         moe.moe_destroy(ctx)
+
+
+@pytest.mark.parametrize("B,bits", [(1, 4), (2, 4), (5, 4), (8, 4), (1, 8), (8, 8), (12, 4)])
+def test_stack_kernel_equals_per_layer_kernels(B, bits):
+    """The persistent stack kernel (B <= 8, all resident) and the per-layer
+    kernels share one arithmetic: every layer's routing and output agree bit
+    for bit; and each layer matches the oracle fed the GPU's own layer input."""
+    w = dataclasses.replace(TINY, n_layers=3, bits=bits)
+    L = w.n_layers
+    ctx = _ctx(w, max_batch=B)
+    try:
+        x = torch.from_numpy(synth.tokens(w.seed, 3, B, w.hidden)).cuda()
+        y = torch.empty_like(x)
+        xt = torch.empty((L, B, w.hidden), device="cuda")
+        yt = torch.empty((L, B, w.hidden), device="cuda")
+        it = torch.empty((L, B, w.top_k), dtype=torch.int32, device="cuda")
+        n0 = moe.moe_launch_count(ctx)
+        moe.moe_forward_decode_stack(ctx, 0, L, x, B, y, 1e-6, xt, it, yt, torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        launches = moe.moe_launch_count(ctx) - n0
+        assert launches == (1 if B <= 8 else 4 * L + L - 1)
+        for l in range(L):
+            yl = torch.empty_like(x)
+            il = torch.empty((B, w.top_k), dtype=torch.int32, device="cuda")
+            moe.moe_forward_decode(ctx, l, xt[l].contiguous(), B, yl, il)
+            torch.cuda.synchronize()
+            assert torch.equal(il, it[l]), l
+            assert torch.equal(yl, yt[l]), l
+            ref = oracle_layer(w, l).tokens(xt[l].cpu().numpy())
+            assert np.array_equal(it[l].cpu().numpy(), ref["idx"])
+            assert_close(yt[l].cpu().numpy(), ref["y"], what=f"layer {l}")
+        assert torch.equal(y, yt[L - 1])
+    finally:
+        moe.moe_destroy(ctx)
+
+
+def test_stack_kernel_wider_shapes():
+    """Hidden 512, 64 experts top-10, intermediate 192 and shared 64 (ragged
+    chunk counts), Zipf router bias, 4 layers, B = 3."""
+    w = dataclasses.replace(TINY, n_layers=4, n_experts=64, top_k=10, hidden=512, inter=192, shared_inter=64,
+                            router_sigma=1.0 / np.sqrt(512), zipf_s=1.1)
+    B, L = 3, 4
+    ctx = _ctx(w, max_batch=B)
+    try:
+        x = torch.from_numpy(synth.tokens(w.seed, 0, B, w.hidden)).cuda()
+        y = torch.empty_like(x)
+        xt = torch.empty((L, B, w.hidden), device="cuda")
+        yt = torch.empty((L, B, w.hidden), device="cuda")
+        it = torch.empty((L, B, w.top_k), dtype=torch.int32, device="cuda")
+        moe.moe_forward_decode_stack(ctx, 0, L, x, B, y, 1e-6, xt, it, yt)
+        torch.cuda.synchronize()
+        for l in range(L):
+            ref = oracle_layer(w, l).tokens(xt[l].cpu().numpy())
+            assert np.array_equal(it[l].cpu().numpy(), ref["idx"]), l
+            assert_close(yt[l].cpu().numpy(), ref["y"], what=f"layer {l}")
+            if l + 1 < L:
+                assert_close(xt[l + 1].cpu().numpy(), oracle.renorm(yt[l].cpu().numpy()), rel_l2=1e-6,
+                             max_abs_frac=1e-6, what="renorm")
+    finally:
+        moe.moe_destroy(ctx)
+
+
+def test_stack_repeated_launches_are_deterministic():
+    """The barrier counters reset at the end of every launch: 50 launches in a
+    row give identical results and no device-side wait runs out."""
+    w = dataclasses.replace(TINY, n_layers=2)
+    ctx = _ctx(w, max_batch=2)
+    try:
+        x = torch.from_numpy(synth.tokens(w.seed, 9, 2, w.hidden)).cuda()
+        y0 = torch.empty_like(x)
+        moe.moe_forward_decode_stack(ctx, 0, 2, x, 2, y0)
+        y = torch.empty_like(x)
+        for _ in range(50):
+            moe.moe_forward_decode_stack(ctx, 0, 2, x, 2, y)
+        torch.cuda.synchronize()
+        assert torch.equal(y, y0)
+        moe.moe_forward_decode_stack(ctx, 0, 2, x, 2, y)  # would raise MOE_ETIMEOUT after a timed-out launch
+        torch.cuda.synchronize()
+    finally:
+        moe.moe_destroy(ctx)
