@@ -14,6 +14,7 @@ from __future__ import annotations
 
 import argparse
 import concurrent.futures as cf
+import dataclasses
 import json
 import os
 import subprocess
@@ -41,6 +42,7 @@ def parse_args():
     ap.add_argument("--config", default="35b", choices=["35b", "80b", "stress"])
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--bits", type=int, default=0)
+    ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling cases)")
     ap.add_argument("--cpu-samples", type=int, default=64, help="(token, layer) samples of the oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -201,6 +203,8 @@ def run_ours(args):
         pg = dist
     torch.cuda.set_device(local)
     w = synth.CONFIGS[args.config]
+    if args.layers:
+        w = dataclasses.replace(w, n_layers=args.layers)
     bits = args.bits or w.bits
     B = args.batch
     L, H, k = w.n_layers, w.hidden, w.top_k
