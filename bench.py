@@ -31,6 +31,8 @@ import synth  # noqa: E402
 
 METRIC = "MoE-stack decode tok/s; expert-weight HBM GB/s as fraction of GB300 peak"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1700.0
+PREFILL_METRIC = "MoE prefill tok/s; grouped-GEMM bf16 TFLOP/s as fraction of GB300 dense peak"
 
 
 def parse_args():
@@ -39,7 +41,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=2048)
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="35b", choices=["35b", "80b", "stress"])
+    ap.add_argument("--config", default="35b", choices=["35b", "80b", "80b-prefill", "stress"])
+    ap.add_argument("--tokens", type=int, default=0, help="prefill tokens per step (default: the workload's)")
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--bits", type=int, default=0)
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling cases)")
@@ -59,6 +62,18 @@ def peaks():
         d = json.load(open(p))
         return float(d.get("hbm_gbs", FALLBACK_HBM_GBS)), "measured"
     return FALLBACK_HBM_GBS, "fallback"
+
+
+def tensor_peak():
+    """Dense bf16 TFLOP/s for a kernel timed inside a long loop (sustained figure)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        if "bf16_tflops_sustained" in d:
+            return float(d["bf16_tflops_sustained"]), "measured (sustained)"
+        if "bf16_tflops" in d:
+            return float(d["bf16_tflops"]), "measured (burst)"
+    return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def workload_desc(w, B, bits):
@@ -297,10 +312,142 @@ def run_ours(args):
             pg.destroy_process_group()
 
 
+# --------------------------------------------------------------------------
+# prefill (one 80B-shaped layer, T tokens per step)
+# --------------------------------------------------------------------------
+def prefill_desc(w, T, bits):
+    return (f"{w.name}: one MoE layer, hidden {w.hidden}, {w.n_experts} experts top-{w.top_k}, expert inter "
+            f"{w.inter}, shared inter {w.shared_inter}, int{bits} group-64 affine, {T} tokens per step, "
+            "Zipf(1.1) router bias, tokens sorted per expert into tcgen05 grouped GEMMs, all experts resident")
+
+
+def prefill_cpu_baseline(w, bits, n_tokens):
+    """The oracle's prefill definition on n_tokens of the workload (one layer), all host cores."""
+    import oracle
+    threads = os.cpu_count() or 1
+    x = synth.tokens(w.seed, 900001, n_tokens, w.hidden)
+    wr, wsg, beta = synth.layer_inputs(w, 0)
+    router = oracle.Layer(w.hidden, w.n_experts, w.top_k, w.inter, w.shared_inter, wr, wsg, {}, router_bias=beta)
+    need = sorted({int(e) for t in range(n_tokens) for e in router.route(x[t])[1]})
+    with cf.ThreadPoolExecutor(threads) as ex:
+        experts = dict(zip(need, ex.map(lambda e: synth.expert(w.seed, 0, e, w.hidden, w.inter, bits, w.sigma), need)))
+    lay = oracle.Layer(w.hidden, w.n_experts, w.top_k, w.inter, w.shared_inter, wr, wsg, experts, router_bias=beta,
+                       shared=synth.expert(w.seed, 0, synth.SHARED, w.hidden, w.shared_inter, bits, w.sigma))
+    t0 = time.perf_counter()
+    lay.tokens(x, prefill=True, threads=threads)
+    secs = time.perf_counter() - t0
+    return {"value": n_tokens / secs, "unit": "tok/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n_tokens} tokens of the prefill layer through the fp64 scalar oracle (prefill definition: "
+                      f"bf16 weights and x), split over {threads} host threads; {secs:.1f} s wall"}
+
+
+def run_prefill(args):
+    import torch
+
+    import int4_expert_streaming_gb300 as moe
+    from int4_expert_streaming_gb300 import workload
+
+    rank, world, local = dist_env()
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        pg = dist
+    torch.cuda.set_device(local)
+    w = synth.CONFIGS[args.config]
+    bits = args.bits or w.bits
+    T = args.tokens or w.prefill_tokens
+    H, k = w.hidden, w.top_k
+    moe.build()
+    ctx = workload.create_loaded(w, bits, max_tokens=T)
+    try:
+        n_ring = 5  # 5 x T x H fp32 inputs: larger than L2 at the workload's T
+        X = torch.from_numpy(np.stack([synth.tokens(w.seed, s, T, H) for s in range(n_ring)])).cuda()
+        y = torch.empty((T, H), device="cuda")
+        st = torch.cuda.current_stream()
+        flop = 2.0 * T * k * 3 * H * w.inter + 2.0 * T * 3 * H * w.shared_inter
+        for s in range(args.warmup):
+            moe.moe_forward_prefill(ctx, 0, X[s % n_ring], T, y, None, None, st)
+        torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+        moe.moe_prefill_profile(ctx, True)
+        l0 = moe.moe_launch_count(ctx)
+        clk = ClockSampler(local)
+        clk.start()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(st)
+        for s in range(args.steps):
+            moe.moe_forward_prefill(ctx, 0, X[s % n_ring], T, y, None, None, st)
+        e1.record(st)
+        torch.cuda.synchronize()
+        clocks = clk.stop()
+        launches = moe.moe_launch_count(ctx) - l0
+        kms, calls = moe.moe_prefill_kernel_ms(ctx)
+        moe.moe_prefill_profile(ctx, False)
+        ms = e0.elapsed_time(e1)
+        if pg:
+            t = torch.tensor([ms])
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            ms = float(t.item())
+            pg.barrier()
+        secs = ms / 1e3
+        value = args.steps * T * world / secs
+        per_kernel = {n: v / calls for n, v in kms.items()}
+        gemm_ms = per_kernel["gateup_gemm"] + per_kernel["down_gemm"]
+        peak, peak_kind = tensor_peak()
+        achieved = flop / (gemm_ms / 1e3) / 1e12
+        e2e = None
+        if not args.no_e2e:
+            xh = torch.from_numpy(np.stack([synth.tokens(w.seed, s, T, H) for s in range(2)])).pin_memory()
+            yh = torch.empty((T, H)).pin_memory()
+            xd = torch.empty((T, H), device="cuda")
+            n_e2e = min(args.steps, 32)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for s in range(n_e2e):
+                xd.copy_(xh[s % 2], non_blocking=True)
+                moe.moe_forward_prefill(ctx, 0, xd, T, y, None, None, st)
+                yh.copy_(y, non_blocking=True)
+                st.synchronize()
+            e2e_s = time.perf_counter() - t0
+            e2e = {"value": n_e2e * T * world / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": T * H * 4,
+                   "d2h_bytes_per_step": T * H * 4, "steps": n_e2e}
+        line = {
+            "metric": PREFILL_METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": prefill_desc(w, T, bits), "tokens": T, "bits": bits,
+                       "parallelism": "replicas" if world > 1 else "single-gpu",
+                       "l2": "inputs larger than L2: 5 rotating token batches of "
+                             f"{T * H * 4 / 1e6:.1f} MB plus the touched experts' weights"},
+            "layer_tflops": flop / secs * args.steps / 1e12,
+            "kernel_ms": per_kernel,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "peak_kind": peak_kind, "traffic": None,
+                         "kernel": "grouped GEMMs (gate/up + down), algorithmic FLOPs 2*T*k*3*H*I + 2*T*3*H*I_s",
+                         "flops_per_launch": flop, "ms_per_launch": gemm_ms},
+            "gpu_launches": int(launches),
+            "clocks": clocks,
+            "e2e": e2e,
+        }
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = prefill_cpu_baseline(w, bits, 16)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+    finally:
+        moe.moe_destroy(ctx)
+        if pg:
+            pg.destroy_process_group()
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.config == "80b-prefill":
+        run_prefill(args)
     else:
         run_ours(args)
 

@@ -225,6 +225,22 @@ int moe_pool_stats(moe_ctx* ctx, int32_t layer, moe_pool_stats_t* out);
  */
 int moe_pool_trace(moe_ctx* ctx, int32_t* buf_host, size_t cap, size_t* n_out);
 
+/*
+ * Prefill kernel timing (diagnostics).  enable = 1: every later prefill call
+ * records a CUDA event on its stream before and after each of its kernels;
+ * enable = 0 stops recording.  moe_prefill_kernel_ms adds up, over the calls
+ * recorded since profiling was enabled, the device milliseconds of each
+ * kernel, in launch order:
+ *   [0] router logits  [1] top-k / weights / shared gate  [2] pair histogram
+ *   [3] scan + chunk list  [4] scatter  [5] gate/up grouped GEMM
+ *   [6] down grouped GEMM
+ * into ms_out[MOE_PREFILL_KERNELS] and the number of calls into *calls.
+ * Synchronises with the recorded events.
+ */
+#define MOE_PREFILL_KERNELS 7
+int moe_prefill_profile(moe_ctx* ctx, int32_t enable);
+int moe_prefill_kernel_ms(moe_ctx* ctx, double* ms_out, int64_t* calls);
+
 /* Number of CUDA kernels this context has launched so far (all entry points). */
 int moe_launch_count(moe_ctx* ctx, uint64_t* out);
 

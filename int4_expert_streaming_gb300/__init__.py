@@ -29,7 +29,7 @@ _ERRNAMES = {MOE_EINVAL: "MOE_EINVAL", MOE_ENOMEM: "MOE_ENOMEM", MOE_ECUDA: "MOE
 EXPORTS = (
     "moe_blob_bytes", "moe_blob_stride", "moe_pack_expert", "moe_create", "moe_destroy", "moe_load_experts",
     "moe_set_router_bias", "moe_forward_decode", "moe_forward_decode_stack", "moe_forward_prefill",
-    "moe_pool_stats", "moe_pool_trace", "moe_launch_count", "moe_last_error", "moe_slotpool_create", "moe_slotpool_destroy",
+    "moe_pool_stats", "moe_pool_trace", "moe_launch_count", "moe_prefill_profile", "moe_prefill_kernel_ms", "moe_last_error", "moe_slotpool_create", "moe_slotpool_destroy",
     "moe_slotpool_request",
 )
 
@@ -85,6 +85,8 @@ def load_library(path: str | None = None):
         lib.moe_pool_stats.argtypes = [vp, i32, c.POINTER(moe_pool_stats_t)]
         lib.moe_pool_trace.argtypes = [vp, vp, sz, c.POINTER(sz)]
         lib.moe_launch_count.argtypes = [vp, c.POINTER(c.c_uint64)]
+        lib.moe_prefill_profile.argtypes = [vp, i32]
+        lib.moe_prefill_kernel_ms.argtypes = [vp, c.POINTER(c.c_double), c.POINTER(c.c_int64)]
         lib.moe_last_error.argtypes = [vp]
         lib.moe_last_error.restype = c.c_char_p
         lib.moe_slotpool_create.argtypes = [i32, i32, i32, c.POINTER(vp)]
@@ -219,6 +221,21 @@ def moe_pool_trace(ctx) -> np.ndarray:
     buf = np.empty((n.value, 6), np.int32)
     _check(lib.moe_pool_trace(ctx, _ptr(buf) if n.value else None, n.value, ctypes.byref(n)), ctx)
     return buf
+
+
+PREFILL_KERNELS = ("router_logits", "select", "histogram", "scan", "scatter", "gateup_gemm", "down_gemm")
+
+
+def moe_prefill_profile(ctx, enable: bool = True) -> None:
+    _check(load_library().moe_prefill_profile(ctx, int(bool(enable))), ctx)
+
+
+def moe_prefill_kernel_ms(ctx) -> tuple:
+    """-> ({kernel name: accumulated device ms}, recorded calls)"""
+    ms = (ctypes.c_double * len(PREFILL_KERNELS))()
+    n = ctypes.c_int64()
+    _check(load_library().moe_prefill_kernel_ms(ctx, ms, ctypes.byref(n)), ctx)
+    return dict(zip(PREFILL_KERNELS, list(ms))), n.value
 
 
 def moe_launch_count(ctx) -> int:

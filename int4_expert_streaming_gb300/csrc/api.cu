@@ -28,6 +28,7 @@
 #include <vector>
 
 #include "moe_internal.h"
+#include "prefill.h"
 #include "stack.h"
 
 int32_t moe_slotpool_resident(const moe_slotpool* p);
@@ -70,6 +71,13 @@ struct moe_ctx {
     moe::Dispatch disp{};
     moe::TokenDigits xd{};
     moe::StackScratch stack{};
+    moe::PrefillScratch pre{};
+    // prefill kernel timing: a ring of event sets, harvested lazily
+    static constexpr int kProfRing = 32;
+    bool prof_on = false;
+    std::vector<cudaEvent_t> prof_ev;  // [kProfRing][kPrefillKernels + 1]
+    int64_t prof_calls = 0, prof_harvested = 0;
+    double prof_ms[moe::kPrefillKernels] = {};
 
     // host
     uint8_t* store = nullptr;
@@ -275,6 +283,26 @@ int decode_layer(moe_ctx* c, int layer, const float* x, int B, float* y, int32_t
     return MOE_OK;
 }
 
+// Adds the kernel times of recorded prefill call i (ring slot i % kProfRing).
+int prof_harvest_one(moe_ctx* c, int64_t i) {
+    cudaEvent_t* ev = c->prof_ev.data() + (size_t)(i % moe_ctx::kProfRing) * (moe::kPrefillKernels + 1);
+    CUDA_TRY(c, cudaEventSynchronize(ev[moe::kPrefillKernels]));
+    for (int k = 0; k < moe::kPrefillKernels; ++k) {
+        float ms = 0.0f;
+        CUDA_TRY(c, cudaEventElapsedTime(&ms, ev[k], ev[k + 1]));
+        c->prof_ms[k] += ms;
+    }
+    return MOE_OK;
+}
+
+int prof_harvest_all(moe_ctx* c) {
+    for (; c->prof_harvested < c->prof_calls; ++c->prof_harvested) {
+        int rc = prof_harvest_one(c, c->prof_harvested);
+        if (rc) return rc;
+    }
+    return MOE_OK;
+}
+
 }  // namespace
 
 // ===========================================================================
@@ -309,6 +337,8 @@ extern "C" void moe_destroy(moe_ctx* c) {
     cudaFree(c->xd.sums);
     cudaFree(c->xd.exps);
     moe::stack_free(c->stack);
+    moe::prefill_free(c->pre);
+    for (cudaEvent_t e : c->prof_ev) cudaEventDestroy(e);
     if (c->store) cudaFreeHost(c->store);
     if (c->dir_host) cudaFreeHost(c->dir_host);
     if (c->idx_host) cudaFreeHost(c->idx_host);
@@ -400,6 +430,14 @@ extern "C" int moe_create(const moe_config* cfg, moe_ctx** out) {
         cudaMemset(c->router_bias, 0, sizeof(float) * (size_t)L * E) != cudaSuccess) {
         c->err = "cudaMemset failed";
         return bail(MOE_ECUDA);
+    }
+    if (g.max_tokens > 0) {
+        if (!c->resident) {
+            c->err = "prefill (max_tokens > 0) needs an all-resident context (pool_slots == n_experts)";
+            return bail(MOE_EINVAL);
+        }
+        rc = moe::prefill_alloc(c->pre, s, g.max_tokens, g.device, c->err);
+        if (rc) return bail(rc);
     }
     if (c->resident) {
         rc = moe::stack_alloc(c->stack, s, L, Bm, g.device, c->err);
@@ -581,8 +619,42 @@ extern "C" int moe_forward_prefill(moe_ctx* c, int32_t layer, const float* x, in
     if (!c) return fail(nullptr, MOE_EINVAL, "ctx is NULL");
     int rc = check_layer(c, layer);
     if (rc) return rc;
-    (void)x, (void)T, (void)y, (void)topk_idx, (void)topk_w, (void)stream;
-    return fail(c, MOE_ESTATE, "prefill is not available in this build");
+    if (c->cfg.max_tokens <= 0) return fail(c, MOE_ESTATE, "context created without prefill (max_tokens = 0)");
+    if (T < 1 || T > c->cfg.max_tokens) return fail(c, MOE_EINVAL, "T=%d outside 1..max_tokens", T);
+    if (!x || !y || x == y) return fail(c, MOE_EINVAL, "x and y must be distinct device buffers");
+    if (const int st = moe::prefill_last_status(c->pre)) {
+        c->poisoned = true;
+        return fail(c, MOE_ETIMEOUT, "a device-side wait of an earlier prefill ran out (status %d)", st);
+    }
+    CUDA_TRY(c, cudaSetDevice(c->cfg.device));
+    const int E = c->cfg.n_experts, H = c->cfg.hidden;
+    moe::PrefillArgs a{};
+    a.T = T;
+    a.x = x;
+    a.y = y;
+    a.user_idx = topk_idx;
+    a.user_w = topk_w;
+    a.router_w = c->router_w + (size_t)layer * E * H;
+    a.router_bias = c->router_bias + (size_t)layer * E;
+    a.shared_gate = c->cfg.shared_inter > 0 ? c->shared_gate + (size_t)layer * H : nullptr;
+    a.dir = c->dir + (size_t)layer * E;
+    a.shared_blob = shared_blob(c, layer);
+    a.timeout_ns = (unsigned long long)std::min(timeout_ms(c), 1000) * 1000000ull;  // per device-side wait
+    cudaEvent_t* ev = nullptr;
+    if (c->prof_on) {
+        if (c->prof_calls - c->prof_harvested >= moe_ctx::kProfRing) {  // the slot about to be reused
+            int rc2 = prof_harvest_one(c, c->prof_harvested++);
+            if (rc2) return rc2;
+        }
+        ev = c->prof_ev.data() + (size_t)(c->prof_calls % moe_ctx::kProfRing) * (moe::kPrefillKernels + 1);
+        c->prof_calls++;
+    }
+    int n = 0;
+    cudaError_t e = moe::launch_prefill(c->sh, c->pre, a, static_cast<cudaStream_t>(stream), &n, ev);
+    c->launches += n;
+    if (e != cudaSuccess) return fail(c, MOE_ECUDA, "prefill launch failed: %s", cudaGetErrorString(e));
+    c->stats[layer].calls++;
+    return MOE_OK;
 }
 
 extern "C" int moe_pool_stats(moe_ctx* c, int32_t layer, moe_pool_stats_t* out) {
@@ -612,6 +684,34 @@ extern "C" int moe_pool_stats(moe_ctx* c, int32_t layer, moe_pool_stats_t* out) 
         out->calls += S.calls;
         out->resident += c->resident ? (c->loaded[l] ? g.n_experts : 0) : moe_slotpool_resident(c->pools[l]);
     }
+    return MOE_OK;
+}
+
+extern "C" int moe_prefill_profile(moe_ctx* c, int32_t enable) {
+    if (!c) return fail(nullptr, MOE_EINVAL, "ctx is NULL");
+    if (c->poisoned) return fail(c, MOE_ESTATE, "context poisoned by an earlier CUDA error");
+    CUDA_TRY(c, cudaSetDevice(c->cfg.device));
+    if (enable && c->prof_ev.empty()) {
+        c->prof_ev.assign((size_t)moe_ctx::kProfRing * (moe::kPrefillKernels + 1), nullptr);
+        for (auto& e : c->prof_ev) CUDA_TRY(c, cudaEventCreate(&e));
+    }
+    if (enable && !c->prof_on) {  // a fresh accumulation
+        int rc = prof_harvest_all(c);
+        if (rc) return rc;
+        for (double& v : c->prof_ms) v = 0.0;
+        c->prof_calls = c->prof_harvested = 0;
+    }
+    c->prof_on = enable != 0;
+    return MOE_OK;
+}
+
+extern "C" int moe_prefill_kernel_ms(moe_ctx* c, double* ms_out, int64_t* calls) {
+    if (!c || !ms_out || !calls) return fail(c, MOE_EINVAL, "NULL argument");
+    if (c->poisoned) return fail(c, MOE_ESTATE, "context poisoned by an earlier CUDA error");
+    int rc = prof_harvest_all(c);
+    if (rc) return rc;
+    for (int k = 0; k < moe::kPrefillKernels; ++k) ms_out[k] = c->prof_ms[k];
+    *calls = c->prof_calls;
     return MOE_OK;
 }
 

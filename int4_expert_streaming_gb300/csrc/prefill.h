@@ -1,0 +1,70 @@
+// prefill.h -- the prefill path: exact routing of T tokens, a counting sort of
+// the T*top_k (token, expert) pairs by expert, and two grouped GEMMs on the
+// tensor cores (gate/up + SwiGLU, then down + weighted scatter into y).
+#pragma once
+
+#include <string>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+// Chunk of sorted rows handled by one GEMM tile column block: {expert e (E =
+// the shared expert), first row row0 (sorted position for a routed expert,
+// token index for the shared one), n rows (1..kChunk), first row in the
+// SwiGLU buffers (each expert's rows start on a multiple of 16 there)}.
+constexpr int kChunk = 256;
+
+struct PrefillScratch {
+    int max_tokens = 0, n_hist = 0, max_chunks = 0;
+    float* logits = nullptr;      // [T][E]
+    uint16_t* x_bf = nullptr;     // [T][H] bf16(x)
+    int32_t* idx = nullptr;       // [T][k]
+    float* w = nullptr;           // [T][k]
+    float* sigma = nullptr;       // [T]
+    int32_t* local_rank = nullptr;  // [T*k] rank of a pair among the same expert's pairs of its histogram block
+    int32_t* cnt = nullptr;       // [E][n_hist] pairs per (expert, block), then their first sorted position
+    int32_t* offsets = nullptr;   // [E + 1]
+    int32_t* perm = nullptr;      // [T*k] sorted position -> pair id (token * k + slot)
+    int4* chunks = nullptr;       // [max_chunks] {e, row0, n, hrow0}
+    int32_t* n_chunks = nullptr;  // [1]
+    // SwiGLU output h = hi + lo (two bf16), rows: routed experts in sorted
+    // order then the shared expert, each expert padded to 16 rows; stored in
+    // planes of 64 columns [h_stride / 64][h_rows][64], each 128-byte row
+    // swizzled like a shared-memory MMA tile (chunk c at c ^ (row & 7)).
+    uint16_t* h_hi = nullptr;
+    uint16_t* h_lo = nullptr;
+    int h_rows = 0;
+    int* status_host = nullptr;   // pinned, mapped: 0 = ok, else a device-side wait ran out
+    int* status_dev = nullptr;    // device alias of status_host
+    int sms = 0;
+};
+
+struct PrefillArgs {
+    int T;
+    const float* x;              // [T][H]
+    float* y;                    // [T][H]
+    int32_t* user_idx;           // optional [T][k]
+    float* user_w;               // optional [T][k]
+    const uint16_t* router_w;    // [E][H] of the layer
+    const float* router_bias;    // [E]
+    const uint16_t* shared_gate; // [H] or NULL
+    const uint8_t* const* dir;   // [E] blob addresses of the layer
+    const uint8_t* shared_blob;  // or NULL
+    unsigned long long timeout_ns;
+};
+
+// Shapes the prefill kernels support (hidden <= 2048, multiples of 256;
+// inter and shared_inter multiples of 128).  Returns an empty string if ok.
+std::string prefill_check(const Shapes& s);
+int prefill_alloc(PrefillScratch& p, const Shapes& s, int max_tokens, int device, std::string& err);
+void prefill_free(PrefillScratch& p);
+int prefill_last_status(const PrefillScratch& p);
+// Enqueues the whole layer; returns the first launch error and the number of
+// kernels launched through *launches.  ev (optional, kPrefillKernels + 1
+// events) is recorded before the first kernel and after each kernel.
+constexpr int kPrefillKernels = 7;
+cudaError_t launch_prefill(const Shapes& s, PrefillScratch& p, const PrefillArgs& a, cudaStream_t st,
+                           int* launches, cudaEvent_t* ev = nullptr);
+
+}  // namespace moe

@@ -59,5 +59,5 @@ def create_loaded(w: "synth.Workload", bits: int | None = None, max_batch: int =
     buf = np.empty(w.n_experts * stride, np.uint8)
     for layer in (range(cfg.n_layers) if layers is None else layers):
         blobs, shared, wr, wsg, beta = layer_blobs(w, layer, bits, threads, out=buf)
-        moe_load_experts(ctx, layer, blobs, stride, shared, wr, wsg, beta)
+        moe_load_experts(ctx, layer, blobs, stride, shared, wr, wsg if shared is not None else None, beta)
     return ctx
