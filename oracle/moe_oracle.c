@@ -38,9 +38,14 @@
  *    reduction with offsets 16, 8, 4, 2, 1, then + bias.
  *  - Expert FFN: SwiGLU, h = silu(G x) * (U x), silu(z) = z / (1 + e^-z),
  *    out = D h.  Shared expert gated by sigmoid(w_sg . x).
- *  - Prefill mode emulates bf16 tensor-core operands: weights rounded to bf16
- *    after an fp32 fma(scale, q, bias), activations and the SwiGLU output
- *    rounded to bf16, products accumulated exactly (here in fp64).
+ *  - Prefill mode emulates the bf16 tensor-core operands of a grouped GEMM:
+ *    weights rounded to bf16 after an fp32 fma(scale, q, bias) and the token
+ *    activations rounded to bf16, products accumulated exactly (here in fp64).
+ *    The SwiGLU output h is not rounded: rounding it to one bf16 would make
+ *    the layer output jump by 2^-8 of an h element whenever the accumulation
+ *    order moves h across a bf16 rounding boundary, far outside the layer
+ *    tolerance, so the GPU path carries h as a pair of bf16 (hi + lo, h to
+ *    about 2^-17) and this definition keeps h exact.
  *
  * Build: gcc -O2 -ffp-contract=off (every fused multiply-add is an explicit
  * fmaf; nothing else is contracted).
@@ -206,7 +211,7 @@ static double silu(double z) { return z / (1.0 + exp(-z)); }
 
 /*
  * out = D (silu(G x) * (U x)), all in fp64 (decode mode), or with bf16
- * operands and fp64 accumulation (prefill mode).
+ * weights and x and fp64 accumulation (prefill mode).
  */
 static int expert_ffn(const orc_expert* e, int hidden, int inter, const float* x, int prefill, double* out) {
     double* wg = malloc(sizeof(double) * (size_t)inter * hidden);
@@ -236,7 +241,7 @@ static int expert_ffn(const orc_expert* e, int hidden, int inter, const float* x
             u += wu[(size_t)r * hidden + c] * xv[c];
         }
         double h = silu(a) * u;
-        hv[r] = prefill ? (double)bf16_round((float)h) : h;
+        hv[r] = h;
     }
     for (int j = 0; j < hidden; ++j) {
         double acc = 0.0;

@@ -339,19 +339,41 @@ def test_worked_example_row_dependent_down_and_other_column():
     assert np.allclose(out["y"], base * np.array(rows), rtol=1e-7, atol=0)
 
 
-def test_worked_example_prefill_mode():
-    """Prefill emulation on the same example: weights and x are already bf16-exact,
-    so the only rounding is h = bf16(silu(c) * u), worked out here with torch."""
-    v, layer, x = _worked_layer()
-    out = layer.token(x, prefill=True)
-
-    def hb(c, u):
-        return float(torch.tensor([_silu(c) * u], dtype=torch.float32).to(torch.bfloat16).float())
-    e = math.e
-    want = (e / (1 + e)) * 64 * v["d0"] * hb(v["c0"], v["u0"]) \
-        + (1 / (1 + e)) * 64 * v["d1"] * hb(v["c1"], v["u1"]) \
-        + (1 / (1 + math.exp(-v["g"]))) * 64 * v["ds"] * hb(v["cs"], v["us"])
-    assert np.allclose(out["y"], want, rtol=1e-7, atol=0)
+def test_worked_example_prefill_rounds_x_and_weights_only():
+    """Prefill emulation on the worked example with x0 = 1 + 2^-10 (fp32) and expert 0's
+    down value d0' = d0 (1 + 2^-10) (fp16-exact, not bf16-exact).  The expert FFNs see
+    bf16(x0) = 1 and bf16(d0') = d0; the router and the shared gate see the fp32 x0; the
+    SwiGLU output silu(c) u is used unrounded.  The decode definition sees x0 and d0'
+    as they are."""
+    v = _read_golden("worked_example.txt")
+    eps = 2.0 ** -10
+    H = 64
+    x0 = 1.0 + eps
+    d0p = v["d0"] * (1.0 + eps)
+    assert f16(d0p) != f16(v["d0"]) and bf16(d0p) == bf16(v["d0"])
+    rw = np.zeros((2, H), np.uint16)
+    rw[0, 0] = bf16(1.0)
+    wsg = np.zeros(H, np.uint16)
+    wsg[0] = bf16(v["g"])
+    experts = {0: _hand_expert(v["c0"], v["u0"], d0p), 1: _hand_expert(v["c1"], v["u1"], v["d1"])}
+    layer = oracle.Layer(H, 2, 2, 64, 64, rw, wsg, experts, shared=_hand_expert(v["cs"], v["us"], v["ds"]))
+    x = np.zeros(H, np.float32)
+    x[0] = x0
+    l0 = x0  # fp32 router logit of expert 0; expert 1's is 0
+    w0, w1 = math.exp(l0) / (math.exp(l0) + 1), 1 / (math.exp(l0) + 1)
+    sig = 1 / (1 + math.exp(-v["g"] * x0))
+    want_p = w0 * 64 * v["d0"] * v["u0"] * _silu(v["c0"]) \
+        + w1 * 64 * v["d1"] * v["u1"] * _silu(v["c1"]) \
+        + sig * 64 * v["ds"] * v["us"] * _silu(v["cs"])
+    want_d = w0 * 64 * d0p * v["u0"] * x0 * _silu(v["c0"] * x0) \
+        + w1 * 64 * v["d1"] * v["u1"] * x0 * _silu(v["c1"] * x0) \
+        + sig * 64 * v["ds"] * v["us"] * x0 * _silu(v["cs"] * x0)
+    p = layer.token(x, prefill=True)
+    d = layer.token(x)
+    assert list(p["idx"]) == [0, 1] and list(d["idx"]) == [0, 1]
+    assert np.allclose(p["y"], want_p, rtol=1e-12, atol=0)
+    assert np.allclose(d["y"], want_d, rtol=1e-12, atol=0)
+    assert abs(want_p - want_d) > 1e-4 * abs(want_d)  # the two definitions differ here
 
 
 # --------------------------------------------------------------------------
