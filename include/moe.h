@@ -209,6 +209,25 @@ int moe_forward_decode_stack(moe_ctx* ctx, int32_t layer0, int32_t n_layers, con
 int moe_forward_prefill(moe_ctx* ctx, int32_t layer, const float* x_dev, int32_t T, float* y_dev,
                         int32_t* topk_idx_dev, float* topk_w_dev, void* stream);
 
+/*
+ * Routing only, allocation-free: router logits, top-k and routing weights of
+ * B decode tokens of one layer (the same kernels and results as the routing
+ * inside moe_forward_decode), with all of its scratch in one fixed device
+ * array inside the library (256 KiB; no cudaMalloc or other allocation by
+ * the call).  The Swiftlet pages have no counterpart of this call.
+ *   x_dev fp32 [B x hidden]; topk_idx_dev int32 [B x top_k] and topk_w_dev
+ *   fp32 [B x top_k] receive the result (device, caller-owned, required).
+ * The scratch needs B*(n_experts + 2*top_k + 1)*4 bytes (each part rounded up
+ * to 256); a larger request fails with MOE_EINVAL before any GPU work.
+ * Nothing in the array has to start at zero: every element the kernels read
+ * is written earlier in the same call.  The first call on a device looks up
+ * the array's address (cudaGetSymbolAddress) and should therefore come before
+ * any stream capture.  The array is shared by all contexts of a device: calls
+ * that may overlap in time (other streams, other host threads) race on it.
+ */
+int moe_route_noalloc(moe_ctx* ctx, int32_t layer, const float* x_dev, int32_t B, int32_t* topk_idx_dev,
+                      float* topk_w_dev, void* stream);
+
 /* ------------------------------------------------------------------ */
 /* pool introspection                                                   */
 /* ------------------------------------------------------------------ */

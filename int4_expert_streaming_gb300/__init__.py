@@ -29,7 +29,7 @@ _ERRNAMES = {MOE_EINVAL: "MOE_EINVAL", MOE_ENOMEM: "MOE_ENOMEM", MOE_ECUDA: "MOE
 EXPORTS = (
     "moe_blob_bytes", "moe_blob_stride", "moe_pack_expert", "moe_create", "moe_destroy", "moe_load_experts",
     "moe_set_router_bias", "moe_forward_decode", "moe_forward_decode_stack", "moe_forward_prefill",
-    "moe_pool_stats", "moe_pool_trace", "moe_launch_count", "moe_prefill_profile", "moe_prefill_kernel_ms", "moe_last_error", "moe_slotpool_create", "moe_slotpool_destroy",
+    "moe_pool_stats", "moe_pool_trace", "moe_launch_count", "moe_prefill_profile", "moe_prefill_kernel_ms", "moe_route_noalloc", "moe_last_error", "moe_slotpool_create", "moe_slotpool_destroy",
     "moe_slotpool_request",
 )
 
@@ -86,6 +86,7 @@ def load_library(path: str | None = None):
         lib.moe_pool_trace.argtypes = [vp, vp, sz, c.POINTER(sz)]
         lib.moe_launch_count.argtypes = [vp, c.POINTER(c.c_uint64)]
         lib.moe_prefill_profile.argtypes = [vp, i32]
+        lib.moe_route_noalloc.argtypes = [vp, i32, vp, i32, vp, vp, vp]
         lib.moe_prefill_kernel_ms.argtypes = [vp, c.POINTER(c.c_double), c.POINTER(c.c_int64)]
         lib.moe_last_error.argtypes = [vp]
         lib.moe_last_error.restype = c.c_char_p
@@ -206,6 +207,11 @@ def moe_forward_prefill(ctx, layer: int, x, T: int, y, topk_idx=None, topk_w=Non
     _check(load_library().moe_forward_prefill(ctx, layer, _dev(x, "float32"), T, _dev(y, "float32"),
                                               _dev(topk_idx, "int32"), _dev(topk_w, "float32"), _stream(stream)),
            ctx)
+
+
+def moe_route_noalloc(ctx, layer: int, x, B: int, topk_idx, topk_w, stream=None):
+    _check(load_library().moe_route_noalloc(ctx, layer, _dev(x, "float32"), B, _dev(topk_idx, "int32"),
+                                            _dev(topk_w, "float32"), _stream(stream)), ctx)
 
 
 def moe_pool_stats(ctx, layer: int = -1) -> dict:

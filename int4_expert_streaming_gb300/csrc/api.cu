@@ -614,6 +614,41 @@ extern "C" int moe_forward_decode_stack(moe_ctx* c, int32_t layer0, int32_t n, c
     return MOE_OK;
 }
 
+extern "C" int moe_route_noalloc(moe_ctx* c, int32_t layer, const float* x, int32_t B, int32_t* topk_idx,
+                                 float* topk_w, void* stream) {
+    if (!c) return fail(nullptr, MOE_EINVAL, "ctx is NULL");
+    int rc = check_layer(c, layer);
+    if (rc) return rc;
+    if (!x || !topk_idx || !topk_w) return fail(c, MOE_EINVAL, "x, topk_idx and topk_w are required");
+    if (B < 1 || B > c->cfg.max_batch) return fail(c, MOE_EINVAL, "B=%d outside 1..max_batch", B);
+    const int E = c->cfg.n_experts, k = c->cfg.top_k, H = c->cfg.hidden;
+    // scratch: logits [B][E], idx [B][k], w [B][k], sigma [B]; each part 256-byte aligned
+    auto up = [](size_t n) { return (n + 255) / 256 * 256; };
+    const size_t lg_b = up(sizeof(float) * (size_t)B * E), ix_b = up(sizeof(int32_t) * (size_t)B * k),
+                 w_b = up(sizeof(float) * (size_t)B * k), sg_b = up(sizeof(float) * (size_t)B);
+    CUDA_TRY(c, cudaSetDevice(c->cfg.device));
+    void* base = nullptr;
+    size_t cap = 0;
+    CUDA_TRY(c, moe::noalloc_scratch(c->cfg.device, &base, &cap));
+    if (lg_b + ix_b + w_b + sg_b > cap)
+        return fail(c, MOE_EINVAL, "routing scratch of %zu bytes exceeds the fixed %zu-byte array", lg_b + ix_b + w_b + sg_b,
+                    cap);
+    uint8_t* p = static_cast<uint8_t*>(base);
+    float* lg = reinterpret_cast<float*>(p);
+    int32_t* ix = reinterpret_cast<int32_t*>(p + lg_b);
+    float* wt = reinterpret_cast<float*>(p + lg_b + ix_b);
+    float* sg = reinterpret_cast<float*>(p + lg_b + ix_b + w_b);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const uint16_t* wr = c->router_w + (size_t)layer * E * H;
+    const float* bias = c->router_bias + (size_t)layer * E;
+    const uint16_t* wsg = c->cfg.shared_inter > 0 ? c->shared_gate + (size_t)layer * H : nullptr;
+    CUDA_TRY(c, moe::launch_router(c->sh, wr, bias, x, B, lg, st));
+    CUDA_TRY(c, moe::launch_route_dispatch(c->sh, 1 | 4, lg, x, wsg, B, ix, wt, sg, topk_idx, topk_w, nullptr,
+                                           nullptr, c->disp, c->xd, nullptr, st));
+    c->launches += 2;
+    return MOE_OK;
+}
+
 extern "C" int moe_forward_prefill(moe_ctx* c, int32_t layer, const float* x, int32_t T, float* y,
                                    int32_t* topk_idx, float* topk_w, void* stream) {
     if (!c) return fail(nullptr, MOE_EINVAL, "ctx is NULL");

@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(1024) route_dispatch_kernel(
             }
             const float sg = wsg ? shared_gate(wsg, x + (size_t)t * H, H, lane) : 0.0f;
             if (lane == 0) sigma[t] = sg;
+            if (mode & 4) continue;  // routing only: no token digits
             const int nc = H / (s.bits == 4 ? 32 : 16);
             const int dwn = s.bits == 4 ? 24 : 12;
             if (s.bits == 4)

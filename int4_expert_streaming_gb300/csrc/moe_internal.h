@@ -57,7 +57,7 @@ struct TokenDigits {
 // kernels (decode_kernels.cu)
 cudaError_t launch_router(const Shapes& s, const uint16_t* w_r, const float* bias, const float* x, int B,
                           float* logits, cudaStream_t st);
-// mode bit 1 = top-k, bit 2 = dispatch
+// mode bit 1 = top-k, bit 2 = dispatch, bit 4 = skip the token digits (routing only)
 cudaError_t launch_route_dispatch(const Shapes& s, int mode, const float* logits, const float* x,
                                   const uint16_t* shared_gate_w, int B, int32_t* idx, float* w, float* sigma,
                                   int32_t* user_idx, float* user_w, const uint8_t* const* dir_layer,
@@ -66,5 +66,8 @@ cudaError_t launch_route_dispatch(const Shapes& s, int mode, const float* logits
 cudaError_t launch_gateup(const Shapes& s, Dispatch d, TokenDigits xd, float* h, int B, cudaStream_t st);
 cudaError_t launch_down(const Shapes& s, Dispatch d, const float* h, float* y, int B, cudaStream_t st);
 cudaError_t launch_renorm(const float* y, float* x_next, int B, int hidden, float eps, cudaStream_t st);
+
+// noalloc.cu: the fixed scratch array of moe_route_noalloc on `device`
+cudaError_t noalloc_scratch(int device, void** ptr, size_t* bytes);
 
 }  // namespace moe
