@@ -553,4 +553,46 @@ __device__ __forceinline__ void row_dot_h2(const uint8_t* q0, const uint32_t* sb
     r1 = p1;
 }
 
+// Two down rows at once when a row has exactly 16 chunks (int4, 512 columns):
+// lanes 0-15 take row q0, lanes 16-31 row q1, lane L holding chunk L & 15 of
+// h.  Each half reduces with the butterfly offsets 8, 4, 2, 1, the same pairs
+// as row_dot_h's 32-lane butterfly (whose offset-16 step adds the zeros of the
+// idle lanes), so each result equals row_dot_h of that row.  Returns the row
+// of this lane's half (r0 on lanes 0-15, r1 on lanes 16-31); lanes 0 and 16
+// hold the finished values.
+template <int BITS>
+__device__ __forceinline__ float row_dot_h_halves(const uint8_t* q0, const uint32_t* sb0, const uint8_t* q1,
+                                                  const uint32_t* sb1, const HF<BITS>& h, int lane) {
+    constexpr int CPG = 64 / Codes<BITS>::kCols;
+    const int c = lane & 15;
+    const uint8_t* q = lane < 16 ? q0 : q1;
+    const uint32_t* sb = lane < 16 ? sb0 : sb1;
+    const float A = chunk_dot_f(reinterpret_cast<const uint4*>(q)[c], h.v, Codes<BITS>{});
+    float v = chunk_term_f<BITS>(A, h.s, sb[c / CPG]);
+#pragma unroll
+    for (int off = 8; off >= 1; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(kFullMask, v, off));
+    return v;
+}
+
+// NP row pairs of row_dot_h_halves at once (rows q[2i] on lanes 0-15 and
+// q[2i+1] on lanes 16-31), their butterflies interleaved; v[i] equals
+// row_dot_h_halves of pair i.
+template <int BITS, int NP>
+__device__ __forceinline__ void row_dot_h_halves_n(const uint8_t* const (&q)[2 * NP], const uint32_t* const (&sb)[2 * NP],
+                                                   const HF<BITS>& h, int lane, float (&v)[NP]) {
+    constexpr int CPG = 64 / Codes<BITS>::kCols;
+    const int c = lane & 15, hi = lane >> 4;
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+        const uint8_t* qi = hi ? q[2 * i + 1] : q[2 * i];  // static indices: the arrays stay in registers
+        const uint32_t* si = hi ? sb[2 * i + 1] : sb[2 * i];
+        const float A = chunk_dot_f(reinterpret_cast<const uint4*>(qi)[c], h.v, Codes<BITS>{});
+        v[i] = chunk_term_f<BITS>(A, h.s, si[c / CPG]);
+    }
+#pragma unroll
+    for (int off = 8; off >= 1; off >>= 1)
+#pragma unroll
+        for (int i = 0; i < NP; ++i) v[i] = __fadd_rn(v[i], __shfl_xor_sync(kFullMask, v[i], off));
+}
+
 }  // namespace moe

@@ -40,7 +40,6 @@ namespace moe {
 namespace {
 
 constexpr int kST = 256, kSW = kST / 32;
-constexpr int kEPT = (1024 + kST - 1) / kST;  // experts per thread in the dispatch scan (E <= 1024)
 constexpr int kNSG = 4, kNSD = 2;  // gate/up stages, down stages
 constexpr int kMaxB = 8;
 constexpr int kNB = kNSG + kNSD + 2;  // mbarriers: G stages, D stages, prefetch[2]
@@ -134,58 +133,58 @@ __device__ __forceinline__ void ll_load2(const unsigned long long* p, unsigned l
     asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
 }
 
-// Re-poll one {value, epoch} pair until both carry ep (out of line: the slow
-// path).  Returns the pair; ok = 0 on timeout or abort.
-struct LLPair {
-    unsigned long long a, b;
-    int ok;
-};
-
-__device__ __noinline__ LLPair ll_wait_pair(const unsigned long long* src, uint32_t ep, int* status) {
-    const unsigned long long t0 = gtime();
-    unsigned spins = 0;
-    LLPair r;
-    r.ok = 1;
-    for (;;) {
-        ll_load2(src, r.a, r.b);
-        if ((uint32_t)(r.a >> 32) == ep && (uint32_t)(r.b >> 32) == ep) return r;
-        if (spin_abort(status, spins, t0)) {
-            r.ok = 0;
-            return r;
-        }
-        __nanosleep(32);
-    }
-}
-
-// Poll n words (n even, 16-byte aligned) until each carries epoch ep; the
-// values go to out[].  Loads are issued in batches of 8 before any is checked.
-// Returns false on timeout or abort.
-__device__ bool ll_read(const unsigned long long* src, int n, uint32_t ep, float* out, int tid,
-                                     int nthreads, int* status) {
-    for (int base = 2 * tid; base < n; base += 16 * nthreads) {
-        unsigned long long a[8], b[8];
+// Poll the first `cols` words of rows row0 .. row0+nrows-1 of an exchange
+// buffer (row stride `stride` words) until each carries epoch ep; the values
+// go to dst[(row - row0) * stride + col].  cols and stride are even.  All
+// threads take part; each polls batches of 8 word pairs, re-issuing the whole
+// batch until every pair carries ep (a rolled loop: this runs once per
+// exchange and its code size matters more than its arithmetic).  Returns false
+// on timeout or abort.
+__device__ bool ll_read_rows(const unsigned long long* base, int row0, int nrows, int stride, int cols, uint32_t ep,
+                             float* dst, int tid, int nthreads, int* status) {
+    const int n = nrows * cols;
+    const unsigned long long* b0 = base + (size_t)row0 * stride;
+    for (int b = 2 * tid; b < n; b += 16 * nthreads) {
+        int off[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-            const int i = base + 2 * nthreads * q;
-            a[q] = b[q] = (unsigned long long)ep << 32;
-            if (i < n) ll_load2(src + i, a[q], b[q]);
+            const int i = b + 2 * nthreads * q;
+            const int r = i / cols;
+            off[q] = i < n ? r * stride + (i - r * cols) : -1;
         }
+        unsigned long long a[8], c[8];
+        unsigned spins = 0;
+        unsigned long long t0 = 0;
+        for (;;) {
+            bool all = true;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int i = base + 2 * nthreads * q;
-            if ((uint32_t)(a[q] >> 32) != ep || (uint32_t)(b[q] >> 32) != ep) {
-                const LLPair r = ll_wait_pair(src + i, ep, status);
-                if (!r.ok) return false;
-                a[q] = r.a;
-                b[q] = r.b;
+            for (int q = 0; q < 8; ++q) {
+                a[q] = c[q] = (unsigned long long)ep << 32;
+                if (off[q] >= 0) ll_load2(b0 + off[q], a[q], c[q]);
             }
-            if (i < n) {
-                out[i] = __uint_as_float((uint32_t)a[q]);
-                out[i + 1] = __uint_as_float((uint32_t)b[q]);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                all = all && (uint32_t)(a[q] >> 32) == ep && (uint32_t)(c[q] >> 32) == ep;
+            if (all) break;
+            if (!t0) t0 = gtime();
+            if (spin_abort(status, spins, t0)) return false;
+            __nanosleep(32);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            if (off[q] >= 0) {
+                dst[off[q]] = __uint_as_float((uint32_t)a[q]);
+                dst[off[q] + 1] = __uint_as_float((uint32_t)c[q]);
             }
         }
     }
     return true;
+}
+
+// n contiguous words (n even)
+__device__ __forceinline__ bool ll_read(const unsigned long long* src, int n, uint32_t ep, float* out, int tid,
+                                        int nthreads, int* status) {
+    return ll_read_rows(src, 0, 1, n, n, ep, out, tid, nthreads, status);
 }
 
 // ---------------------------------------------------------------------------
@@ -199,7 +198,6 @@ struct Disp {
     float rs[kMaxB];
     int xe[kMaxB];         // block-fixed-point exponent of each token's x
     float xmax[kMaxB];     // max |x| of each token
-    uint32_t keys[kMaxB][16];
     float red[2 * kRenormThreads / 32];
     int n_act, n_routed, n_pairs, pad;
 };
@@ -325,31 +323,6 @@ __device__ void issue_down(const Params& p, const Lists& D, int aa, int ab, int 
     }
 }
 
-// inclusive block scan of one int per thread (kST threads)
-__device__ int block_scan(int v, int* wsum) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(kFullMask, v, off);
-        if (lane >= off) v += o;
-    }
-    if (lane == 31) wsum[warp] = v;
-    __syncthreads();
-    if (warp == 0) {
-        int s = lane < kSW ? wsum[lane] : 0;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int o = __shfl_up_sync(kFullMask, s, off);
-            if (lane >= off) s += o;
-        }
-        if (lane < kSW) wsum[lane] = s;
-    }
-    __syncthreads();
-    if (warp > 0) v += wsum[warp - 1];
-    __syncthreads();
-    return v;
-}
-
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
@@ -357,13 +330,11 @@ template <int BITS, int NPER>
 __global__ void __launch_bounds__(kST, 1) stack_kernel(const Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ uint64_t mbar[kNB];
-    __shared__ int s_wsum[32];
     uint64_t* mbG = mbar;
     uint64_t* mbD = mbar + kNSG;
     uint64_t* mbP = mbar + kNSG + kNSD;
 
     static_assert(kST == kRenormThreads, "the renormalisation order is defined for kRenormThreads threads");
-    static_assert((1024 + kSW - 1) / kSW <= 128, "top-k slices hold at most 128 logits");
     constexpr int CC = Codes<BITS>::kCols, DW = Codes<BITS>::kDigitWords;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x, G = gridDim.x;
@@ -432,37 +403,58 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const Params p) {
             }
         }
         __syncthreads();
-        if (l != p.layer0)
-            for (int i = tid; i < B * H; i += kST) xs[i] = __fmul_rn(xs[i], ds->rs[i / H]);
-        // block fixed point of each token: exponent from max |x|, then digits
+        // x = y * r (from the second layer on) and its block-fixed-point digits,
+        // one pass: a warp covers 32 consecutive columns of one token (one int4
+        // chunk, two int8 chunks); the digit words are assembled with shuffles
+        // in the layout of bfp_chunk and stored whole.
         {
             if (tid < B) ds->xe[tid] = bfp_exponent(ds->xmax[tid]);
             __syncthreads();
-            uint8_t* xb = reinterpret_cast<uint8_t*>(xdw);
+            const bool scale = l != p.layer0;
             for (int i = tid; i < B * H; i += kST) {
                 const int t = i / H, col = i - t * H;
-                const int V = bfp_int(xs[i], ds->xe[t]);
+                float xv = xs[i];
+                if (scale) {
+                    xv = __fmul_rn(xv, ds->rs[t]);
+                    xs[i] = xv;
+                }
+                const int V = bfp_int(xv, ds->xe[t]);
                 uint32_t d0, d1, d2;
                 bfp_digits(V, d0, d1, d2);
-                const int ch = col / CC, pos = col - ch * CC;
-                uint8_t* cw = xb + ((size_t)(t * nc + ch) * DW) * 4;
+                const uint32_t dig = d0 | (d1 << 8) | (d2 << 16);
                 if (BITS == 4) {
-                    const int wi = pos >> 3, b8 = pos & 7, odd = b8 & 1, by = b8 >> 1;
-                    cw[(6 * wi + 0 + odd) * 4 + by] = (uint8_t)d0;
-                    cw[(6 * wi + 2 + odd) * 4 + by] = (uint8_t)d1;
-                    cw[(6 * wi + 4 + odd) * 4 + by] = (uint8_t)d2;
+                    // word L = 6 cw + 2 j + odd: digit j of columns 8 cw + 2 b + odd, b = 0..3
+                    const int Lw = lane < 24 ? lane : 0;
+                    const int cw = Lw / 6, r = Lw - 6 * cw, j = r >> 1, odd = r & 1;
+                    const uint32_t g0 = __shfl_sync(kFullMask, dig, 8 * cw + 0 + odd);
+                    const uint32_t g1 = __shfl_sync(kFullMask, dig, 8 * cw + 2 + odd);
+                    const uint32_t g2 = __shfl_sync(kFullMask, dig, 8 * cw + 4 + odd);
+                    const uint32_t g3 = __shfl_sync(kFullMask, dig, 8 * cw + 6 + odd);
+                    const uint32_t sel = (uint32_t)j | ((uint32_t)(j + 4) << 4);
+                    const uint32_t word = __byte_perm(__byte_perm(g0, g1, sel), __byte_perm(g2, g3, sel), 0x5410);
+                    const int ch = col / CC;
+                    if (lane < 24) xdw[(size_t)(t * nc + ch) * DW + lane] = word;
                     const int S = __reduce_add_sync(kFullMask, V);
                     if (lane == 0) xS[t * nc + ch] = S;
                 } else {
-                    const int wi = pos >> 2, by = pos & 3;
-                    cw[(3 * wi + 0) * 4 + by] = (uint8_t)d0;
-                    cw[(3 * wi + 1) * 4 + by] = (uint8_t)d1;
-                    cw[(3 * wi + 2) * 4 + by] = (uint8_t)d2;
+                    // per half-warp chunk: word 3 cw + j = digit j of columns 4 cw + b, b = 0..3
+                    const int hb = lane & 16, L = lane & 15;
+                    const int Lw = L < 12 ? L : 0;
+                    const int cw = Lw / 3, j = Lw - 3 * cw;
+                    const uint32_t g0 = __shfl_sync(kFullMask, dig, hb + 4 * cw + 0);
+                    const uint32_t g1 = __shfl_sync(kFullMask, dig, hb + 4 * cw + 1);
+                    const uint32_t g2 = __shfl_sync(kFullMask, dig, hb + 4 * cw + 2);
+                    const uint32_t g3 = __shfl_sync(kFullMask, dig, hb + 4 * cw + 3);
+                    const uint32_t sel = (uint32_t)j | ((uint32_t)(j + 4) << 4);
+                    const uint32_t word = __byte_perm(__byte_perm(g0, g1, sel), __byte_perm(g2, g3, sel), 0x5410);
+                    const int ch = col / CC;
+                    if (L < 12) xdw[(size_t)(t * nc + ch) * DW + L] = word;
                     const int S = lane < 16 ? __reduce_add_sync(0x0000ffffu, V) : __reduce_add_sync(0xffff0000u, V);
-                    if ((lane & 15) == 0) xS[t * nc + ch] = S;
+                    if (L == 0) xS[t * nc + ch] = S;
                 }
             }
         }
+        __syncthreads();
         if (p.x_trace && c == 0)
             for (int i = tid; i < B * H; i += kST) p.x_trace[(size_t)li * B * H + i] = xs[i];
         if (!stage_wait(mbar, kNSG + kNSD + par, wt, p)) {
@@ -508,14 +500,17 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const Params p) {
             }
         }
         // ------------------------------------------------------------ phase B
-        float* s_lg = reinterpret_cast<float*>(Gbuf);  // temp area, before the stage copies
-        int* s_cnt = reinterpret_cast<int*>(Gbuf + r16i(B * E * 4));
-        unsigned long long* s_msk = reinterpret_cast<unsigned long long*>(Gbuf + r16i(B * E * 4) + r16i(E * 4));
-        int* s_scan = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(s_msk) + (size_t)E * 8);
-        for (int e = tid; e < E; e += kST) {
-            s_cnt[e] = 0;
-            s_msk[e] = 0ull;
-        }
+        // Routing by ranks (no serial selection loop).  Temp area in the
+        // gate/up stages, before this layer's copies land there.
+        const int C = kSW * k;  // top-k candidates per token (k from each warp's slice)
+        uint8_t* tp = Gbuf;
+        float* s_lg = reinterpret_cast<float*>(tp);  // [B][E] logits
+        tp += r16i(B * E * 4);
+        uint32_t* s_key = reinterpret_cast<uint32_t*>(tp);  // [B][E] order keys
+        tp += r16i(B * E * 4);
+        uint32_t* c_key = reinterpret_cast<uint32_t*>(tp);  // [B][C]
+        tp += r16i(B * C * 4);
+        int32_t* c_idx = reinterpret_cast<int32_t*>(tp);  // [B][C], -1 = empty
         {
             const bool got = ll_read(p.lg_ll + (size_t)par * kMaxB * E, B * E, ep, s_lg, tid, kST, p.status);
             if (!__syncthreads_and(got ? 1 : 0)) {
@@ -523,101 +518,135 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const Params p) {
                 break;
             }
         }
-        // top-k in two levels: every warp selects the k best of its slice of each
-        // token's logits, then one warp per token selects among the candidates
+        for (int i = tid; i < B * E; i += kST) s_key[i] = order_key(s_lg[i]);
+        for (int i = tid; i < B * C; i += kST) c_idx[i] = -1;
+        __syncthreads();
+        // level 1: each warp selects the k best keys of its slice of every
+        // token (key desc, index asc; <= 4 keys per lane), one per round: a
+        // warp max of the lanes' best keys, then the lowest index among the
+        // lanes holding it.  The slice's picks become candidates in order.
         {
-            uint32_t* ck = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(s_scan) + r16i(E * 4));
-            int32_t* ci = reinterpret_cast<int32_t*>(ck + kMaxB * kSW * 16);
-            uint32_t* kk_all = reinterpret_cast<uint32_t*>(ci + kMaxB * kSW * 16);
-            int32_t* ii_all = reinterpret_cast<int32_t*>(kk_all + kSW * 128);
-            const int eb = (int)((long long)E * warp / kSW), ee = (int)((long long)E * (warp + 1) / kSW);
-            const int nsl = ee - eb, kk = min(k, nsl);
+            const int S = ((E + kSW - 1) / kSW + 31) / 32 * 32;  // slice of whole warp-rows
+            const int sb = warp * S, se = min(E, sb + S), M1 = S / 32;
             for (int t = 0; t < B; ++t) {
-                uint32_t keys[4];
-                int32_t ids[4];
+                uint32_t key[4];
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
-                    const int i = lane + 32 * m;
-                    keys[m] = i < nsl ? order_key(s_lg[t * E + eb + i]) : 0u;
-                    ids[m] = eb + i;
+                    const int j = sb + lane + 32 * m;
+                    key[m] = (m < M1 && j < se) ? s_key[t * E + j] : 0u;
                 }
-                // stage the slice as candidate arrays for warp_select
-                uint32_t* sk = ck + (t * kSW + warp) * 16;
-                int32_t* si = ci + (t * kSW + warp) * 16;
-                uint32_t* wk = kk_all + warp * 128;
-                int32_t* wi = ii_all + warp * 128;
+#pragma unroll 1
+                for (int r = 0; r < k; ++r) {
+                    uint32_t best = key[0];
+                    int bm = 0;
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    wk[lane + 32 * m] = keys[m];
-                    wi[lane + 32 * m] = ids[m];
+                    for (int m = 1; m < 4; ++m)
+                        if (key[m] > best) best = key[m], bm = m;
+                    const uint32_t mx = __reduce_max_sync(kFullMask, best);
+                    const uint32_t jw = __reduce_min_sync(
+                        kFullMask, (best == mx && mx != 0u) ? (uint32_t)(sb + lane + 32 * bm) : 0xffffffffu);
+                    if (jw == 0xffffffffu) break;  // the slice has fewer than k keys
+                    if (lane == 0) {
+                        c_key[t * C + warp * k + r] = mx;
+                        c_idx[t * C + warp * k + r] = (int)jw;
+                    }
+                    const int lw = (int)(jw - sb) & 31, mw = (int)(jw - sb) >> 5;
+#pragma unroll
+                    for (int m = 0; m < 4; ++m)
+                        if (lane == lw && m == mw) key[m] = 0u;
                 }
-                __syncwarp();
-                warp_select<4>(wk, wi, nsl, kk, lane, si, sk);
-                if (lane >= kk && lane < 16) {
-                    sk[lane] = 0u;
-                    si[lane] = 0x7fffffff;
-                }
-                __syncwarp();
             }
-            __syncthreads();
-            if (warp < B) {
-                const int t = warp;
-                warp_select<(kSW * 16 + 31) / 32>(ck + t * kSW * 16, ci + t * kSW * 16, kSW * 16, k, lane, ds->idx[t],
-                                                   ds->keys[t]);
-                if (lane < k) ds->val[t][lane] = s_lg[t * E + ds->idx[t][lane]];
-                __syncwarp();
-                topk_weights(s_lg + t * E, E, k, p.norm_topk, lane, ds->val[t], ds->w[t]);
-            }
-            __syncthreads();
         }
+        __syncthreads();
+        // level 2 (one warp per token): the same selection over the token's
+        // candidates (<= 4 per lane), ties to the lower expert index; then the
+        // routing weights
+        if (warp < B) {
+            const int t = warp;
+            uint32_t key[4];
+            int id[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int j = lane + 32 * m;
+                const int ij = j < C ? c_idx[t * C + j] : -1;
+                key[m] = ij >= 0 ? c_key[t * C + j] : 0u;
+                id[m] = ij >= 0 ? ij : 0x7fffffff;
+            }
+#pragma unroll 1
+            for (int r = 0; r < k; ++r) {
+                uint32_t best = key[0];
+                int bi = id[0];
+#pragma unroll
+                for (int m = 1; m < 4; ++m)
+                    if (key[m] > best || (key[m] == best && id[m] < bi)) best = key[m], bi = id[m];
+                const uint32_t mx = __reduce_max_sync(kFullMask, best);
+                const int w = (int)__reduce_min_sync(kFullMask, best == mx ? (uint32_t)bi : 0xffffffffu);
+                if (lane == 0) {
+                    ds->idx[t][r] = w;
+                    ds->val[t][r] = s_lg[t * E + w];
+                }
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                    if (id[m] == w) key[m] = 0u, id[m] = 0x7fffffff;
+            }
+            __syncwarp();
+            topk_weights(s_lg + t * E, E, k, p.norm_topk, lane, ds->val[t], ds->w[t]);
+        }
+        __syncthreads();
         if (p.idx_trace && c == 0 && tid < B * k) p.idx_trace[(size_t)li * B * k + tid] = ds->idx[tid / k][tid % k];
-        for (int q = tid; q < B * k; q += kST) {
-            const int e = ds->idx[q / k][q % k], t = q / k;
-            atomicAdd(&s_cnt[e], 1);
-            atomicOr(&s_msk[e], 1ull << t);
+        // dispatch (warp 0): pairs sorted by (expert, token) by rank (pair key
+        // expert << 3 | token), then active experts in ascending id
+        const int nq = B * k;
+        if (warp == 0) {
+            for (int m = 0; m * 32 < nq; ++m) {
+                const int q = lane + 32 * m;
+                const uint32_t kq = q < nq ? ((uint32_t)ds->idx[q / k][q % k] << 3) | (uint32_t)(q / k) : 0xffffffffu;
+                int rank = 0;
+                for (int mm = 0; mm * 32 < nq; ++mm) {
+                    const int qb = lane + 32 * mm;
+                    const uint32_t kb =
+                        qb < nq ? ((uint32_t)ds->idx[qb / k][qb % k] << 3) | (uint32_t)(qb / k) : 0xffffffffu;
+                    const int lim = min(32, nq - 32 * mm);
+#pragma unroll 4
+                    for (int s2 = 0; s2 < lim; ++s2) rank += __shfl_sync(kFullMask, kb, s2) < kq ? 1 : 0;
+                }
+                if (q < nq) {
+                    D.pair_act[rank] = (int)kq;  // the sorted keys, replaced by active indices below
+                    D.pair_w[rank] = ds->w[q / k][q % k];
+                }
+            }
+            __syncwarp();
+            int base = 0;
+            uint32_t prev = 0xffffffffu;
+            for (int m = 0; m * 32 < nq; ++m) {
+                const int pr = lane + 32 * m;
+                const uint32_t kq = pr < nq ? (uint32_t)D.pair_act[pr] : 0xffffffffu;
+                uint32_t kp = __shfl_up_sync(kFullMask, kq, 1);
+                if (lane == 0) kp = prev;
+                const bool first = pr < nq && (kp == 0xffffffffu || (kp >> 3) != (kq >> 3));
+                const unsigned bal = __ballot_sync(kFullMask, first);
+                const int a = base + __popc(bal & (0xffffffffu >> (31 - lane))) - 1;
+                prev = __shfl_sync(kFullMask, kq, 31);
+                __syncwarp();
+                if (pr < nq) {
+                    const int e = (int)(kq >> 3);
+                    D.pair_token[pr] = (int)(kq & 7u);
+                    D.pair_act[pr] = a;
+                    if (first) {
+                        D.act_expert[a] = e;
+                        D.act_blob[a] = p.dir[(size_t)l * E + e];
+                        D.act_off[a] = pr;
+                    }
+                }
+                base += __popc(bal);
+            }
+            if (lane == 0) ds->n_routed = base;
         }
         __syncthreads();
-        {
-            int v[kEPT], tot = 0;
-#pragma unroll
-            for (int q = 0; q < kEPT; ++q) {
-                const int e = tid * kEPT + q;
-                v[q] = e < E ? ((s_cnt[e] << 16) | (s_cnt[e] > 0 ? 1 : 0)) : 0;
-                tot += v[q];
-            }
-            const int incl = block_scan(tot, s_wsum);
-            int run = incl - tot;
-#pragma unroll
-            for (int q = 0; q < kEPT; ++q) {
-                const int e = tid * kEPT + q;
-                if (e < E) s_scan[e] = run;
-                run += v[q];
-            }
-            if (tid == kST - 1) {
-                ds->n_routed = incl & 0xffff;
-                ds->n_pairs = B * k + (p.Is > 0 ? B : 0);
-                ds->n_act = (incl & 0xffff) + (p.Is > 0 ? 1 : 0);
-            }
-        }
-        __syncthreads();
-        for (int e = tid; e < E; e += kST) {
-            if (s_cnt[e] > 0) {
-                const int a = s_scan[e] & 0xffff;
-                D.act_expert[a] = e;
-                D.act_blob[a] = p.dir[(size_t)l * E + e];
-                D.act_off[a] = s_scan[e] >> 16;
-            }
-        }
-        for (int q = tid; q < B * k; q += kST) {
-            const int e = ds->idx[q / k][q % k], t = q / k;
-            const int rank = __popcll(s_msk[e] & ((1ull << t) - 1ull));
-            const int pr = (s_scan[e] >> 16) + rank;
-            D.pair_token[pr] = t;
-            D.pair_w[pr] = ds->w[t][q % k];
-            D.pair_act[pr] = s_scan[e] & 0xffff;
-        }
         if (tid == 0) {
             const int nr = ds->n_routed;
+            ds->n_pairs = B * k + (p.Is > 0 ? B : 0);
+            ds->n_act = nr + (p.Is > 0 ? 1 : 0);
             if (p.Is > 0) {
                 D.act_expert[nr] = -1;
                 D.act_blob[nr] = p.shared_pool + (size_t)l * p.shared_stride;
@@ -638,7 +667,7 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const Params p) {
         const int U = ds->n_routed * p.I;
         const int u0 = (int)((long long)U * c / G), u1 = (int)((long long)U * (c + 1) / G);
         const int mine = u1 - u0;
-        const int gcs = mine > 0 ? min(p.g_cap, (mine + kNSG - 1) / kNSG) : 1;
+        const int gcs = mine > 0 ? min(p.g_cap, max(2 * kSW, (mine + kNSG - 1) / kNSG)) : 1;
         const int n_gch = (mine + gcs - 1) / gcs;
         const int dcs = min(p.d_cap, (n_act + kNSD - 1) / kNSD);
         const int n_dch = jn > 0 ? (n_act + dcs - 1) / dcs : 0;
@@ -698,7 +727,6 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const Params p) {
         }
         if (!ok) break;
         // ------------------------------------------------------------ phase C
-        const int half = (jn + 1) / 2;
         for (int ch = 0; ch < n_dch && ok; ++ch) {
             const int s = ch % kNSD;
             if (!stage_wait(mbar, kNSG + s, wt, p)) {
@@ -708,64 +736,70 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const Params p) {
             const uint8_t* st = Dbuf + (size_t)s * dstage;
             const int aa = ch * dcs, ab = min(n_act, aa + dcs);
             const int pa = D.act_off[aa], pb = D.act_off[ab];
+            // h of the pairs, into the (idle) gate/up stage area: all pairs at the
+            // first stage when they fit, else this stage's pairs
+            const bool all_h = (long long)n_pairs * p.h_stride * 4 <= (long long)kNSG * gstage;
+            const int ha = all_h ? 0 : pa, hb = all_h ? n_pairs : pb;
+            float* hs = reinterpret_cast<float*>(Gbuf) - (size_t)ha * p.h_stride;  // hs[pr * h_stride + col]
+            if (!all_h || ch == 0) {
+                const int nrt = max(0, min(hb, B * k) - ha);  // routed pairs (cols I), then shared pairs (cols Is)
+                bool okh = ll_read_rows(hll, ha, nrt, p.h_stride, p.I, ep, hs + (size_t)ha * p.h_stride, tid, kST,
+                                        p.status);
+                if (okh && hb > ha + nrt)
+                    okh = ll_read_rows(hll, ha + nrt, hb - ha - nrt, p.h_stride, p.Is, ep,
+                                       hs + (size_t)(ha + nrt) * p.h_stride, tid, kST, p.status);
+                if (!__syncthreads_and(okh ? 1 : 0)) {
+                    ok = false;
+                    break;
+                }
+            }
             bool okc = true;
-            // tasks: (pair, half of this CTA's rows)
-            for (int task = warp; task < 2 * (pb - pa); task += kSW) {
-                const int pr = pa + (task >> 1), hf = task & 1;
+            // tasks: (pair, group of kRG of this CTA's rows)
+            constexpr int kRG = 8;
+            const int ngr = (jn + kRG - 1) / kRG;
+            for (int task = warp; task < (pb - pa) * ngr; task += kSW) {
+                const int pr = pa + task / ngr, g0 = (task % ngr) * kRG;
                 const int a = D.pair_act[pr];
                 const int cols = D.act_expert[a] < 0 ? p.Is : p.I;
                 const uint32_t rb = (uint32_t)cols * BITS / 8, dsb = (uint32_t)cols / 16;
                 const uint8_t* unit = st + (size_t)(a - aa) * p.d_unit;
                 const uint8_t* sbase = unit + p.d_rows_bytes + ((j0 * dsb) & 15u);
-                // h of the pair: lane L polls its chunk's CC words, 8 loads in flight at a time
                 HF<BITS> hd;
-                float* hv = hd.v;
-                const bool mine_c = lane < cols / CC;
-                const unsigned long long* src = hll + (size_t)pr * p.h_stride + lane * CC;
+                const bool halves = BITS == 4 && cols == 16 * CC;
+                const float* hrow = hs + (size_t)pr * p.h_stride + (halves ? (lane & 15) : lane) * CC;
+                if (halves || lane < cols / CC) {
 #pragma unroll
-                for (int i0 = 0; i0 < CC; i0 += 16) {
-                    unsigned long long wa[8], wb[8];
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        wa[q] = wb[q] = (unsigned long long)ep << 32;
-                        if (mine_c) ll_load2(src + i0 + 2 * q, wa[q], wb[q]);
+                    for (int i = 0; i < CC; i += 4) {
+                        const float4 v = *reinterpret_cast<const float4*>(hrow + i);
+                        hd.v[i] = v.x, hd.v[i + 1] = v.y, hd.v[i + 2] = v.z, hd.v[i + 3] = v.w;
                     }
+                } else {
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        if (okc && ((uint32_t)(wa[q] >> 32) != ep || (uint32_t)(wb[q] >> 32) != ep)) {
-                            const LLPair r = ll_wait_pair(src + i0 + 2 * q, ep, p.status);
-                            okc = r.ok != 0;
-                            wa[q] = r.a;
-                            wb[q] = r.b;
-                        }
-                        hv[i0 + 2 * q] = mine_c ? __uint_as_float((uint32_t)wa[q]) : 0.0f;
-                        hv[i0 + 2 * q + 1] = mine_c ? __uint_as_float((uint32_t)wb[q]) : 0.0f;
-                    }
-                }
-                if (__any_sync(kFullMask, !okc)) {
-                    okc = false;
-                    break;
+                    for (int i = 0; i < CC; ++i) hd.v[i] = 0.0f;
                 }
                 hf_sum(hd);
                 const float wp = D.pair_w[pr];
-                const int jb = hf * half, je = min(jn, jb + half);
-                int jj = jb;
-                for (; jj + 1 < je; jj += 2) {
-                    float v0, v1;
-                    row_dot_h2<BITS>(unit + (size_t)jj * rb, reinterpret_cast<const uint32_t*>(sbase + (size_t)jj * dsb),
-                                     unit + (size_t)(jj + 1) * rb,
-                                     reinterpret_cast<const uint32_t*>(sbase + (size_t)(jj + 1) * dsb), hd, cols, lane, v0,
-                                     v1);
-                    if (lane == 0) {
-                        part[(size_t)pr * p.jn + jj] = __fmul_rn(wp, v0);
-                        part[(size_t)pr * p.jn + jj + 1] = __fmul_rn(wp, v1);
+                const int je = min(jn, g0 + kRG);
+                if (halves) {
+                    // 16 chunks per row: two rows per pass, one per half-warp
+#pragma unroll 1
+                    for (int jj = g0; jj < je; jj += 2) {
+                        const int j1 = min(jj + 1, je - 1);  // an odd tail repeats its row in the upper half
+                        const float v = row_dot_h_halves<BITS>(
+                            unit + (size_t)jj * rb, reinterpret_cast<const uint32_t*>(sbase + (size_t)jj * dsb),
+                            unit + (size_t)j1 * rb, reinterpret_cast<const uint32_t*>(sbase + (size_t)j1 * dsb), hd,
+                            lane);
+                        const int jo = jj + (lane >> 4);
+                        if ((lane & 15) == 0 && jo < je) part[(size_t)pr * p.jn + jo] = __fmul_rn(wp, v);
                     }
-                }
-                if (jj < je) {
-                    const float v = row_dot_h<BITS>(unit + (size_t)jj * rb,
-                                                    reinterpret_cast<const uint32_t*>(sbase + (size_t)jj * dsb), hd,
-                                                    cols, lane);
-                    if (lane == 0) part[(size_t)pr * p.jn + jj] = __fmul_rn(wp, v);
+                } else {
+#pragma unroll 1
+                    for (int jj = g0; jj < je; ++jj) {
+                        const float v = row_dot_h<BITS>(unit + (size_t)jj * rb,
+                                                        reinterpret_cast<const uint32_t*>(sbase + (size_t)jj * dsb), hd,
+                                                        cols, lane);
+                        if (lane == 0) part[(size_t)pr * p.jn + jj] = __fmul_rn(wp, v);
+                    }
                 }
             }
             fence_proxy_async();
@@ -860,10 +894,14 @@ bool plan(const Shapes& sh, int B, int grid, int max_smem, Params& p) {
     const int budget = max_smem - 1024;  // static shared memory of the kernel
     int left = budget - off;
     p.d_cap = std::max(1, std::min((k + 2 + kNSD - 1) / kNSD, left / 3 / (kNSD * p.d_unit)));
-    const int dbytes = kNSD * p.d_cap * p.d_unit;
+    const int dbytes = kNSD * p.d_cap * p.d_unit;  // sized before any reduction of d_cap below
     left -= dbytes;
     p.g_cap = left / (kNSG * p.g_unit);
     if (p.g_cap < 1) return false;
+    // phase C stages the h of a down stage's pairs (<= d_cap * B + B) in the gate/up area
+    while (p.d_cap > 1 && (long long)(p.d_cap * B + B) * sh.h_stride * 4 > (long long)kNSG * p.g_cap * p.g_unit)
+        --p.d_cap;
+    if ((long long)(p.d_cap * B + B) * sh.h_stride * 4 > (long long)kNSG * p.g_cap * p.g_unit) return false;
     p.off_G = off;
     off += kNSG * p.g_cap * p.g_unit;
     off = r128(off);
@@ -872,7 +910,7 @@ bool plan(const Shapes& sh, int B, int grid, int max_smem, Params& p) {
     p.smem_bytes = off;
     // the top-k temp area lives in the gate/up stages
     const long long tmp =
-        r16i(B * E * 4) + r16i(E * 4) + (long long)E * 8 + r16i(E * 4) + 2LL * kMaxB * kSW * 16 * 4 + 2LL * kSW * 128 * 4;
+        2LL * r16i(B * E * 4) + 2LL * r16i(B * kSW * k * 4);
     if (tmp > (long long)kNSG * p.g_cap * p.g_unit) return false;
     return off <= budget;
 }
