@@ -38,7 +38,7 @@ PREFILL_METRIC = "MoE prefill tok/s; grouped-GEMM bf16 TFLOP/s as fraction of GB
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2048)
+    ap.add_argument("--steps", type=int, default=0, help="timed steps (default: 2048 decode, 1024 stress, 50 prefill)")
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="35b", choices=["35b", "80b", "80b-prefill", "stress"])
@@ -442,12 +442,168 @@ def run_prefill(args):
             pg.destroy_process_group()
 
 
+# --------------------------------------------------------------------------
+# streaming stress (pool of 128 of 512 slots per layer, store in pinned host memory)
+# --------------------------------------------------------------------------
+def host_link_probe_gbs(nbytes: int = 1 << 30) -> float:
+    """Pinned host -> device copy bandwidth (one cudaMemcpyAsync per copy)."""
+    import torch
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        d.copy_(h, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(5):
+        d.copy_(h, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    gbs = 5 * nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9
+    del h, d
+    return gbs
+
+
+def run_stress(args):
+    import torch
+
+    import int4_expert_streaming_gb300 as moe
+    from int4_expert_streaming_gb300 import workload
+
+    rank, world, local = dist_env()
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        pg = dist
+    torch.cuda.set_device(local)
+    w = synth.CONFIGS["stress"]
+    if args.layers:
+        w = dataclasses.replace(w, n_layers=args.layers)
+    bits = args.bits or w.bits
+    L, H, k = w.n_layers, w.hidden, w.top_k
+    moe.build()
+    link_peak = host_link_probe_gbs()
+    ctx = workload.create_loaded(w, bits, max_batch=1)
+    try:
+        drift = workload.Drift(w)
+        n_ring = 256
+        X = torch.from_numpy(np.stack([synth.tokens(w.seed, s, 1, H) for s in range(n_ring)])).cuda()
+        y = torch.empty((1, H), device="cuda")
+        st = torch.cuda.current_stream()
+        stride = moe.moe_blob_stride(H, w.inter, bits)
+        sblob = moe.moe_blob_bytes(H, w.shared_inter, bits) if w.shared_inter else 0
+        step = 0
+        at64 = None
+
+        def one_step():
+            nonlocal step, at64
+            if step > 0:
+                drift.advance(ctx, st)
+            moe.moe_forward_decode_stack(ctx, 0, L, X[step % n_ring], 1, y, 1e-6, None, None, None, st)
+            step += 1
+            if step == 64:
+                at64 = moe.moe_pool_stats(ctx)
+
+        for _ in range(args.warmup):
+            one_step()
+        torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+        s0 = moe.moe_pool_stats(ctx)
+        l0 = moe.moe_launch_count(ctx)
+        clk = ClockSampler(local)
+        clk.start()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(st)
+        for _ in range(args.steps):
+            one_step()
+        e1.record(st)
+        torch.cuda.synchronize()
+        clocks = clk.stop()
+        launches = moe.moe_launch_count(ctx) - l0
+        ms = e0.elapsed_time(e1)
+        s1 = moe.moe_pool_stats(ctx)
+        if pg:
+            t = torch.tensor([ms])
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            ms = float(t.item())
+            pg.barrier()
+        secs = ms / 1e3
+        value = args.steps * world / secs
+
+        def rate(a, b):
+            h, m = b["hits"] - (a["hits"] if a else 0), b["misses"] - (a["misses"] if a else 0)
+            return h / max(1, h + m)
+
+        h2d = s1["h2d_bytes"] - s0["h2d_bytes"]
+        h2d_ms = s1["h2d_ms"] - s0["h2d_ms"]
+        expert_bytes = L * (k * stride + sblob)  # batch 1: k distinct routed experts + the shared one per layer
+        peak, peak_kind = peaks()
+        gbs = expert_bytes * args.steps / secs / 1e9
+        e2e = None
+        if not args.no_e2e:
+            xh = torch.from_numpy(np.stack([synth.tokens(w.seed, s, 1, H) for s in range(n_ring)])).pin_memory()
+            yh = torch.empty((1, H)).pin_memory()
+            xd = torch.empty((1, H), device="cuda")
+            n_e2e = min(args.steps, 64)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for i in range(n_e2e):
+                xd.copy_(xh[(step + i) % n_ring], non_blocking=True)
+                drift.advance(ctx, st)
+                moe.moe_forward_decode_stack(ctx, 0, L, xd, 1, y, 1e-6, None, None, None, st)
+                yh.copy_(y, non_blocking=True)
+                st.synchronize()
+            step += n_e2e
+            e2e_s = time.perf_counter() - t0
+            e2e = {"value": n_e2e * world / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": H * 4,
+                   "d2h_bytes_per_step": H * 4, "steps": n_e2e}
+        line = {
+            "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": (f"stress: {L}-layer 80B-shaped decode stack, int{bits} group-64, batch 1, "
+                                    f"{w.pool_slots} of {w.n_experts} slots per layer in HBM, full store in pinned "
+                                    f"host memory, Zipf(1.1) routing with {w.drift_swaps} adjacent-rank swaps per "
+                                    "layer per step, misses by cudaMemcpyAsync on a side stream, pool starts cold"),
+                       "batch": 1, "layers": L, "bits": bits, "pool_slots": w.pool_slots,
+                       "parallelism": "replicas" if world > 1 else "single-gpu",
+                       "l2": "inputs larger than L2: each step reads its experts from the HBM pool or the host"},
+            "pool": {"hit_rate_all": rate(None, s1), "hit_rate_after_step64": rate(at64, s1) if at64 else None,
+                     "hit_rate_timed": rate(s0, s1), "misses_timed": s1["misses"] - s0["misses"],
+                     "h2d_bytes_timed": h2d, "h2d_device_ms_timed": h2d_ms,
+                     "host_link_gbs_during_copies": h2d / max(h2d_ms, 1e-9) / 1e6,
+                     "host_link_gbs_wall": h2d / secs / 1e9, "host_link_probe_gbs": link_peak},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                         "peak_kind": peak_kind, "traffic": None,
+                         "kernel": "streaming decode stack (per-layer kernels, host pool decision per layer)",
+                         "bytes_per_launch": expert_bytes},
+            "gpu_launches": int(launches),
+            "clocks": clocks,
+            "e2e": e2e,
+        }
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w, bits, args.cpu_samples)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+    finally:
+        moe.moe_destroy(ctx)
+        if pg:
+            pg.destroy_process_group()
+
+
 def main():
     args = parse_args()
+    if not args.steps:
+        args.steps = {"80b-prefill": 50, "stress": 1024}.get(args.config, 2048)
     if args.impl == "reference":
         run_reference(args)
     elif args.config == "80b-prefill":
         run_prefill(args)
+    elif args.config == "stress":
+        run_stress(args)
     else:
         run_ours(args)
 

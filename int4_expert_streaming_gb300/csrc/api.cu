@@ -65,6 +65,7 @@ struct moe_ctx {
     int32_t* idx = nullptr;
     float* w = nullptr;
     float* h = nullptr;
+    float* part = nullptr;  // [max_pairs][H] weighted down rows of each pair
     float* xbuf = nullptr;  // [2][max_batch][H]
     float* ybuf = nullptr;  // [max_batch][H]
     void* disp_mem = nullptr;
@@ -265,7 +266,7 @@ int decode_layer(moe_ctx* c, int layer, const float* x, int B, float* y, int32_t
     const uint16_t* wsg = c->cfg.shared_inter > 0 ? c->shared_gate + (size_t)layer * c->cfg.hidden : nullptr;
     const uint8_t* const* dir = c->dir + (size_t)layer * E;
     CUDA_TRY(c, moe::launch_router(s, wr, bias, x, B, c->logits, st));
-    c->launches += c->resident ? 4 : 5;
+    c->launches += 6;  // router, top-k (per token), dispatch, gate/up, down, combine
     if (c->resident) {
         CUDA_TRY(c, moe::launch_route_dispatch(s, 3, c->logits, x, wsg, B, c->idx, c->w, c->sigma, uidx, uw, dir,
                                                shared_blob(c, layer), c->disp, c->xd, c->hits_dev + layer, st));
@@ -277,8 +278,9 @@ int decode_layer(moe_ctx* c, int layer, const float* x, int B, float* y, int32_t
         CUDA_TRY(c, moe::launch_route_dispatch(s, 2, c->logits, x, wsg, B, c->idx, c->w, c->sigma, nullptr,
                                                nullptr, dir, shared_blob(c, layer), c->disp, c->xd, nullptr, st));
     }
-    CUDA_TRY(c, moe::launch_gateup(s, c->disp, c->xd, c->h, B, st));
-    CUDA_TRY(c, moe::launch_down(s, c->disp, c->h, y, B, st));
+    CUDA_TRY(c, moe::launch_gateup_batched(s, c->disp, c->xd, c->h, st));
+    CUDA_TRY(c, moe::launch_down_batched(s, c->disp, c->h, c->part, st));
+    CUDA_TRY(c, moe::launch_combine(s, c->disp, c->part, y, B, c->cfg.shared_inter > 0, st));
     c->stats[layer].calls++;
     return MOE_OK;
 }
@@ -330,6 +332,7 @@ extern "C" void moe_destroy(moe_ctx* c) {
     cudaFree(c->idx);
     cudaFree(c->w);
     cudaFree(c->h);
+    cudaFree(c->part);
     cudaFree(c->xbuf);
     cudaFree(c->ybuf);
     cudaFree(c->disp_mem);
@@ -371,6 +374,7 @@ extern "C" int moe_create(const moe_config* cfg, moe_ctx** out) {
     s.max_act = std::min(E, Bm * k) + 1;
     s.max_pairs = Bm * (k + 1);
     s.h_stride = std::max(g.inter, g.shared_inter);
+    s.max_work = s.max_act + s.max_pairs / 8 + 1;
     c->loaded.assign(L, 0);
     c->stats.assign(L, LayerStats{});
 
@@ -396,6 +400,7 @@ extern "C" int moe_create(const moe_config* cfg, moe_ctx** out) {
         (rc = dev_alloc(c, &c->sigma, (size_t)Bm, "sigma")) ||
         (rc = dev_alloc(c, &c->idx, (size_t)Bm * k, "idx")) || (rc = dev_alloc(c, &c->w, (size_t)Bm * k, "w")) ||
         (rc = dev_alloc(c, &c->h, (size_t)s.max_pairs * s.h_stride, "h")) ||
+        (rc = dev_alloc(c, &c->part, (size_t)s.max_pairs * H, "down partials")) ||
         (rc = dev_alloc(c, &c->xbuf, (size_t)2 * Bm * H, "xbuf")) ||
         (rc = dev_alloc(c, &c->ybuf, (size_t)Bm * H, "ybuf")) ||
         (rc = dev_alloc(c, &c->xd.words, (size_t)Bm * H * 3 / 4, "token digits")) ||
@@ -405,7 +410,8 @@ extern "C" int moe_create(const moe_config* cfg, moe_ctx** out) {
     // dispatch scratch in one allocation
     {
         const size_t A = s.max_act, P = s.max_pairs;
-        const size_t bytes = 16 + A * 4 + A * 8 + (A + 1) * 4 + P * 4 + P * 4 + 16 + 64;
+        const size_t W = s.max_work;
+        const size_t bytes = 16 + A * 4 + A * 8 + (A + 1) * 4 + P * 4 + P * 4 + (size_t)Bm * 17 * 4 + W * 16 + 16 + 256;
         if ((rc = dev_alloc(c, reinterpret_cast<uint8_t**>(&c->disp_mem), bytes, "dispatch"))) return bail(rc);
         uint8_t* p = static_cast<uint8_t*>(c->disp_mem);
         auto take = [&](size_t n) {
@@ -420,6 +426,9 @@ extern "C" int moe_create(const moe_config* cfg, moe_ctx** out) {
         c->disp.act_off = reinterpret_cast<int32_t*>(take((A + 1) * 4));
         c->disp.pair_token = reinterpret_cast<int32_t*>(take(P * 4));
         c->disp.pair_w = reinterpret_cast<float*>(take(P * 4));
+        c->disp.tok_pairs = reinterpret_cast<int32_t*>(take((size_t)Bm * 17 * 4));
+        c->disp.work = reinterpret_cast<int4*>(take(W * 16));
+        c->disp.n_work = reinterpret_cast<int32_t*>(take(4));
         if (cudaMemset(c->disp_mem, 0, bytes) != cudaSuccess) {
             c->err = "cudaMemset failed";
             return bail(MOE_ECUDA);
@@ -568,7 +577,9 @@ extern "C" int moe_forward_decode_stack(moe_ctx* c, int32_t layer0, int32_t n, c
                     moe::stack_last_status(c->stack)) == MOE_ETIMEOUT
                    ? (c->poisoned = true, MOE_ETIMEOUT)
                    : MOE_ETIMEOUT;
-    if (c->resident && moe::stack_supported(c->sh, c->stack, B)) {
+    // the persistent kernel wins for a few tokens; from 4 tokens on, the batched
+    // per-layer kernels (each expert's rows read once for all of its tokens) are faster
+    if (c->resident && B <= moe::kStackPreferMaxB && moe::stack_supported(c->sh, c->stack, B)) {
         moe::StackArgs a{};
         a.layer0 = layer0;
         a.n_layers = n;

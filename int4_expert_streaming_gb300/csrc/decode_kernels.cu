@@ -1,7 +1,8 @@
 // decode_kernels.cu -- per-layer decode kernels for sm_103a: router logits,
-// top-k + dispatch (+ the tokens' block-fixed-point digits), fused dequant
-// gate/up + SwiGLU, dequant down + weighted combine, and the between-layer
-// renormalisation.  They serve streaming contexts (which read the routing
+// top-k + dispatch (+ the tokens' block-fixed-point digits), batched dequant
+// gate/up + SwiGLU and down (a CTA per active expert and row block, so each
+// expert's weights are read once for all of its tokens), the per-token
+// weighted combine, and the between-layer renormalisation.  They serve streaming contexts (which read the routing
 // back between kernels), batches above the persistent kernel's limit and
 // single-layer calls; the arithmetic is the one in gemv.cuh, shared with the
 // persistent stack kernel, so both paths give the same bits.
@@ -13,8 +14,7 @@ namespace {
 
 constexpr int kMaxE = 1024, kMaxK = 16, kMaxB = 64;
 constexpr int kThreads = 256, kNWarps = kThreads / 32;
-constexpr int kGateupRowsPerCta = 16;
-constexpr int kDownRowsPerWarp = 2;
+constexpr int kWorkPairs = 8;  // pairs per work item of the batched kernels
 
 // ---------------------------------------------------------------------------
 // router logits: one warp per expert, all tokens
@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(1024) route_dispatch_kernel(
     __shared__ int s_total;
 
     if (mode & 1) {
-        for (int t = warp; t < B; t += nw) {
+        for (int t = blockIdx.x * nw + warp; t < B; t += gridDim.x * nw) {
             warp_topk(logits + (size_t)t * E, E, k, s.norm_topk, lane, s_idx[t], s_val[t], s_w[t]);
             if (lane < k) {
                 idx[t * k + lane] = s_idx[t][lane];
@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(1024) route_dispatch_kernel(
         }
     }
     if (!(mode & 2)) return;
-    __syncthreads();
+    __syncthreads();  // (mode 2 runs as a single CTA)
     const int tid = threadIdx.x;
     for (int e = tid; e < kMaxE; e += blockDim.x) {
         s_cnt[e] = 0;
@@ -174,68 +174,41 @@ __global__ void __launch_bounds__(1024) route_dispatch_kernel(
             d.pair_w[npair + t] = sigma[t];
         }
     }
-}
-
-// ---------------------------------------------------------------------------
-// gate/up: one warp per row, the token's digits read from memory
-// ---------------------------------------------------------------------------
-template <int BITS>
-__device__ __forceinline__ float row_dot_tok(const uint8_t* q_row, const uint32_t* sb_row, const uint32_t* words,
-                                             const int32_t* sums, int e, int cols, int lane) {
-    constexpr int CC = Codes<BITS>::kCols, CPG = 64 / CC, DW = Codes<BITS>::kDigitWords;
-    const int nchunk = cols / CC;
-    const uint4* q = reinterpret_cast<const uint4*>(q_row);
-    float part = 0.0f;
-    for (int c = lane; c < nchunk; c += 32) {
-        uint32_t dw[DW];
-#pragma unroll
-        for (int i = 0; i < DW; i += 4) {
-            const uint4 v = *reinterpret_cast<const uint4*>(words + (size_t)c * DW + i);
-            dw[i] = v.x, dw[i + 1] = v.y, dw[i + 2] = v.z, dw[i + 3] = v.w;
+    // each token's pairs in ascending pair order (ascending expert, the shared one last)
+    __syncthreads();
+    const int npt = k + (shared_blob ? 1 : 0);
+    for (int t = tid; t < B; t += blockDim.x) {
+        int v[kMaxK + 1];
+        for (int i = 0; i < k; ++i) {
+            const int e = idx[t * k + i];
+            v[i] = (s_scan[e] >> 16) + __popcll(s_msk[e] & ((1ull << t) - 1ull));
         }
-        const float A = chunk_dot(__ldg(q + c), dw, Codes<BITS>{});
-        part = chunk_term(part, A, sums[c], __ldg(sb_row + c / CPG));
-    }
-    return pow2_scale(warp_sum(part), -e);
-}
-
-template <int BITS>
-__global__ void __launch_bounds__(kThreads) gateup_kernel(Shapes s, Dispatch d, TokenDigits xd,
-                                                          float* __restrict__ h) {
-    constexpr int CC = Codes<BITS>::kCols, DW = Codes<BITS>::kDigitWords;
-    const int a = blockIdx.y;
-    if (a >= *d.n_act) return;
-    const bool shared = d.act_expert[a] < 0;
-    const int rows = shared ? s.shared_inter : s.inter;
-    const int r0 = blockIdx.x * kGateupRowsPerCta;
-    if (r0 >= rows) return;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int H = s.hidden, nc = H / CC;
-    const uint8_t* blob = d.act_blob[a];
-    const BlobLayout L = blob_layout(H, rows, BITS);
-    const size_t row_bytes = (size_t)H * BITS / 8;
-    const int ng = H / 64;
-    const int p0 = d.act_off[a], p1 = d.act_off[a + 1];
-    const int r1 = min(r0 + kGateupRowsPerCta, rows);
-    for (int r = r0 + warp; r < r1; r += kNWarps) {
-        const uint8_t* gq = blob + L.gate_q + r * row_bytes;
-        const uint8_t* uq = blob + L.up_q + r * row_bytes;
-        const uint32_t* gsb = reinterpret_cast<const uint32_t*>(blob + L.gate_sb) + (size_t)r * ng;
-        const uint32_t* usb = reinterpret_cast<const uint32_t*>(blob + L.up_sb) + (size_t)r * ng;
-        for (int p = p0; p < p1; ++p) {
-            const int t = d.pair_token[p];
-            const uint32_t* words = xd.words + (size_t)t * nc * DW;
-            const int32_t* sums = xd.sums + (size_t)t * nc;
-            const int e = xd.exps[t];
-            const float g = row_dot_tok<BITS>(gq, gsb, words, sums, e, H, lane);
-            const float u = row_dot_tok<BITS>(uq, usb, words, sums, e, H, lane);
-            if (lane == 0) h[(size_t)p * s.h_stride + r] = silu_mul(g, u);
+        for (int i = 1; i < k; ++i) {  // insertion sort, k <= 16
+            const int x = v[i];
+            int j = i - 1;
+            while (j >= 0 && v[j] > x) {
+                v[j + 1] = v[j];
+                --j;
+            }
+            v[j + 1] = x;
         }
+        if (shared_blob) v[k] = npair + t;
+        for (int i = 0; i < npt; ++i) d.tok_pairs[t * (kMaxK + 1) + i] = v[i];
     }
+    // work items of the batched kernels: (active expert, first pair, <= kWorkPairs pairs),
+    // so an expert chosen by many tokens is spread over many CTAs
+    __syncthreads();
+    const int n_all = n_routed + (shared_blob ? 1 : 0);
+    const int P = tid < n_all ? d.act_off[tid + 1] - d.act_off[tid] : 0;
+    const int grp = (P + kWorkPairs - 1) / kWorkPairs;
+    const int gincl = block_scan_incl(grp, s_wsum);
+    for (int g = 0; g < grp; ++g)
+        d.work[gincl - grp + g] = make_int4(tid, d.act_off[tid] + g * kWorkPairs, min(kWorkPairs, P - g * kWorkPairs), 0);
+    if (tid == blockDim.x - 1) *d.n_work = gincl;
 }
 
 // ---------------------------------------------------------------------------
-// down: the pair's h as digits in registers (one chunk per lane), rows of the warp
+// down rows multiply fp32 h (HF: one chunk per lane)
 // ---------------------------------------------------------------------------
 // this lane's chunk of an h vector of `cols` values (cols / CC <= 32), zeros past the end
 template <int BITS>
@@ -250,44 +223,213 @@ __device__ __forceinline__ void load_hf(const float* h, int cols, int lane, HF<B
     hf_sum(hf);
 }
 
-// y[t][j] = sum over active experts a (ascending, shared last) of w * (D_a[j] . h)
+// ---------------------------------------------------------------------------
+// batched gate/up: a CTA per (active expert, kGuRows rows); the digits of the
+// expert's tokens staged in shared memory kGuTok at a time; each warp's rows
+// against each token with row_dot_x2 (the persistent kernel's arithmetic)
+// ---------------------------------------------------------------------------
+constexpr int kGuRows = 32, kGuTok = 8;
+
+template <int BITS, int NPER>
+__global__ void __launch_bounds__(kThreads, 2) gateup_batched_kernel(Shapes s, Dispatch d, TokenDigits xd,
+                                                                  float* __restrict__ h) {
+    constexpr int CC = Codes<BITS>::kCols, DW = Codes<BITS>::kDigitWords;
+    static_assert(kGuTok >= kWorkPairs, "a work item's tokens fit the staging area");
+    extern __shared__ __align__(16) uint32_t g_sm[];
+    if ((int)blockIdx.y >= *d.n_work) return;
+    const int4 wi = d.work[blockIdx.y];
+    const int a = wi.x, pg = wi.y, n = wi.z;
+    const bool shared = d.act_expert[a] < 0;
+    const int rows = shared ? s.shared_inter : s.inter;
+    const int r0 = blockIdx.x * kGuRows;
+    if (r0 >= rows) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int H = s.hidden, nc = H / CC, ng = H / 64;
+    uint32_t* sw = g_sm;                                                 // [kGuTok][nc * DW]
+    int32_t* ss = reinterpret_cast<int32_t*>(g_sm + kGuTok * nc * DW);  // [kGuTok][nc]
+    const uint8_t* blob = d.act_blob[a];
+    const BlobLayout L = blob_layout(H, rows, BITS);
+    const size_t row_bytes = (size_t)H * BITS / 8;
+    for (int i = threadIdx.x; i < n * nc * DW / 4; i += kThreads) {
+        const int j = i / (nc * DW / 4), o = i - j * (nc * DW / 4);
+        const int t = d.pair_token[pg + j];
+        reinterpret_cast<uint4*>(sw)[i] = reinterpret_cast<const uint4*>(xd.words + (size_t)t * nc * DW)[o];
+    }
+    for (int i = threadIdx.x; i < n * nc; i += kThreads) {
+        const int j = i / nc;
+        ss[i] = xd.sums[(size_t)d.pair_token[pg + j] * nc + (i - j * nc)];
+    }
+    __syncthreads();
+    constexpr int CPG = 64 / CC;
+    int ex[kGuTok];
+#pragma unroll
+    for (int j = 0; j < kGuTok; ++j) ex[j] = j < n ? xd.exps[d.pair_token[pg + j]] : 0;
+    for (int r = r0 + warp; r < min(r0 + kGuRows, rows); r += kNWarps) {
+        // the row's code chunks and scale/bias words, once for all tokens
+        const uint4* gq = reinterpret_cast<const uint4*>(blob + L.gate_q + r * row_bytes);
+        const uint4* uq = reinterpret_cast<const uint4*>(blob + L.up_q + r * row_bytes);
+        const uint32_t* gsb = reinterpret_cast<const uint32_t*>(blob + L.gate_sb) + (size_t)r * ng;
+        const uint32_t* usb = reinterpret_cast<const uint32_t*>(blob + L.up_sb) + (size_t)r * ng;
+        uint4 wg[NPER], wu[NPER];
+        uint32_t sg[NPER], su[NPER];
+#pragma unroll
+        for (int i = 0; i < NPER; ++i) {
+            const int c = lane + 32 * i;
+            if (c < nc) {
+                wg[i] = __ldg(gq + c), wu[i] = __ldg(uq + c);
+                sg[i] = __ldg(gsb + c / CPG), su[i] = __ldg(usb + c / CPG);
+            }
+        }
+        // per token: this lane's partial sums, in row_dot_x2's chunk order
+        float v[2 * kGuTok];
+#pragma unroll
+        for (int j = 0; j < kGuTok; ++j) {
+            float p0 = 0.0f, p1 = 0.0f;
+            if (j < n) {
+                XDigits<BITS, NPER> xr;
+                load_xdigits(xr, sw + (size_t)j * nc * DW, ss + j * nc, nc, lane);
+#pragma unroll
+                for (int i = 0; i < NPER; ++i) {
+                    const int c = lane + 32 * i;
+                    if (c < nc) {
+                        p0 = chunk_term(p0, chunk_dot(wg[i], xr.dw[i], Codes<BITS>{}), xr.S[i], sg[i]);
+                        p1 = chunk_term(p1, chunk_dot(wu[i], xr.dw[i], Codes<BITS>{}), xr.S[i], su[i]);
+                    }
+                }
+            }
+            v[2 * j] = p0;
+            v[2 * j + 1] = p1;
+        }
+        // reduce-scatter of the 16 partials over the warp: the xor-16, 8, 4, 2, 1
+        // pairs of warp_sum, each value followed by the lanes that keep it;
+        // lanes 2m and 2m + 1 end with value m (bitwise warp_sum of it)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const bool hi = lane & 16;
+            const float send = hi ? v[i] : v[8 + i], keep = hi ? v[8 + i] : v[i];
+            v[i] = __fadd_rn(keep, __shfl_xor_sync(kFullMask, send, 16));
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const bool hi = lane & 8;
+            const float send = hi ? v[i] : v[4 + i], keep = hi ? v[4 + i] : v[i];
+            v[i] = __fadd_rn(keep, __shfl_xor_sync(kFullMask, send, 8));
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const bool hi = lane & 4;
+            const float send = hi ? v[i] : v[2 + i], keep = hi ? v[2 + i] : v[i];
+            v[i] = __fadd_rn(keep, __shfl_xor_sync(kFullMask, send, 4));
+        }
+        {
+            const bool hi = lane & 2;
+            const float send = hi ? v[0] : v[1], keep = hi ? v[1] : v[0];
+            v[0] = __fadd_rn(keep, __shfl_xor_sync(kFullMask, send, 2));
+        }
+        v[0] = __fadd_rn(v[0], __shfl_xor_sync(kFullMask, v[0], 1));
+        // value m = 2 j (gate) on lanes 4j, 4j+1, value 2 j + 1 (up) on lanes 4j+2, 4j+3
+        const float up = __shfl_down_sync(kFullMask, v[0], 2);
+        const int j = lane >> 2;
+        int e = 0;
+#pragma unroll
+        for (int q = 0; q < kGuTok; ++q)
+            if (q == j) e = ex[q];
+        if ((lane & 3) == 0 && j < n)
+            h[(size_t)(pg + j) * s.h_stride + r] = silu_mul(pow2_scale(v[0], -e), pow2_scale(up, -e));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// batched down: a CTA per (active expert, kDnRows output rows); for each of
+// the expert's pairs, weighted row dots into part[pair][row]
+// ---------------------------------------------------------------------------
+constexpr int kDnRows = 64;
+
 template <int BITS>
-__global__ void __launch_bounds__(kThreads) down_kernel(Shapes s, Dispatch d, const float* __restrict__ h,
-                                                        float* __restrict__ y, int B) {
-    __shared__ float yacc[kNWarps][kDownRowsPerWarp][kMaxB];
+__global__ void __launch_bounds__(kThreads, 2) down_batched_kernel(Shapes s, Dispatch d, const float* __restrict__ h,
+                                                                float* __restrict__ part) {
+    constexpr int CC = Codes<BITS>::kCols, CPG = 64 / CC, RW = kDnRows / kNWarps;
+    static_assert(RW == 8, "eight rows per warp: four half-warp passes");
+    __shared__ __align__(16) float hs[kWorkPairs][1024];  // the item's h rows (cols <= 1024)
+    if ((int)blockIdx.y >= *d.n_work) return;
+    const int4 wi = d.work[blockIdx.y];
+    const int a = wi.x, pg = wi.y, n = wi.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = s.hidden;
-    const int n_act = *d.n_act;
-    const int j0 = (blockIdx.x * kNWarps + warp) * kDownRowsPerWarp;
-    if (j0 >= H) return;
-    const int nj = min(kDownRowsPerWarp, H - j0);
-    for (int jj = 0; jj < nj; ++jj)
-        for (int t = lane; t < B; t += 32) yacc[warp][jj][t] = 0.0f;
-    __syncwarp();
-    for (int a = 0; a < n_act; ++a) {
-        const bool shared = d.act_expert[a] < 0;
-        const int cols = shared ? s.shared_inter : s.inter;
-        const BlobLayout L = blob_layout(H, cols, BITS);
-        const uint8_t* blob = d.act_blob[a];
-        const size_t row_bytes = (size_t)cols * BITS / 8;
-        const int ng = cols / 64;
-        for (int p = d.act_off[a]; p < d.act_off[a + 1]; ++p) {
+    const bool shared = d.act_expert[a] < 0;
+    const int cols = shared ? s.shared_inter : s.inter;
+    const BlobLayout L = blob_layout(H, cols, BITS);
+    const uint8_t* blob = d.act_blob[a];
+    const size_t row_bytes = (size_t)cols * BITS / 8;
+    const int ng = cols / 64;
+    const int jb = blockIdx.x * kDnRows + warp * RW;
+    for (int i = threadIdx.x; i < n * cols / 4; i += kThreads) {
+        const int j = i / (cols / 4), o = i - j * (cols / 4);
+        reinterpret_cast<float4*>(hs[j])[o] = reinterpret_cast<const float4*>(h + (size_t)(pg + j) * s.h_stride)[o];
+    }
+    __syncthreads();
+    if (jb >= H) return;
+    const int je = min(H, jb + RW);
+    if (BITS == 4 && cols == 16 * CC && je - jb == RW) {
+        // rows jb + 2i (lanes 0-15) and jb + 2i + 1 (lanes 16-31): this lane's code chunk and
+        // scale/bias word of each, kept in registers for all of the item's pairs
+        const int c = lane & 15, hi = lane >> 4;
+        uint4 q[RW / 2];
+        uint32_t sb[RW / 2];
+#pragma unroll
+        for (int i = 0; i < RW / 2; ++i) {
+            const int j = jb + 2 * i + hi;
+            q[i] = __ldg(reinterpret_cast<const uint4*>(blob + L.down_q + j * row_bytes) + c);
+            sb[i] = __ldg(reinterpret_cast<const uint32_t*>(blob + L.down_sb) + (size_t)j * ng + c / CPG);
+        }
+        for (int p = 0; p < n; ++p) {
             HF<BITS> hd;
-            load_hf<BITS>(h + (size_t)p * s.h_stride, cols, lane, hd);
-            const int t = d.pair_token[p];
-            const float wp = d.pair_w[p];
-            for (int jj = 0; jj < nj; ++jj) {
-                const int j = j0 + jj;
-                const float v = row_dot_h<BITS>(blob + L.down_q + j * row_bytes,
-                                                reinterpret_cast<const uint32_t*>(blob + L.down_sb) + (size_t)j * ng, hd,
-                                                cols, lane);
-                if (lane == 0) yacc[warp][jj][t] = __fadd_rn(yacc[warp][jj][t], __fmul_rn(wp, v));
+#pragma unroll
+            for (int i = 0; i < CC; i += 4) {
+                const float4 f = *reinterpret_cast<const float4*>(&hs[p][c * CC + i]);
+                hd.v[i] = f.x, hd.v[i + 1] = f.y, hd.v[i + 2] = f.z, hd.v[i + 3] = f.w;
             }
-            __syncwarp();
+            hf_sum(hd);
+            // row_dot_h_halves of the four row pairs, butterflies interleaved
+            float v[RW / 2];
+#pragma unroll
+            for (int i = 0; i < RW / 2; ++i) v[i] = chunk_term_f<BITS>(chunk_dot_f(q[i], hd.v, Codes<BITS>{}), hd.s, sb[i]);
+#pragma unroll
+            for (int off = 8; off >= 1; off >>= 1)
+#pragma unroll
+                for (int i = 0; i < RW / 2; ++i) v[i] = __fadd_rn(v[i], __shfl_xor_sync(kFullMask, v[i], off));
+            if (c == 0) {
+                const float wp = d.pair_w[pg + p];
+                float* out = part + (size_t)(pg + p) * H + jb + hi;
+#pragma unroll
+                for (int i = 0; i < RW / 2; ++i) out[2 * i] = __fmul_rn(wp, v[i]);
+            }
+        }
+    } else {
+        for (int p = 0; p < n; ++p) {
+            HF<BITS> hd;
+            load_hf<BITS>(hs[p], cols, lane, hd);
+            const float wp = d.pair_w[pg + p];
+            float* out = part + (size_t)(pg + p) * H;
+            for (int j = jb; j < je; ++j) {
+                const float v = row_dot_h<BITS>(blob + L.down_q + j * row_bytes,
+                                                reinterpret_cast<const uint32_t*>(blob + L.down_sb) + (size_t)j * ng,
+                                                hd, cols, lane);
+                if (lane == 0) out[j] = __fmul_rn(wp, v);
+            }
         }
     }
-    for (int jj = 0; jj < nj; ++jj)
-        for (int t = lane; t < B; t += 32) y[(size_t)t * H + j0 + jj] = yacc[warp][jj][t];
+}
+
+// y[t][j] = sum of the token's weighted pair rows in ascending pair order
+__global__ void __launch_bounds__(kThreads) combine_kernel(Dispatch d, const float* __restrict__ part,
+                                                           float* __restrict__ y, int B, int H, int npt) {
+    const int i = blockIdx.x * kThreads + threadIdx.x;
+    if (i >= B * H) return;
+    const int t = i / H, j = i - t * H;
+    float acc = 0.0f;
+    for (int q = 0; q < npt; ++q) acc = __fadd_rn(acc, part[(size_t)d.tok_pairs[t * (kMaxK + 1) + q] * H + j]);
+    y[i] = acc;
 }
 
 // x = y / sqrt(mean(y^2) + eps), one block of kRenormThreads per token
@@ -305,6 +447,7 @@ __global__ void __launch_bounds__(kRenormThreads) renorm_kernel(const float* __r
 
 cudaError_t launch_router(const Shapes& s, const uint16_t* w_r, const float* bias, const float* x, int B,
                           float* logits, cudaStream_t st) {
+    if (s.hidden <= 2048) return launch_logits(w_r, bias, x, B, s.hidden, s.n_experts, 8, logits, st);
     router_kernel<<<(s.n_experts + kNWarps - 1) / kNWarps, kThreads, 0, st>>>(w_r, bias, x, B, s.hidden,
                                                                             s.n_experts, logits);
     return cudaGetLastError();
@@ -315,29 +458,58 @@ cudaError_t launch_route_dispatch(const Shapes& s, int mode, const float* logits
                                   int32_t* user_idx, float* user_w, const uint8_t* const* dir_layer,
                                   const uint8_t* shared_blob, Dispatch d, TokenDigits xd,
                                   unsigned long long* hit_counter, cudaStream_t st) {
-    route_dispatch_kernel<<<1, 1024, 0, st>>>(s, mode, logits, x, shared_gate_w, B, idx, w, sigma, user_idx,
-                                              user_w, dir_layer, shared_blob, d, xd, hit_counter);
+    // the per-token part (top-k, weights, shared gate, digits: one warp per token) spread
+    // over B/8 CTAs; the dispatch lists in one CTA of 1024 threads
+    if (mode & 1) {
+        route_dispatch_kernel<<<(B + 7) / 8, 256, 0, st>>>(s, mode & ~2, logits, x, shared_gate_w, B, idx, w, sigma,
+                                                            user_idx, user_w, dir_layer, shared_blob, d, xd,
+                                                            hit_counter);
+    }
+    if (mode & 2) {
+        route_dispatch_kernel<<<1, 1024, 0, st>>>(s, mode & ~1, logits, x, shared_gate_w, B, idx, w, sigma,
+                                                  user_idx, user_w, dir_layer, shared_blob, d, xd, hit_counter);
+    }
     return cudaGetLastError();
 }
 
-cudaError_t launch_gateup(const Shapes& s, Dispatch d, TokenDigits xd, float* h, int B, cudaStream_t st) {
-    (void)B;
+cudaError_t launch_gateup_batched(const Shapes& s, Dispatch d, TokenDigits xd, float* h, cudaStream_t st) {
     const int rows = s.inter > s.shared_inter ? s.inter : s.shared_inter;
-    dim3 grid((rows + kGateupRowsPerCta - 1) / kGateupRowsPerCta, s.max_act);
-    if (s.bits == 4)
-        gateup_kernel<4><<<grid, kThreads, 0, st>>>(s, d, xd, h);
-    else
-        gateup_kernel<8><<<grid, kThreads, 0, st>>>(s, d, xd, h);
+    dim3 grid((rows + kGuRows - 1) / kGuRows, s.max_work);
+    const int nc = s.hidden / (s.bits == 4 ? 32 : 16), DW = s.bits == 4 ? 24 : 12;
+    const size_t smem = (size_t)kGuTok * nc * (DW + 1) * 4;
+    const int nper = (nc + 31) / 32;
+    cudaError_t e = cudaSuccess;
+#define MOE_GU(B_, N_)                                                                                         \
+    do {                                                                                                     \
+        e = cudaFuncSetAttribute(gateup_batched_kernel<B_, N_>, cudaFuncAttributeMaxDynamicSharedMemorySize,  \
+                                 (int)smem);                                                                  \
+        if (e == cudaSuccess) gateup_batched_kernel<B_, N_><<<grid, kThreads, smem, st>>>(s, d, xd, h);       \
+    } while (0)
+    if (s.bits == 4) {
+        if (nper <= 1) MOE_GU(4, 1); else if (nper == 2) MOE_GU(4, 2); else return cudaErrorInvalidValue;
+    } else {
+        if (nper <= 1) MOE_GU(8, 1); else if (nper == 2) MOE_GU(8, 2); else if (nper <= 4) MOE_GU(8, 4);
+        else return cudaErrorInvalidValue;
+    }
+#undef MOE_GU
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
-cudaError_t launch_down(const Shapes& s, Dispatch d, const float* h, float* y, int B, cudaStream_t st) {
-    const int rows_per_cta = kNWarps * kDownRowsPerWarp;
-    const int grid = (s.hidden + rows_per_cta - 1) / rows_per_cta;
+cudaError_t launch_down_batched(const Shapes& s, Dispatch d, const float* h, float* part, cudaStream_t st) {
+    dim3 grid((s.hidden + kDnRows - 1) / kDnRows, s.max_work);
     if (s.bits == 4)
-        down_kernel<4><<<grid, kThreads, 0, st>>>(s, d, h, y, B);
+        down_batched_kernel<4><<<grid, kThreads, 0, st>>>(s, d, h, part);
     else
-        down_kernel<8><<<grid, kThreads, 0, st>>>(s, d, h, y, B);
+        down_batched_kernel<8><<<grid, kThreads, 0, st>>>(s, d, h, part);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const Shapes& s, Dispatch d, const float* part, float* y, int B, bool has_shared,
+                           cudaStream_t st) {
+    const int n = B * s.hidden;
+    combine_kernel<<<(n + kThreads - 1) / kThreads, kThreads, 0, st>>>(d, part, y, B, s.hidden,
+                                                                       s.top_k + (has_shared ? 1 : 0));
     return cudaGetLastError();
 }
 

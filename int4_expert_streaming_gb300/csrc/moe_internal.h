@@ -39,11 +39,15 @@ struct Dispatch {
     int32_t* pair_token;   // [max_pairs]
     float* pair_w;         // [max_pairs] routing weight (sigmoid gate for the shared expert)
     int32_t* status;       // [1] device error word (0 = ok, 1 = routed to a non-resident expert)
+    int32_t* tok_pairs;    // [max_batch][17] each token's pairs, ascending (the shared pair last)
+    int4* work;            // [max_work] {active expert, first pair, pairs (<= 8), 0} of the batched kernels
+    int32_t* n_work;       // [1]
 };
 
 struct Shapes {
     int hidden, n_experts, top_k, inter, shared_inter, bits, norm_topk;
     int max_act, max_pairs, h_stride;  // h_stride = max(inter, shared_inter)
+    int max_work;                      // max_act + max_pairs / 8 + 1 work items of the batched kernels
 };
 
 // Block-fixed-point digits of the decode tokens (see gemv.cuh), written by the
@@ -63,9 +67,18 @@ cudaError_t launch_route_dispatch(const Shapes& s, int mode, const float* logits
                                   int32_t* user_idx, float* user_w, const uint8_t* const* dir_layer,
                                   const uint8_t* shared_blob, Dispatch d, TokenDigits xd,
                                   unsigned long long* hit_counter, cudaStream_t st);
-cudaError_t launch_gateup(const Shapes& s, Dispatch d, TokenDigits xd, float* h, int B, cudaStream_t st);
-cudaError_t launch_down(const Shapes& s, Dispatch d, const float* h, float* y, int B, cudaStream_t st);
 cudaError_t launch_renorm(const float* y, float* x_next, int B, int hidden, float eps, cudaStream_t st);
+// batched per-layer path: gate/up per (expert, row block) with staged token digits,
+// down per (expert, row block) into part[pair][H], then the per-token combine
+cudaError_t launch_gateup_batched(const Shapes& s, Dispatch d, TokenDigits xd, float* h, cudaStream_t st);
+cudaError_t launch_down_batched(const Shapes& s, Dispatch d, const float* h, float* part, cudaStream_t st);
+cudaError_t launch_combine(const Shapes& s, Dispatch d, const float* part, float* y, int B, bool has_shared,
+                           cudaStream_t st);
+
+// prefill_route.cu: router logits of T tokens in the fixed fp32 order, register
+// tiled (hidden <= 2048, a multiple of 256); tok_tile tokens per CTA (<= 64)
+cudaError_t launch_logits(const uint16_t* w_r, const float* bias, const float* x, int T, int H, int E, int tok_tile,
+                          float* logits, cudaStream_t st);
 
 // noalloc.cu: the fixed scratch array of moe_route_noalloc on `device`
 cudaError_t noalloc_scratch(int device, void** ptr, size_t* bytes);

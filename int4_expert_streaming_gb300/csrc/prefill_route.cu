@@ -57,12 +57,12 @@ __device__ __forceinline__ void cp_async_wait() {
 __global__ void __launch_bounds__(kLgThreads, 1) logits_kernel(const uint16_t* __restrict__ w_r,
                                                                const float* __restrict__ bias,
                                                                const float* __restrict__ x, int T, int H, int E,
-                                                               float* __restrict__ logits) {
+                                                               int tok_tile, float* __restrict__ logits) {
     extern __shared__ __align__(16) float4 xs[];  // [kLgStages][kLgStageTok][H / 4]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nc = H / 256, q4 = H / 4;
     const int e0 = blockIdx.x * kLgExperts + warp * kLgExpertsPerWarp;
-    const int t0 = blockIdx.y * kLgTokens, tn = min(kLgTokens, T - t0);
+    const int t0 = blockIdx.y * tok_tile, tn = min(tok_tile, T - t0);
     const int nstage = (tn + kLgStageTok - 1) / kLgStageTok;
 
     auto load_stage = [&](int st) {
@@ -331,6 +331,17 @@ cudaError_t dalloc(T** p, size_t n) {
 
 }  // namespace
 
+cudaError_t launch_logits(const uint16_t* w_r, const float* bias, const float* x, int T, int H, int E, int tok_tile,
+                          float* logits, cudaStream_t st) {
+    const size_t smem = (size_t)kLgStages * kLgStageTok * H * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    tok_tile = std::max(1, std::min(tok_tile, kLgTokens));
+    dim3 grid((E + kLgExperts - 1) / kLgExperts, (T + tok_tile - 1) / tok_tile);
+    logits_kernel<<<grid, kLgThreads, smem, st>>>(w_r, bias, x, T, H, E, tok_tile, logits);
+    return cudaGetLastError();
+}
+
 std::string prefill_check(const Shapes& s) {
     if (s.hidden % 256 || s.hidden > 256 * kMaxNC) return "prefill needs hidden to be a multiple of 256, at most 2048";
     if (s.inter % 128 || s.shared_inter % 128) return "prefill needs inter and shared_inter to be multiples of 128";
@@ -417,14 +428,8 @@ cudaError_t launch_prefill(const Shapes& s, PrefillScratch& p, const PrefillArgs
     int mark = 0;
     auto stamp = [&]() -> cudaError_t { return ev ? cudaEventRecord(ev[mark++], st) : cudaSuccess; };
     if ((e = stamp())) return e;
-    {
-        const size_t smem = (size_t)kLgStages * kLgStageTok * H * sizeof(float);
-        if ((e = cudaFuncSetAttribute(logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
-            return e;
-        dim3 grid((E + kLgExperts - 1) / kLgExperts, (T + kLgTokens - 1) / kLgTokens);
-        logits_kernel<<<grid, kLgThreads, smem, st>>>(a.router_w, a.router_bias, a.x, T, H, E, p.logits);
-        ++*launches;
-    }
+    if ((e = launch_logits(a.router_w, a.router_bias, a.x, T, H, E, kLgTokens, p.logits, st))) return e;
+    ++*launches;
     if ((e = stamp())) return e;
     select_kernel<<<(T + 7) / 8, 256, 0, st>>>(p.logits, a.x, a.shared_blob ? a.shared_gate : nullptr, T, H, E, k,
                                                s.norm_topk, p.idx, p.w, p.sigma, a.user_idx, a.user_w, p.x_bf, a.y);

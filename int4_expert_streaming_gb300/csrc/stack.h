@@ -36,6 +36,9 @@ struct StackArgs {
     size_t shared_stride;
 };
 
+// largest batch the decode stack sends to the persistent kernel (measured crossover)
+constexpr int kStackPreferMaxB = 3;
+
 int stack_alloc(StackScratch& s, const Shapes& sh, int n_layers, int max_batch, int device, std::string& err);
 void stack_free(StackScratch& s);
 bool stack_supported(const Shapes& sh, const StackScratch& s, int B);

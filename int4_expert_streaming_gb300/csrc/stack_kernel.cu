@@ -506,8 +506,6 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const Params p) {
         uint8_t* tp = Gbuf;
         float* s_lg = reinterpret_cast<float*>(tp);  // [B][E] logits
         tp += r16i(B * E * 4);
-        uint32_t* s_key = reinterpret_cast<uint32_t*>(tp);  // [B][E] order keys
-        tp += r16i(B * E * 4);
         uint32_t* c_key = reinterpret_cast<uint32_t*>(tp);  // [B][C]
         tp += r16i(B * C * 4);
         int32_t* c_idx = reinterpret_cast<int32_t*>(tp);  // [B][C], -1 = empty
@@ -518,7 +516,6 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const Params p) {
                 break;
             }
         }
-        for (int i = tid; i < B * E; i += kST) s_key[i] = order_key(s_lg[i]);
         for (int i = tid; i < B * C; i += kST) c_idx[i] = -1;
         __syncthreads();
         // level 1: each warp selects the k best keys of its slice of every
@@ -533,7 +530,7 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const Params p) {
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
                     const int j = sb + lane + 32 * m;
-                    key[m] = (m < M1 && j < se) ? s_key[t * E + j] : 0u;
+                    key[m] = (m < M1 && j < se) ? order_key(s_lg[t * E + j]) : 0u;
                 }
 #pragma unroll 1
                 for (int r = 0; r < k; ++r) {
@@ -910,7 +907,7 @@ bool plan(const Shapes& sh, int B, int grid, int max_smem, Params& p) {
     p.smem_bytes = off;
     // the top-k temp area lives in the gate/up stages
     const long long tmp =
-        2LL * r16i(B * E * 4) + 2LL * r16i(B * kSW * k * 4);
+        r16i(B * E * 4) + 2LL * r16i(B * kSW * k * 4);
     if (tmp > (long long)kNSG * p.g_cap * p.g_unit) return false;
     return off <= budget;
 }

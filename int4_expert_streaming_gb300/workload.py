@@ -61,3 +61,31 @@ def create_loaded(w: "synth.Workload", bits: int | None = None, max_batch: int =
         blobs, shared, wr, wsg, beta = layer_blobs(w, layer, bits, threads, out=buf)
         moe_load_experts(ctx, layer, blobs, stride, shared, wr, wsg if shared is not None else None, beta)
     return ctx
+
+
+class Drift:
+    """Temporally correlated popularity drift of a Zipf-biased workload.
+
+    Each layer keeps the rank permutation its router bias is drawn from
+    (beta_e = ln p(rank(e)), p(r) ~ r^-s).  Before decode step s >= 1,
+    ``advance`` applies the workload's adjacent-rank swaps of step s to every
+    layer and sends the new bias to the context with moe_set_router_bias;
+    step 0 runs with the bias the layer was loaded with.  ``bias(layer)``
+    gives the current bias, so a checker can rebuild the router of any step.
+    """
+
+    def __init__(self, w: "synth.Workload"):
+        self.w = w
+        self.perm = [synth.rank_permutation(w.seed, l, w.n_experts) for l in range(w.n_layers)]
+        self.step = 0
+
+    def bias(self, layer: int) -> np.ndarray:
+        return synth.zipf_bias(self.perm[layer], self.w.zipf_s)
+
+    def advance(self, ctx=None, stream=None) -> None:
+        from . import moe_set_router_bias
+        self.step += 1
+        for l in range(self.w.n_layers):
+            synth.drift_step(self.w.seed, l, self.step, self.perm[l], self.w.drift_swaps)
+            if ctx is not None:
+                moe_set_router_bias(ctx, l, self.bias(l), stream)

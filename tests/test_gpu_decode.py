@@ -231,11 +231,12 @@ def test_injected_faults_fail_cleanly():
         moe.moe_destroy(ctx)
 
 
-@pytest.mark.parametrize("B,bits", [(1, 4), (2, 4), (5, 4), (8, 4), (1, 8), (8, 8), (12, 4)])
+@pytest.mark.parametrize("B,bits", [(1, 4), (2, 4), (3, 4), (5, 4), (1, 8), (3, 8), (12, 4)])
 def test_stack_kernel_equals_per_layer_kernels(B, bits):
-    """The persistent stack kernel (B <= 8, all resident) and the per-layer
-    kernels share one arithmetic: every layer's routing and output agree bit
-    for bit; and each layer matches the oracle fed the GPU's own layer input."""
+    """The persistent stack kernel (B <= 3, all resident) and the batched
+    per-layer kernels share one arithmetic: every layer's routing and output
+    agree bit for bit; and each layer matches the oracle fed the GPU's own
+    layer input (larger B: the per-layer path on both sides)."""
     w = dataclasses.replace(TINY, n_layers=3, bits=bits)
     L = w.n_layers
     ctx = _ctx(w, max_batch=B)
@@ -249,7 +250,7 @@ def test_stack_kernel_equals_per_layer_kernels(B, bits):
         moe.moe_forward_decode_stack(ctx, 0, L, x, B, y, 1e-6, xt, it, yt, torch.cuda.current_stream())
         torch.cuda.synchronize()
         launches = moe.moe_launch_count(ctx) - n0
-        assert launches == (1 if B <= 8 else 4 * L + L - 1)
+        assert launches == (1 if B <= 3 else 6 * L + L - 1)
         for l in range(L):
             yl = torch.empty_like(x)
             il = torch.empty((B, w.top_k), dtype=torch.int32, device="cuda")
