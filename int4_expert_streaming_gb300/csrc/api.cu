@@ -670,7 +670,10 @@ extern "C" int moe_forward_prefill(moe_ctx* c, int32_t layer, const float* x, in
     if (!x || !y || x == y) return fail(c, MOE_EINVAL, "x and y must be distinct device buffers");
     if (const int st = moe::prefill_last_status(c->pre)) {
         c->poisoned = true;
-        return fail(c, MOE_ETIMEOUT, "a device-side wait of an earlier prefill ran out (status %d)", st);
+        return fail(c, MOE_ETIMEOUT,
+                    "a device-side check of an earlier prefill failed (status %d: 1-4 a wait ran out, 8 the router "
+                    "bound)",
+                    st);
     }
     CUDA_TRY(c, cudaSetDevice(c->cfg.device));
     const int E = c->cfg.n_experts, H = c->cfg.hidden;

@@ -35,6 +35,13 @@ struct PrefillScratch {
     uint16_t* h_hi = nullptr;
     uint16_t* h_lo = nullptr;
     int h_rows = 0;
+    // two-stage router (norm_topk, E a multiple of 128): x as three bf16 pieces
+    // [T][3H] (the first H columns are bf16(x), the operand of the expert GEMMs),
+    // norm bounds of x_t and of the router rows
+    uint16_t* x3 = nullptr;
+    float* xnorm = nullptr;
+    float* wnorm = nullptr;
+    bool two_stage = false;
     int* status_host = nullptr;   // pinned, mapped: 0 = ok, else a device-side wait ran out
     int* status_dev = nullptr;    // device alias of status_host
     int sms = 0;
@@ -66,5 +73,10 @@ int prefill_last_status(const PrefillScratch& p);
 constexpr int kPrefillKernels = 7;
 cudaError_t launch_prefill(const Shapes& s, PrefillScratch& p, const PrefillArgs& a, cudaStream_t st,
                            int* launches, cudaEvent_t* ev = nullptr);
+
+// router_gemm.cu
+bool router_two_stage_ok(const Shapes& s);
+cudaError_t launch_router_two_stage(const Shapes& s, const PrefillScratch& p, const PrefillArgs& a, cudaStream_t st,
+                                    int* launches);
 
 }  // namespace moe

@@ -63,6 +63,7 @@ struct Cfg<1> {  // A0 | A1 | B hi | B lo
 struct GemmArgs {
     int H, E, k, T, P;  // P = T * k
     int inter, shared_inter, slices0, h_rows;
+    int x_stride;  // elements between token rows of x_bf
     const int4* chunks;
     const int32_t* n_chunks;
     const int32_t* perm;
@@ -440,7 +441,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(GemmArgs 
                 for (int i = 0; i < 16; ++i) {
                     const int j = (gt >> 3) + 16 * i;
                     if (j < c.tl.n)
-                        cp_async16(btile + swz_chunk(j, gt & 7), a.x_bf + (size_t)brow[i] * a.H + c.kb * 64 + (gt & 7) * 8);
+                        cp_async16(btile + swz_chunk(j, gt & 7),
+                                   a.x_bf + (size_t)brow[i] * a.x_stride + c.kb * 64 + (gt & 7) * 8);
                     else if (j < np)
                         sts128(btile + swz_chunk(j, gt & 7), make_uint4(0, 0, 0, 0));
                 }
@@ -508,7 +510,8 @@ cudaError_t launch_prefill_gemm(int mode, const Shapes& s, const PrefillScratch&
     g.chunks = p.chunks;
     g.n_chunks = p.n_chunks;
     g.perm = p.perm;
-    g.x_bf = p.x_bf;
+    g.x_bf = p.two_stage ? p.x3 : p.x_bf;
+    g.x_stride = p.two_stage ? 3 * s.hidden : s.hidden;
     g.h_hi = p.h_hi;
     g.h_lo = p.h_lo;
     g.w = p.w;

@@ -252,16 +252,31 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ cnt, i
     __shared__ int tot[1025], off[1025], rem[1025];
     __shared__ int ws[32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int e = warp; e < E; e += 32) {
-        int carry = 0;
+    // block counts -> first positions within each expert: a warp takes 8 of its
+    // experts at a time, 32 blocks per step, loads issued before the scans
+    for (int e8 = warp * 8; e8 < E; e8 += 32 * 8) {
+        int carry[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) carry[q] = 0;
         for (int cb = 0; cb < n_hist; cb += 32) {
             const int i = cb + lane;
-            const int v = i < n_hist ? cnt[(size_t)e * n_hist + i] : 0;
-            const int incl = warp_incl_scan(v, lane);
-            if (i < n_hist) cnt[(size_t)e * n_hist + i] = carry + incl - v;
-            carry += __shfl_sync(kFullMask, incl, 31);
+            int v[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) v[q] = (e8 + q < E && i < n_hist) ? cnt[(size_t)(e8 + q) * n_hist + i] : 0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int incl = warp_incl_scan(v[q], lane);
+                if (e8 + q < E && i < n_hist) cnt[(size_t)(e8 + q) * n_hist + i] = carry[q] + incl - v[q];
+                carry[q] += __shfl_sync(kFullMask, incl, 31);
+            }
         }
-        if (lane == 0) tot[e] = carry;
+        if (lane < 8 && e8 + lane < E) {
+            int cl = 0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (q == lane) cl = carry[q];
+            tot[e8 + lane] = cl;
+        }
     }
     __syncthreads();
     const int NE = E + (has_shared ? 1 : 0);  // chunk owners
@@ -360,6 +375,7 @@ int prefill_alloc(PrefillScratch& p, const Shapes& s, int max_tokens, int device
     p.n_hist = (int)((P + kHistThreads - 1) / kHistThreads);
     p.max_chunks = (int)((P + T) / kChunk + E + 2);
     p.h_rows = (int)((P + T + 16 * (E + 1) + 15) / 16 * 16);
+    p.two_stage = router_two_stage_ok(s);
     cudaDeviceProp prop;
     if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) {
         cudaGetLastError();
@@ -371,7 +387,8 @@ int prefill_alloc(PrefillScratch& p, const Shapes& s, int max_tokens, int device
         dalloc(&p.sigma, T) || dalloc(&p.local_rank, P) || dalloc(&p.cnt, E * p.n_hist) ||
         dalloc(&p.offsets, E + 1) || dalloc(&p.perm, P) || dalloc(&p.chunks, (size_t)p.max_chunks) ||
         dalloc(&p.n_chunks, 1) || dalloc(&p.h_hi, (size_t)p.h_rows * s.h_stride) ||
-        dalloc(&p.h_lo, (size_t)p.h_rows * s.h_stride)) {
+        dalloc(&p.h_lo, (size_t)p.h_rows * s.h_stride) ||
+        (router_two_stage_ok(s) && (dalloc(&p.x3, T * 3 * H) || dalloc(&p.xnorm, T) || dalloc(&p.wnorm, E)))) {
         cudaGetLastError();
         char buf[160];
         snprintf(buf, sizeof buf, "cudaMalloc of the prefill scratch for %d tokens failed", max_tokens);
@@ -413,6 +430,9 @@ void prefill_free(PrefillScratch& p) {
     cudaFree(p.n_chunks);
     cudaFree(p.h_hi);
     cudaFree(p.h_lo);
+    cudaFree(p.x3);
+    cudaFree(p.xnorm);
+    cudaFree(p.wnorm);
     if (p.status_host) cudaFreeHost(p.status_host);
     p = PrefillScratch{};
 }
@@ -428,12 +448,19 @@ cudaError_t launch_prefill(const Shapes& s, PrefillScratch& p, const PrefillArgs
     int mark = 0;
     auto stamp = [&]() -> cudaError_t { return ev ? cudaEventRecord(ev[mark++], st) : cudaSuccess; };
     if ((e = stamp())) return e;
-    if ((e = launch_logits(a.router_w, a.router_bias, a.x, T, H, E, kLgTokens, p.logits, st))) return e;
-    ++*launches;
-    if ((e = stamp())) return e;
-    select_kernel<<<(T + 7) / 8, 256, 0, st>>>(p.logits, a.x, a.shared_blob ? a.shared_gate : nullptr, T, H, E, k,
-                                               s.norm_topk, p.idx, p.w, p.sigma, a.user_idx, a.user_w, p.x_bf, a.y);
-    ++*launches;
+    if (p.two_stage) {
+        // approximate logits on the tensor cores, exact logits of the candidates
+        if ((e = launch_router_two_stage(s, p, a, st, launches))) return e;
+        if ((e = stamp())) return e;
+    } else {
+        if ((e = launch_logits(a.router_w, a.router_bias, a.x, T, H, E, kLgTokens, p.logits, st))) return e;
+        ++*launches;
+        if ((e = stamp())) return e;
+        select_kernel<<<(T + 7) / 8, 256, 0, st>>>(p.logits, a.x, a.shared_blob ? a.shared_gate : nullptr, T, H, E,
+                                                   k, s.norm_topk, p.idx, p.w, p.sigma, a.user_idx, a.user_w, p.x_bf,
+                                                   a.y);
+        ++*launches;
+    }
     if ((e = stamp())) return e;
     {
         const size_t smem = (size_t)32 * E * sizeof(uint16_t);

@@ -79,6 +79,22 @@ def test_tiny_prefill_zipf_skew_full_and_partial_chunks():
         moe.moe_destroy(ctx)
 
 
+def test_two_stage_router_small():
+    """128 experts (a multiple of 128): the router runs as tensor-core approximate
+    logits plus exact logits of the candidates the error bound leaves; the
+    chosen experts and weights must still equal the exact router's."""
+    w = dataclasses.replace(TINY_ZIPF, n_experts=128, top_k=6)
+    T = 700
+    ctx = workload.create_loaded(w, max_tokens=T)
+    try:
+        x = synth.tokens(w.seed, 21, T, w.hidden)
+        y, idx, wt = _prefill(ctx, w, x)
+        _check(w, x, y, idx, wt)
+        _prefill(ctx, w, x[:5])  # a second call reports any failed device-side check of the first
+    finally:
+        moe.moe_destroy(ctx)
+
+
 def test_tiny_prefill_int8():
     w = dataclasses.replace(TINY, bits=8)
     ctx = workload.create_loaded(w, max_tokens=300)
@@ -209,6 +225,7 @@ def test_80b_prefill_full_size_sampled():
         np.testing.assert_allclose(wt, np.stack([r[2] for r in routes]), rtol=2e-6, atol=1e-7)
         counts = np.bincount(idx.ravel(), minlength=w.n_experts)
         assert counts.sum() == T * w.top_k and counts.max() > 256  # Zipf-skewed: hot experts span chunks
+        _prefill(ctx, w, x[:8])  # reports any failed device-side check of the full call
         rows = np.sort(np.random.default_rng(23).choice(T, 32, replace=False))
         orc = oracle_layer(w, 0, experts=np.unique(idx[rows]))
         ref = orc.tokens(x[rows], prefill=True, threads=16)
