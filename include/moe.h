@@ -251,12 +251,12 @@ int moe_pool_trace(moe_ctx* ctx, int32_t* buf_host, size_t cap, size_t* n_out);
  * recorded since profiling was enabled, the device milliseconds of each
  * kernel, in launch order:
  *   [0] router logits  [1] top-k / weights / shared gate  [2] pair histogram
- *   [3] scan + chunk list  [4] scatter  [5] gate/up grouped GEMM
- *   [6] down grouped GEMM
+ *   [3] scan + chunk lists  [4] scatter  [5] token rows in sorted order
+ *   [6] gate/up grouped GEMM  [7] down grouped GEMM
  * into ms_out[MOE_PREFILL_KERNELS] and the number of calls into *calls.
  * Synchronises with the recorded events.
  */
-#define MOE_PREFILL_KERNELS 7
+#define MOE_PREFILL_KERNELS 8
 int moe_prefill_profile(moe_ctx* ctx, int32_t enable);
 int moe_prefill_kernel_ms(moe_ctx* ctx, double* ms_out, int64_t* calls);
 

@@ -229,7 +229,7 @@ def moe_pool_trace(ctx) -> np.ndarray:
     return buf
 
 
-PREFILL_KERNELS = ("router_logits", "select", "histogram", "scan", "scatter", "gateup_gemm", "down_gemm")
+PREFILL_KERNELS = ("router_logits", "select", "histogram", "scan", "scatter", "gather_x", "gateup_gemm", "down_gemm")
 
 
 def moe_prefill_profile(ctx, enable: bool = True) -> None:

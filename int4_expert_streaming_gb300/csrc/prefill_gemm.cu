@@ -1,34 +1,46 @@
 // prefill_gemm.cu -- the two grouped GEMMs of the prefill path on the 5th
 // generation tensor cores (tcgen05, fp32 accumulators in tensor memory).
 //
-// Work unit ("tile"): one chunk of <= 256 sorted rows of one expert (tokens for
-// the gate/up GEMM, SwiGLU rows for the down GEMM) against 256 weight rows:
-//   mode 0 (gate/up): weight rows s*128 .. s*128+127 of gate AND of up
-//                     (two accumulators), K = hidden; epilogue
+// Work unit ("tile"): one chunk of sorted rows of one expert against 256
+// weight rows, K in blocks of 64:
+//   mode 0 (gate/up): chunk of <= 256 token rows; weight rows s*128 .. +127 of
+//                     gate AND of up (accumulators in tensor-memory columns
+//                     0-255 and 256-511), K = hidden; epilogue
 //                     h = silu(gate) * up in fp32, stored as the bf16 pair
 //                     hi = bf16(h), lo = bf16(h - hi) (h to about 2^-17).
-//   mode 1 (down):    output rows p*256 .. p*256+255 of the down matrix (two
-//                     accumulators of 128 rows), K = inter, every k-block
-//                     multiplied with both hi and lo; epilogue
+//   mode 1 (down):    chunk of <= 128 SwiGLU rows; output rows p*256 .. +255
+//                     of the down matrix (two accumulators of 128 columns,
+//                     double-buffered: columns 0-255 and 256-511), K = inter,
+//                     every k-block multiplied with both hi and lo; epilogue
 //                     y[token] += weight * acc (fp32 reductions in L2).
-// The MMA computes D[128 x N] = A[128 x 64] * B[N x 64]^T per 64-wide k-block,
-// A = dequantised weights, B = activation rows, N = rows rounded up to 16.
+// The MMA computes D[128 x N] = A[128 x 64] * B[N x 64]^T per k-block, A =
+// dequantised weights, B = activation rows, N = rows rounded up to 16.
 //
-// Warp roles of each persistent CTA (one per SM):
+// Warp roles of each persistent CTA (one per SM, 26 warps):
 //   warp 0        one thread issues the MMAs and the commits
-//   warps 1-4     epilogue: tensor memory -> registers -> global (warp w reads
-//                 tensor-memory lanes 32*(w%4) .. +31)
-//   warps 5-12    producers, two groups of four warps taking alternate
-//                 k-blocks: load the packed codes and scale/bias, dequantise
-//                 to bf16(fp32 fma(scale, q, bias)) and write them as
-//                 128-byte-swizzled K-major tiles; mode 0 also gathers the
-//                 token rows of bf16(x) the same way, mode 1 bulk-copies the
-//                 SwiGLU rows, which the gate/up epilogue stored already
-//                 swizzled (one copy per operand per k-block).
-// Stage hand-off uses mbarriers (full: producers -> MMA, empty: MMA commit ->
-// producers; accumulator full/empty between MMA and epilogue).  Every wait is
-// bounded; a wait that runs out records a status word in mapped host memory
-// and the CTA winds down, draining its MMAs and freeing its tensor memory.
+//   warp 1        B loader, a 3-stage ring ahead of the MMA: mode 0 copies
+//                 the chunk's token rows (bf16(x) in sorted pair order, or in
+//                 token order for the shared expert) with TMA, boxes of 64 rows
+//                 x 64 columns landing 128-byte swizzled; mode 1 bulk-copies
+//                 the SwiGLU rows, which the gate/up epilogue stored already
+//                 swizzled
+//   warps 2-9     epilogue: tensor memory -> registers -> global; warp w reads
+//                 tensor-memory lanes 32*(w%4) .. +31, the two warps of a lane
+//                 quarter take alternate 16-column groups
+//   warps 10-25   dequantisers, two threads per weight row (32 columns each):
+//                 each thread stages its own packed codes and scale/bias
+//                 several k-blocks ahead with cp.async (a private ring, so no
+//                 barrier), then writes bf16(fp32 fma(scale, q, bias)) into
+//                 the swizzled A tile of a 3-stage ring (2 for int8)
+// Stage hand-off uses mbarriers (A/B full: producers -> MMA; one "k-block
+// done" commit per k-block into a ring of 6, on which the A producers wait two
+// k-blocks later and the B loader three; accumulator full/empty between MMA
+// and epilogue).  The MMA thread shares its issue slots with busy warps, so
+// its loop is kept short: descriptors are a fixed high word and a low word
+// stepped by adds, stage and phase counters advance without division.
+// Every wait is bounded; a wait that runs out records a status word in mapped
+// host memory and the CTA winds down, draining its MMAs and copies and freeing
+// its tensor memory.
 //
 // MLX affine group quantisation (Swiftlet README, "Relation to
 // TurboFieldfare"): w = scale * q + bias per 64-column group.  The tensor-core
@@ -44,72 +56,134 @@ namespace {
 
 using namespace umma;
 
-constexpr int kGemmThreads = 416;
-constexpr int kGroupThreads = 128;
-constexpr int kTileBytes = 16 * 1024;  // 128 rows x 64 bf16 (one 256-row operand = 2 tiles)
-constexpr int kTmemCols = 512;         // two accumulators of up to 256 columns
+constexpr int kLoadWarp = 1;
+constexpr int kEpiWarp0 = 2, kEpiWarps = 8;
+constexpr int kDqWarp0 = 10, kDqWarps = 16;
+constexpr int kThreads = 32 * (kDqWarp0 + kDqWarps);  // 832
+constexpr int kDqThreads = 32 * kDqWarps;             // two per weight row
+constexpr int kTileBytes = 16 * 1024;                  // 128 rows x 64 bf16
+constexpr int kStageBytes = 2 * kTileBytes;            // two weight tiles, 256 token rows, or hi + lo of 128 rows
+constexpr int kBStages = 3;
+constexpr int kDone = 6;  // k-block done ring: a multiple of both stage counts
+constexpr int kTmemCols = 512;
+constexpr int kOffB = 0;  // shared-memory map from a 1024-byte aligned base: B ring, A ring, code ring
 
-template <int MODE>
-struct Cfg;
-template <>
-struct Cfg<0> {  // A0 | A1 | B
-    static constexpr int kStages = 3, kStageBytes = 4 * kTileBytes;
+// Shared memory per code width: the A ring (3 stages for int4, 2 for int8) and
+// the dequantisers' private code ring: per thread and k-block, 32 packed
+// weights (16 bytes int4, 32 bytes int8 as two 16-byte parts) and the
+// scale/bias word.
+template <int BITS>
+struct Ring {
+    static constexpr int kAStages = BITS == 4 ? 3 : 2;
+    static constexpr int kParts = BITS / 4;  // 16-byte parts per thread
+    static constexpr int kSlotBytes = kDqThreads * (16 * kParts + 4);
+    static constexpr int kSlots = 3;
+    static constexpr int kOffA = kOffB + kBStages * kStageBytes;
+    static constexpr int kOffCodes = kOffA + kAStages * kStageBytes;
+    static constexpr int kSmem = kOffCodes + kSlots * kSlotBytes;
 };
-template <>
-struct Cfg<1> {  // A0 | A1 | B hi | B lo
-    static constexpr int kStages = 2, kStageBytes = 6 * kTileBytes;
-};
+static_assert(kDone % 2 == 0 && kDone % 3 == 0, "done ring");
+static_assert(Ring<4>::kSmem + 1024 + 512 <= 227 * 1024, "shared memory");
+static_assert(Ring<8>::kSmem + 1024 + 512 <= 227 * 1024, "shared memory");
 
 struct GemmArgs {
-    int H, E, k, T, P;  // P = T * k
-    int inter, shared_inter, slices0, h_rows;
-    int x_stride;  // elements between token rows of x_bf
-    const int4* chunks;
+    int H, E, T;
+    int inter, shared_inter;
+    int per;  // tiles per chunk: mode 0 inter slices of 128, mode 1 output slices of 256
+    int h_rows;
+    const ChunkRec* chunks;
     const int32_t* n_chunks;
-    const int32_t* perm;
-    const uint16_t* x_bf;
+    const int32_t* tok_sorted;
+    const float* w_sorted;
     uint16_t* h_hi;
     uint16_t* h_lo;
-    const float* w;
     const float* sigma;
     float* y;
-    const uint8_t* const* dir;
-    const uint8_t* shared_blob;
     int* status;
     unsigned long long timeout_ns;
 };
 
-struct Tile {
-    int e, row0, n, hrow0, sub, kb;
+struct TileInfo {
+    int e, row0, n, hrow0, sub;
     const uint8_t* blob;
 };
 
-template <int MODE>
-__device__ __forceinline__ bool tile_at(const GemmArgs& a, int t, Tile& tl) {
-    const int per = MODE == 0 ? a.slices0 : a.H / 256;
-    const int4 c = a.chunks[t / per];
-    tl.e = c.x;
-    tl.row0 = c.y;
-    tl.n = c.z;
-    tl.hrow0 = c.w;
-    tl.sub = t % per;
-    const bool sh = tl.e == a.E;
-    const int inter_e = sh ? a.shared_inter : a.inter;
-    if (MODE == 0) {
-        if (tl.sub * 128 >= inter_e) return false;
-        tl.kb = a.H / 64;
-    } else {
-        tl.kb = inter_e / 64;
-    }
-    tl.blob = sh ? a.shared_blob : a.dir[tl.e];
-    return tl.blob != nullptr;
-}
-
 __device__ __forceinline__ int n_pad(int n) { return n < 16 ? 16 : (n + 15) & ~15; }
+
+// The CTA's tiles t = blockIdx.x + i * gridDim.x, each with its chunk record;
+// the record of the following tile is loaded one tile ahead, so moving on does
+// not wait for memory.
+template <int MODE>
+struct Tiles {
+    int t, pref_t;
+    int4 pc, pb;  // raw record of tile pref_t
+    TileInfo cur;
+
+    __device__ __forceinline__ static void load(const GemmArgs& a, int t, int4& c, int4& b) {
+        const int4* r = reinterpret_cast<const int4*>(a.chunks + t / a.per);
+        c = __ldg(r);
+        b = __ldg(r + 1);
+    }
+    __device__ __forceinline__ bool decode(const GemmArgs& a, int4 c, int4 b) {
+        cur.e = c.x;
+        cur.row0 = c.y;
+        cur.n = c.z;
+        cur.hrow0 = c.w;
+        cur.sub = t % a.per;
+        cur.blob = reinterpret_cast<const uint8_t*>((unsigned long long)(uint32_t)b.x |
+                                                    ((unsigned long long)(uint32_t)b.y << 32));
+        if (!cur.blob) return false;
+        if (MODE == 0) return cur.sub * 128 < (cur.e == a.E ? a.shared_inter : a.inter);
+        return true;
+    }
+    // moves to the next valid tile; false past the end
+    __device__ __forceinline__ bool next(const GemmArgs& a, int n_tiles) {
+        for (;;) {
+            t += gridDim.x;
+            if (t >= n_tiles) return false;
+            int4 c, b;
+            if (pref_t == t) {
+                c = pc;
+                b = pb;
+            } else {
+                load(a, t, c, b);
+            }
+            pref_t = t + gridDim.x;
+            if (pref_t < n_tiles) load(a, pref_t, pc, pb);
+            if (decode(a, c, b)) return true;
+        }
+    }
+    __device__ __forceinline__ bool first(const GemmArgs& a, int n_tiles) {
+        t = (int)blockIdx.x - (int)gridDim.x;
+        pref_t = -1;
+        return next(a, n_tiles);
+    }
+    __device__ __forceinline__ int kblocks(const GemmArgs& a) const {
+        return (MODE == 0 ? a.H : (cur.e == a.E ? a.shared_inter : a.inter)) / 64;
+    }
+};
 
 __device__ __forceinline__ void fail(const GemmArgs& a, volatile int* abort, int code) {
     *abort = 1;
     *(volatile int*)a.status = code;
+}
+
+// D (+)= A * B^T with both descriptors given as (low, high) words
+__device__ __forceinline__ void mma_bf16_w(uint32_t d, uint32_t alo, uint32_t blo, uint32_t dhi, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n .reg .b64 ad, bd;\n mov.b64 ad, {%1, %3};\n mov.b64 bd, {%2, %3};\n setp.ne.b32 p, %5, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %4, p;\n}" ::"r"(d),
+        "r"(alo), "r"(blo), "r"(dhi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// bounded wait taken by lane 0 for the whole warp
+__device__ __forceinline__ bool warp_wait(uint64_t* b, uint32_t parity, const GemmArgs& a, volatile int* abort,
+                                          int lane) {
+    int ok = 1;
+    if (lane == 0) ok = bar_wait(b, parity, a.timeout_ns, abort) ? 1 : 0;
+    return __shfl_sync(kFullMask, ok, 0) != 0;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -118,145 +192,94 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return r;
 }
 
-// code byte i of v as an exact float: bits 0x4B0000qq = 2^23 + q
-__device__ __forceinline__ float code_f(uint32_t v, int i) {
-    return __fsub_rn(__uint_as_float(__byte_perm(v, 0x4B000000u, 0x7440u | (uint32_t)i)), 8388608.0f);
+// packed fp32 pairs (one register pair, two IEEE operations per instruction)
+__device__ __forceinline__ uint64_t f2(uint32_t lo, uint32_t hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+__device__ __forceinline__ uint64_t add_f2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t fma_f2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint32_t bf16x2_of(uint64_t v) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return pack_bf16(lo, hi);
 }
 
-// bf16(fma(s, q, b)) of 8 consecutive int4 columns (one code word)
-__device__ __forceinline__ uint4 dq8_int4(uint32_t wd, float s, float b) {
+// code byte i of v as the bits of the float 2^23 + q (exact)
+__device__ __forceinline__ uint32_t code_bits(uint32_t v, int i) { return __byte_perm(v, 0x4B000000u, 0x7440u | i); }
+
+// bf16(fma(s, q, b)) of code bytes (x byte i, y byte j) as a bf16 pair;
+// m2 = (-2^23, -2^23)
+__device__ __forceinline__ uint32_t dq_pair(uint32_t x, int i, uint32_t y, int j, uint64_t s2, uint64_t b2,
+                                            uint64_t m2) {
+    return bf16x2_of(fma_f2(s2, add_f2(f2(code_bits(x, i), code_bits(y, j)), m2), b2));
+}
+
+// 8 consecutive int4 columns (one code word, column c in nibble c)
+__device__ __forceinline__ uint4 dq8_int4(uint32_t wd, uint64_t s2, uint64_t b2, uint64_t m2) {
     const uint32_t lo = wd & 0x0F0F0F0Fu, hi = (wd >> 4) & 0x0F0F0F0Fu;  // even / odd columns
-    uint4 o;
-    o.x = pack_bf16(__fmaf_rn(s, code_f(lo, 0), b), __fmaf_rn(s, code_f(hi, 0), b));
-    o.y = pack_bf16(__fmaf_rn(s, code_f(lo, 1), b), __fmaf_rn(s, code_f(hi, 1), b));
-    o.z = pack_bf16(__fmaf_rn(s, code_f(lo, 2), b), __fmaf_rn(s, code_f(hi, 2), b));
-    o.w = pack_bf16(__fmaf_rn(s, code_f(lo, 3), b), __fmaf_rn(s, code_f(hi, 3), b));
-    return o;
+    return make_uint4(dq_pair(lo, 0, hi, 0, s2, b2, m2), dq_pair(lo, 1, hi, 1, s2, b2, m2),
+                      dq_pair(lo, 2, hi, 2, s2, b2, m2), dq_pair(lo, 3, hi, 3, s2, b2, m2));
 }
 
-// ... of 8 consecutive int8 columns (two code words)
-__device__ __forceinline__ uint4 dq8_int8(uint32_t w0, uint32_t w1, float s, float b) {
-    uint4 o;
-    o.x = pack_bf16(__fmaf_rn(s, code_f(w0, 0), b), __fmaf_rn(s, code_f(w0, 1), b));
-    o.y = pack_bf16(__fmaf_rn(s, code_f(w0, 2), b), __fmaf_rn(s, code_f(w0, 3), b));
-    o.z = pack_bf16(__fmaf_rn(s, code_f(w1, 0), b), __fmaf_rn(s, code_f(w1, 1), b));
-    o.w = pack_bf16(__fmaf_rn(s, code_f(w1, 2), b), __fmaf_rn(s, code_f(w1, 3), b));
-    return o;
+// 8 consecutive int8 columns (two code words, column c in byte c)
+__device__ __forceinline__ uint4 dq8_int8(uint32_t w0, uint32_t w1, uint64_t s2, uint64_t b2, uint64_t m2) {
+    return make_uint4(dq_pair(w0, 0, w0, 1, s2, b2, m2), dq_pair(w0, 2, w0, 3, s2, b2, m2),
+                      dq_pair(w1, 0, w1, 1, s2, b2, m2), dq_pair(w1, 2, w1, 3, s2, b2, m2));
 }
 
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
 }
-
-__device__ __forceinline__ uint4 ldg_nc(const void* p) {
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
     uint4 v;
-    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
     return v;
 }
-
-// Producer-side position in the CTA's sequence of (tile, k-block) iterations.
-struct Cursor {
-    int t;        // tile index (global), -1 = past the end
-    int kb;       // k-block within the tile
-    uint32_t it;  // iteration number within the CTA
-    Tile tl;
-};
-
-template <int MODE>
-__device__ __forceinline__ void cursor_first(const GemmArgs& a, int n_tiles, Cursor& c) {
-    c.it = 0;
-    c.kb = 0;
-    for (c.t = blockIdx.x; c.t < n_tiles; c.t += gridDim.x)
-        if (tile_at<MODE>(a, c.t, c.tl)) return;
-    c.t = -1;
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
 }
-
-template <int MODE>
-__device__ __forceinline__ void cursor_next(const GemmArgs& a, int n_tiles, Cursor& c) {
-    if (c.t < 0) return;
-    ++c.it;
-    if (++c.kb < c.tl.kb) return;
-    c.kb = 0;
-    for (c.t += gridDim.x; c.t < n_tiles; c.t += gridDim.x)
-        if (tile_at<MODE>(a, c.t, c.tl)) return;
-    c.t = -1;
-}
-
-// Per producer thread: its 16-byte code units of the two 128-row weight tiles
-// of one k-block (unit u = gt + 128 i: tile u / (128 U), row (u / U) % 128,
-// part u % U, with U = 16-byte units per row per k-block) and their scale/bias.
-template <int BITS>
-struct ProdRegs {
-    static constexpr int U = BITS / 2;
-    static constexpr int kUnitsA = 2 * 128 * U / kGroupThreads;
-    uint4 qa[kUnitsA];
-    uint32_t sba[kUnitsA];
-};
-
-template <int MODE, int BITS>
-__device__ __forceinline__ void prod_load(const GemmArgs& a, const Cursor& c, int gt, ProdRegs<BITS>& R) {
-    using PR = ProdRegs<BITS>;
-    const Tile& tl = c.tl;
-    const int inter_e = tl.e == a.E ? a.shared_inter : a.inter;
-    const BlobLayout L = blob_layout(a.H, inter_e, BITS);
-    const int K = MODE == 0 ? a.H : inter_e;
-    const size_t rowbytes = (size_t)K * BITS / 8;
-    const int groups = K / 64;
-#pragma unroll
-    for (int i = 0; i < PR::kUnitsA; ++i) {
-        const int u = gt + kGroupThreads * i;
-        const int m = u / (128 * PR::U), r = (u / PR::U) % 128, part = u % PR::U;
-        int row;
-        uint64_t qoff, sboff;
-        if (MODE == 0) {
-            row = tl.sub * 128 + r;
-            qoff = m ? L.up_q : L.gate_q;
-            sboff = m ? L.up_sb : L.gate_sb;
-        } else {
-            row = tl.sub * 256 + m * 128 + r;
-            qoff = L.down_q;
-            sboff = L.down_sb;
-        }
-        R.qa[i] = ldg_nc(tl.blob + qoff + row * rowbytes + (size_t)c.kb * 64 * BITS / 8 + part * 16);
-        R.sba[i] = __ldg(reinterpret_cast<const uint32_t*>(tl.blob + sboff) + (size_t)row * groups + c.kb);
-    }
-}
-
-template <int BITS>
-__device__ __forceinline__ void prod_store(int gt, uint32_t stage, const ProdRegs<BITS>& R) {
-    using PR = ProdRegs<BITS>;
-#pragma unroll
-    for (int i = 0; i < PR::kUnitsA; ++i) {
-        const int u = gt + kGroupThreads * i;
-        const int m = u / (128 * PR::U), r = (u / PR::U) % 128, part = u % PR::U;
-        const uint32_t tile = stage + m * kTileBytes;
-        const float s = __half2float(__ushort_as_half((unsigned short)(R.sba[i] & 0xffffu)));
-        const float b = __half2float(__ushort_as_half((unsigned short)(R.sba[i] >> 16)));
-        if (BITS == 4) {
-            sts128(tile + swz_chunk(r, part * 4 + 0), dq8_int4(R.qa[i].x, s, b));
-            sts128(tile + swz_chunk(r, part * 4 + 1), dq8_int4(R.qa[i].y, s, b));
-            sts128(tile + swz_chunk(r, part * 4 + 2), dq8_int4(R.qa[i].z, s, b));
-            sts128(tile + swz_chunk(r, part * 4 + 3), dq8_int4(R.qa[i].w, s, b));
-        } else {
-            sts128(tile + swz_chunk(r, part * 2 + 0), dq8_int8(R.qa[i].x, R.qa[i].y, s, b));
-            sts128(tile + swz_chunk(r, part * 2 + 1), dq8_int8(R.qa[i].z, R.qa[i].w, s, b));
-        }
-    }
-}
-
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
-// arrive on the mbarrier once this thread's earlier cp.async copies have landed
-__device__ __forceinline__ void cp_async_arrive(uint64_t* b) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(b)) : "memory");
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
-
-// token of sorted row j of a gate/up tile
-__device__ __forceinline__ int token_row(const GemmArgs& a, const Tile& tl, int j) {
-    if (j >= tl.n) return 0;
-    return tl.e == a.E ? tl.row0 + j : a.perm[tl.row0 + j] / a.k;
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// TMA: the box at (column x, row y) of a 2D map to shared memory, completion
+// counted on the mbarrier
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* b) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"(map), "r"(x), "r"(y), "r"(smem_u32(b))
+        : "memory");
+}
+__device__ __forceinline__ void bar_arrive_expect_tx(uint64_t* b, uint32_t bytes) {
+    asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 st, [%0], %1;\n}" ::"r"(
+                     smem_u32(b)),
+                 "r"(bytes)
+                 : "memory");
 }
 
 // element offset of (row, col) in a pre-swizzled SwiGLU buffer: planes of 64
@@ -265,32 +288,73 @@ __device__ __forceinline__ size_t h_offset(int rows, int row, int col) {
     return ((size_t)(col >> 6) * rows + row) * 64 + ((((col >> 3) ^ row) & 7) << 3) + (col & 7);
 }
 
+// 32 lanes x 16 consecutive 32-bit tensor-memory columns
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+          "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr));
+}
+
+// Dequantiser thread (weight row r of the tile, column half hf): the address
+// of its codes and of its row's scale/bias words in the tile's expert blob.
 template <int MODE, int BITS>
-__global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(GemmArgs a) {
-    constexpr int S = Cfg<MODE>::kStages, SB = Cfg<MODE>::kStageBytes;
+__device__ __forceinline__ void code_src(const GemmArgs& a, const TileInfo& ti, int r, int hf, const uint8_t*& q,
+                                         const uint8_t*& sb) {
+    const int inter_e = ti.e == a.E ? a.shared_inter : a.inter;
+    const BlobLayout L = blob_layout(a.H, inter_e, BITS);
+    const int K = MODE == 0 ? a.H : inter_e;
+    const size_t rowbytes = (size_t)K * BITS / 8;
+    int row;
+    uint64_t qoff, sboff;
+    if (MODE == 0) {
+        const int m = r >> 7;
+        row = ti.sub * 128 + (r & 127);
+        qoff = m ? L.up_q : L.gate_q;
+        sboff = m ? L.up_sb : L.gate_sb;
+    } else {
+        row = ti.sub * 256 + r;
+        qoff = L.down_q;
+        sboff = L.down_sb;
+    }
+    q = ti.blob + qoff + row * rowbytes + hf * 4 * BITS;
+    sb = ti.blob + sboff + (size_t)row * (K / 64) * 4;
+}
+
+template <int MODE, int BITS>
+__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ CUtensorMap x_map,
+                                                                   const __grid_constant__ CUtensorMap xs_map, GemmArgs a) {
+    using RG = Ring<BITS>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ uint64_t full_bar[S], empty_bar[S], accf_bar, acce_bar, drain_bar;
+    constexpr int kAStages = RG::kAStages;
+    __shared__ uint64_t a_full[kAStages], b_full[kBStages], kb_done[kDone];
+    __shared__ uint64_t acc_full[2], acc_empty[2], drain_bar;
     __shared__ uint32_t tmem_base_s;
-    __shared__ volatile int abort_s;
+    __shared__ volatile int abort_s, never_s;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t smem0 = (smem_u32(smem_raw) + 1023u) & ~1023u;
-    const int n_tiles = *a.n_chunks * (MODE == 0 ? a.slices0 : a.H / 256);
+    const int n_tiles = a.n_chunks[MODE] * a.per;
 
     if (tid == 0) {
-        for (int s = 0; s < S; ++s) {
-            // four producer warps, plus (gate/up) one asynchronous arrival per
-            // producer thread when its token-row copies have landed
-            bar_init(&full_bar[s], MODE == 0 ? 4 + kGroupThreads : 4);
-            bar_init(&empty_bar[s], 1);
+        for (int s = 0; s < kAStages; ++s) bar_init(&a_full[s], kDqWarps);
+        for (int s = 0; s < kBStages; ++s) bar_init(&b_full[s], 1);
+        for (int s = 0; s < kDone; ++s) bar_init(&kb_done[s], 1);
+        for (int s = 0; s < 2; ++s) {
+            bar_init(&acc_full[s], 1);
+            bar_init(&acc_empty[s], kEpiWarps);
         }
-        bar_init(&accf_bar, 1);
-        bar_init(&acce_bar, 4);
         bar_init(&drain_bar, 1);
         abort_s = 0;
+        never_s = 0;
         fence_barrier_init();
     }
     if (warp == 0) tmem_alloc(&tmem_base_s, kTmemCols);
+    // operand rows past a chunk's last row are never written; keep them finite
+    for (int i = tid; i < kBStages * kStageBytes / 16; i += kThreads)
+        sts128(smem0 + kOffB + 16 * i, make_uint4(0, 0, 0, 0));
+    fence_proxy_async_smem();
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -299,98 +363,191 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(GemmArgs 
     if (warp == 0) {
         // ------------------------------------------------------------------ MMA
         if (lane == 0) {
-            uint32_t it = 0, acc = 0;
+            uint32_t tc = 0, sa = 0, pa = 0, sb = 0, pb = 0, sd = 0;
+            const uint32_t dhi = (uint32_t)(sdesc(smem0) >> 32);  // the same for every operand tile
+            const uint32_t a_lo = (uint32_t)sdesc(smem0 + RG::kOffA), b_lo = (uint32_t)sdesc(smem0 + kOffB);
+            constexpr uint32_t kTileLo = kTileBytes >> 4, kStageLo = kStageBytes >> 4;
             bool ok = true;
-            for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-                Tile tl;
-                if (!tile_at<MODE>(a, t, tl)) continue;
-                if (!bar_wait(&acce_bar, (acc & 1u) ^ 1u, a.timeout_ns, &abort_s)) {
+            Tiles<MODE> tiles;
+            for (bool has = tiles.first(a, n_tiles); has && ok; has = tiles.next(a, n_tiles), ++tc) {
+                const TileInfo& ti = tiles.cur;
+                const uint32_t ab = MODE == 0 ? 0u : (tc & 1u);
+                const uint32_t use = MODE == 0 ? tc : (tc >> 1);
+                if (!bar_wait(&acc_empty[ab], (use & 1u) ^ 1u, a.timeout_ns, &abort_s)) {
                     fail(a, &abort_s, 2);
                     break;
                 }
                 fence_after_sync();
-                const uint32_t idesc = idesc_bf16(128, n_pad(tl.n));
-                for (int kb = 0; kb < tl.kb; ++kb, ++it) {
-                    const uint32_t s = it % S;
-                    if (!bar_wait(&full_bar[s], (it / S) & 1u, a.timeout_ns, &abort_s)) {
+                const uint32_t idesc = idesc_bf16(128, n_pad(ti.n));
+                const uint32_t d0 = tmem + (MODE == 0 ? 0u : ab * 256);
+                const int nkb = tiles.kblocks(a);
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!bar_wait(&a_full[sa], pa, a.timeout_ns, &abort_s) ||
+                        !bar_wait(&b_full[sb], pb, a.timeout_ns, &abort_s)) {
                         fail(a, &abort_s, 2);
                         ok = false;
                         break;
                     }
                     fence_after_sync();
-                    fence_proxy_async_smem();  // the token rows were written by cp.async (generic proxy)
-                    const uint32_t st = smem0 + s * SB;
+                    const uint32_t al = a_lo + sa * kStageLo, bl = b_lo + sb * kStageLo;
+                    const uint32_t acc0 = kb ? 1u : 0u;
 #pragma unroll
                     for (int m = 0; m < 2; ++m)
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t ad = sdesc(st + m * kTileBytes + kk * 32);
-                            mma_bf16(tmem + m * 256, ad, sdesc(st + 2 * kTileBytes + kk * 32), idesc,
-                                     (kb | kk) ? 1u : 0u);
-                            if (MODE == 1) mma_bf16(tmem + m * 256, ad, sdesc(st + 4 * kTileBytes + kk * 32), idesc, 1u);
+                            const uint32_t am = al + m * kTileLo + 2 * kk;
+                            if (MODE == 0) {
+                                mma_bf16_w(d0 + m * 256, am, bl + 2 * kk, dhi, idesc, kk ? 1u : acc0);
+                            } else {
+                                mma_bf16_w(d0 + m * 128, am, bl + 2 * kk, dhi, idesc, kk ? 1u : acc0);
+                                mma_bf16_w(d0 + m * 128, am, bl + kTileLo + 2 * kk, dhi, idesc, 1u);
+                            }
                         }
-                    mma_commit(&empty_bar[s]);
+                    mma_commit(&kb_done[sd]);
+                    sd = sd == kDone - 1 ? 0 : sd + 1;
+                    if (++sa == kAStages) {
+                        sa = 0;
+                        pa ^= 1u;
+                    }
+                    if (++sb == kBStages) {
+                        sb = 0;
+                        pb ^= 1u;
+                    }
                 }
                 if (!ok) break;
-                mma_commit(&accf_bar);
-                ++acc;
+                mma_commit(&acc_full[ab]);
             }
             // every MMA issued above has completed once this commit arrives
             mma_commit(&drain_bar);
-            if (!bar_wait(&drain_bar, 0, a.timeout_ns, &abort_s)) fail(a, &abort_s, 2);
+            if (!bar_wait(&drain_bar, 0, a.timeout_ns, &never_s)) fail(a, &abort_s, 2);
         }
         __syncwarp();
-    } else if (warp <= 4) {
+    } else if (warp == kLoadWarp) {
+        // ------------------------------------------------------------- B loader
+        uint32_t it = 0;
+        Tiles<MODE> tiles;
+        if constexpr (MODE == 0) {
+            // one thread: per k-block, ceil(n / 64) boxes of 64 rows
+            if (lane == 0) {
+                for (bool has = tiles.first(a, n_tiles); has; has = tiles.next(a, n_tiles)) {
+                    const TileInfo& ti = tiles.cur;
+                    const CUtensorMap* map = ti.e == a.E ? &x_map : &xs_map;
+                    const int nb = (ti.n + 63) >> 6;
+                    const int nkb = tiles.kblocks(a);
+                    bool ok = true;
+                    for (int kb = 0; kb < nkb; ++kb, ++it) {
+                        const uint32_t s = it % kBStages;
+                        // stage s was last read by the MMAs of k-block it - kBStages
+                        if (it >= kBStages && !bar_wait(&kb_done[(it - kBStages) % kDone],
+                                                        ((it - kBStages) / kDone) & 1u, a.timeout_ns, &abort_s)) {
+                            fail(a, &abort_s, 4);
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t bs = smem0 + kOffB + s * kStageBytes;
+                        bar_arrive_expect_tx(&b_full[s], (uint32_t)nb * 8192u);
+                        for (int q = 0; q < nb; ++q) tma_load_2d(bs + q * 8192, map, kb * 64, ti.row0 + 64 * q, &b_full[s]);
+                    }
+                    if (!ok) break;
+                }
+                // copies still in flight land before the CTA exits
+                for (uint32_t i = it > kBStages ? it - kBStages : 0; i < it; ++i)
+                    bar_wait(&b_full[i % kBStages], (i / kBStages) & 1u, a.timeout_ns, &never_s);
+            }
+            __syncwarp();
+        } else {
+            // one thread: the hi and lo rows of a k-block, two bulk copies
+            if (lane == 0) {
+                for (bool has = tiles.first(a, n_tiles); has; has = tiles.next(a, n_tiles)) {
+                    const TileInfo& ti = tiles.cur;
+                    const uint32_t bytes = (uint32_t)n_pad(ti.n) * 128u;
+                    const int nkb = tiles.kblocks(a);
+                    bool ok = true;
+                    for (int kb = 0; kb < nkb; ++kb, ++it) {
+                        const uint32_t s = it % kBStages;
+                        // stage s was last read by the MMAs of k-block it - kBStages
+                        if (it >= kBStages && !bar_wait(&kb_done[(it - kBStages) % kDone],
+                                                        ((it - kBStages) / kDone) & 1u, a.timeout_ns, &abort_s)) {
+                            fail(a, &abort_s, 4);
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t bs = smem0 + kOffB + s * kStageBytes;
+                        const size_t src = ((size_t)kb * a.h_rows + ti.hrow0) * 64;
+                        bar_arrive_expect_tx(&b_full[s], 2 * bytes);
+                        bulk_g2s(bs, a.h_hi + src, bytes, &b_full[s]);
+                        bulk_g2s(bs + kTileBytes, a.h_lo + src, bytes, &b_full[s]);
+                    }
+                    if (!ok) break;
+                }
+                // copies still in flight land before the CTA exits
+                for (uint32_t i = it > kBStages ? it - kBStages : 0; i < it; ++i)
+                    bar_wait(&b_full[i % kBStages], (i / kBStages) & 1u, a.timeout_ns, &never_s);
+            }
+            __syncwarp();
+        }
+    } else if (warp < kDqWarp0) {
         // ------------------------------------------------------------- epilogue
-        const int q = warp & 3;
+        const int q = warp & 3, hh = (warp - kEpiWarp0) >> 2;
         const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
-        uint32_t acc = 0;
-        for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
-            Tile tl;
-            if (!tile_at<MODE>(a, t, tl)) continue;
-            if (!bar_wait(&accf_bar, acc & 1u, a.timeout_ns, &abort_s)) {
+        uint32_t tc = 0;
+        Tiles<MODE> tiles;
+        for (bool has = tiles.first(a, n_tiles); has; has = tiles.next(a, n_tiles), ++tc) {
+            const TileInfo& ti = tiles.cur;
+            const uint32_t ab = MODE == 0 ? 0u : (tc & 1u);
+            const uint32_t use = MODE == 0 ? tc : (tc >> 1);
+            const bool sh = ti.e == a.E;
+            // mode 1: token and weight of this warp's columns 16 hh + 32 s + i
+            // (step s = 0..3, i = 0..15): lane l holds s = l >> 4 (set A) and
+            // s = 2 + (l >> 4) (set B), column i = l & 15
+            int tokA = 0, tokB = 0;
+            float wA = 0.0f, wB = 0.0f;
+            if constexpr (MODE == 1) {
+                const int ca = 16 * hh + 32 * (lane >> 4) + (lane & 15), cb = ca + 64;
+                if (ca < ti.n) {
+                    tokA = sh ? ti.row0 + ca : __ldg(a.tok_sorted + ti.row0 + ca);
+                    wA = sh ? __ldg(a.sigma + ti.row0 + ca) : __ldg(a.w_sorted + ti.row0 + ca);
+                }
+                if (cb < ti.n) {
+                    tokB = sh ? ti.row0 + cb : __ldg(a.tok_sorted + ti.row0 + cb);
+                    wB = sh ? __ldg(a.sigma + ti.row0 + cb) : __ldg(a.w_sorted + ti.row0 + cb);
+                }
+            }
+            if (!warp_wait(&acc_full[ab], use & 1u, a, &abort_s, lane)) {
                 fail(a, &abort_s, 3);
                 break;
             }
             fence_after_sync();
-            const bool sh = tl.e == a.E;
-            for (int c0 = 0; c0 < tl.n; c0 += 32) {
-                uint32_t d0[32], d1[32];
-                tmem_ld32(trow + c0, d0);
-                tmem_ld32(trow + 256 + c0, d1);
-                tmem_ld_wait();
-                const int nc = min(32, tl.n - c0);
+            for (int c0 = 16 * hh, si = 0; c0 < ti.n; c0 += 32, ++si) {
+                uint32_t d0[16], d1[16];
+                const int nc = min(16, ti.n - c0);
                 if constexpr (MODE == 0) {
-                    const int col = tl.sub * 128 + 32 * q + lane;
+                    tmem_ld16(trow + c0, d0);
+                    tmem_ld16(trow + 256 + c0, d1);
+                    tmem_ld_wait();
+                    const int col = ti.sub * 128 + 32 * q + lane;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
+                    for (int j = 0; j < 16; ++j) {
                         if (j < nc) {
                             const float v = silu_mul(__uint_as_float(d0[j]), __uint_as_float(d1[j]));
                             const __nv_bfloat16 hi = __float2bfloat16_rn(v);
                             const __nv_bfloat16 lo = __float2bfloat16_rn(__fsub_rn(v, __bfloat162float(hi)));
-                            const size_t off = h_offset(a.h_rows, tl.hrow0 + c0 + j, col);
+                            const size_t off = h_offset(a.h_rows, ti.hrow0 + c0 + j, col);
                             a.h_hi[off] = __bfloat16_as_ushort(hi);
                             a.h_lo[off] = __bfloat16_as_ushort(lo);
                         }
                     }
                 } else {
-                    int tok = 0;
-                    float wt = 0.0f;
-                    if (lane < nc) {
-                        if (sh) {
-                            tok = tl.row0 + c0 + lane;
-                            wt = a.sigma[tok];
-                        } else {
-                            const int pair = a.perm[tl.row0 + c0 + lane];
-                            tok = pair / a.k;
-                            wt = a.w[pair];
-                        }
-                    }
-                    float* y0 = a.y + tl.sub * 256 + 32 * q + lane;
+                    tmem_ld16(trow + ab * 256 + c0, d0);
+                    tmem_ld16(trow + ab * 256 + 128 + c0, d1);
+                    tmem_ld_wait();
+                    const int tsrc = (si >> 1) ? tokB : tokA;
+                    const float wsrc = (si >> 1) ? wB : wA;
+                    float* y0 = a.y + ti.sub * 256 + 32 * q + lane;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int tj = __shfl_sync(kFullMask, tok, j);
-                        const float wj = __shfl_sync(kFullMask, wt, j);
+                    for (int j = 0; j < 16; ++j) {
+                        const int tj = __shfl_sync(kFullMask, tsrc, 16 * (si & 1) + j);
+                        const float wj = __shfl_sync(kFullMask, wsrc, 16 * (si & 1) + j);
                         if (j < nc) {
                             float* yr = y0 + (size_t)tj * a.H;
                             atomicAdd(yr, wj * __uint_as_float(d0[j]));
@@ -401,80 +558,83 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(GemmArgs 
             }
             fence_before_sync();
             __syncwarp();
-            if (lane == 0) bar_arrive(&acce_bar);
-            ++acc;
+            if (lane == 0) bar_arrive(&acc_empty[ab]);
         }
     } else {
-        // ------------------------------------------------------------ producers
-        // Two register sets of packed codes, each loaded two own iterations
-        // (four k-blocks) before it is dequantised.
-        const int g = (warp - 5) >> 2, gt = tid - 160 - g * kGroupThreads;
-        ProdRegs<BITS> R0, R1;
-        int brow[16];
-        int brow_tile = -1;
-        Cursor c0, c1, tail;
-        cursor_first<MODE>(a, n_tiles, c0);
-        if (c0.t >= 0 && g == 1) cursor_next<MODE>(a, n_tiles, c0);
-        c1 = c0;
-        cursor_next<MODE>(a, n_tiles, c1);
-        cursor_next<MODE>(a, n_tiles, c1);
-        tail = c1;
-        if (c0.t >= 0) prod_load<MODE, BITS>(a, c0, gt, R0);
-        if (c1.t >= 0) prod_load<MODE, BITS>(a, c1, gt, R1);
-        auto iterate = [&](const Cursor& c, const ProdRegs<BITS>& R) -> bool {
-            const uint32_t s = c.it % S;
-            if (!bar_wait(&empty_bar[s], ((c.it / S) & 1u) ^ 1u, a.timeout_ns, &abort_s)) {
-                fail(a, &abort_s, 1);
-                return false;
+        // ---------------------------------------------------------- dequantisers
+        constexpr int D = RG::kSlots;
+        const int dt = tid - 32 * kDqWarp0, r = dt >> 1, hf = dt & 1;
+        const uint32_t codes0 = smem0 + RG::kOffCodes;
+        // issue side: the (tile, k-block) D k-blocks ahead of the one consumed
+        Tiles<MODE> ahead;
+        bool ahas = ahead.first(a, n_tiles);
+        int akb = 0, anb = ahas ? ahead.kblocks(a) : 0;
+        const uint8_t *aq = nullptr, *asb = nullptr;
+        if (ahas) code_src<MODE, BITS>(a, ahead.cur, r, hf, aq, asb);
+        uint32_t iss = 0;
+        auto issue = [&](uint32_t slot) {
+            if (ahas) {
+                const uint32_t base = codes0 + slot * RG::kSlotBytes;
+#pragma unroll
+                for (int p = 0; p < RG::kParts; ++p)
+                    cp_async16(base + (p * kDqThreads + dt) * 16, aq + (size_t)akb * 8 * BITS + 16 * p);
+                cp_async4(base + RG::kParts * kDqThreads * 16 + dt * 4, asb + (size_t)akb * 4);
+                ++iss;
+                if (++akb == anb) {
+                    akb = 0;
+                    ahas = ahead.next(a, n_tiles);
+                    if (ahas) {
+                        anb = ahead.kblocks(a);
+                        code_src<MODE, BITS>(a, ahead.cur, r, hf, aq, asb);
+                    }
+                }
             }
-            const uint32_t st = smem0 + s * SB;
-            if constexpr (MODE == 0) {
-                // token rows of bf16(x): 8 lanes per 128-byte row, copied straight into the swizzled tile
-                if (c.t != brow_tile) {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) brow[i] = token_row(a, c.tl, (gt >> 3) + 16 * i);
-                    brow_tile = c.t;
-                }
-                const int np = n_pad(c.tl.n);
-                const uint32_t btile = st + 2 * kTileBytes;
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int j = (gt >> 3) + 16 * i;
-                    if (j < c.tl.n)
-                        cp_async16(btile + swz_chunk(j, gt & 7),
-                                   a.x_bf + (size_t)brow[i] * a.x_stride + c.kb * 64 + (gt & 7) * 8);
-                    else if (j < np)
-                        sts128(btile + swz_chunk(j, gt & 7), make_uint4(0, 0, 0, 0));
-                }
-                cp_async_arrive(&full_bar[s]);
+            cp_async_commit();
+        };
+#pragma unroll 1
+        for (int j = 0; j < D; ++j) issue(j);
+        const uint64_t m2 = f2(__float_as_uint(-8388608.0f), __float_as_uint(-8388608.0f));
+        const int m = r >> 7, rr = r & 127;
+        for (uint32_t it = 0; it < iss; ++it) {
+            cp_async_wait<D - 1>();
+            const uint32_t slot = it % D;
+            const uint32_t base = codes0 + slot * RG::kSlotBytes;
+            const uint32_t sbw = lds32(base + RG::kParts * kDqThreads * 16 + dt * 4);
+            const float s = __half2float(__ushort_as_half((unsigned short)(sbw & 0xffffu)));
+            const float b = __half2float(__ushort_as_half((unsigned short)(sbw >> 16)));
+            const uint64_t s2 = f2(__float_as_uint(s), __float_as_uint(s));
+            const uint64_t b2 = f2(__float_as_uint(b), __float_as_uint(b));
+            uint4 o[4];
+            if (BITS == 4) {
+                const uint4 w = lds128(base + dt * 16);
+                o[0] = dq8_int4(w.x, s2, b2, m2);
+                o[1] = dq8_int4(w.y, s2, b2, m2);
+                o[2] = dq8_int4(w.z, s2, b2, m2);
+                o[3] = dq8_int4(w.w, s2, b2, m2);
             } else {
-                if (gt == 0) {
-                    // the SwiGLU rows of this chunk and k-block, hi and lo, already swizzled
-                    const uint32_t bytes = (uint32_t)n_pad(c.tl.n) * 128u;
-                    const size_t src = ((size_t)c.kb * a.h_rows + c.tl.hrow0) * 64;
-                    bar_expect_tx(&full_bar[s], 2 * bytes);
-                    bulk_g2s(st + 2 * kTileBytes, a.h_hi + src, bytes, &full_bar[s]);
-                    bulk_g2s(st + 4 * kTileBytes, a.h_lo + src, bytes, &full_bar[s]);
-                }
+                const uint4 w0 = lds128(base + dt * 16), w1 = lds128(base + (kDqThreads + dt) * 16);
+                o[0] = dq8_int8(w0.x, w0.y, s2, b2, m2);
+                o[1] = dq8_int8(w0.z, w0.w, s2, b2, m2);
+                o[2] = dq8_int8(w1.x, w1.y, s2, b2, m2);
+                o[3] = dq8_int8(w1.z, w1.w, s2, b2, m2);
             }
-            prod_store<BITS>(gt, st, R);
+            const uint32_t sa = it % kAStages;
+            // stage sa was last read by the MMAs of k-block it - kAStages
+            if (it >= kAStages &&
+                !warp_wait(&kb_done[(it - kAStages) % kDone], ((it - kAStages) / kDone) & 1u, a, &abort_s, lane)) {
+                fail(a, &abort_s, 1);
+                break;
+            }
+            const uint32_t tile = smem0 + RG::kOffA + sa * kStageBytes + m * kTileBytes;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) sts128(tile + swz_chunk(rr, 4 * hf + i), o[i]);
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) bar_arrive(&full_bar[s]);
-            return true;
-        };
-        for (;;) {
-            if (c0.t < 0 || !iterate(c0, R0)) break;
-            cursor_next<MODE>(a, n_tiles, tail);
-            cursor_next<MODE>(a, n_tiles, tail);
-            c0 = tail;
-            if (c0.t >= 0) prod_load<MODE, BITS>(a, c0, gt, R0);
-            if (c1.t < 0 || !iterate(c1, R1)) break;
-            cursor_next<MODE>(a, n_tiles, tail);
-            cursor_next<MODE>(a, n_tiles, tail);
-            c1 = tail;
-            if (c1.t >= 0) prod_load<MODE, BITS>(a, c1, gt, R1);
+            if (lane == 0) bar_arrive(&a_full[sa]);
+            // this slot's codes are consumed: refill it D k-blocks ahead
+            issue(slot);
         }
+        cp_async_wait_all();
     }
 
     fence_before_sync();
@@ -484,12 +644,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(GemmArgs 
 }
 
 template <int MODE, int BITS>
-cudaError_t launch_mode(const GemmArgs& g, int grid, cudaStream_t st) {
-    const size_t smem = (size_t)Cfg<MODE>::kStages * Cfg<MODE>::kStageBytes + 1024;
+cudaError_t launch_mode(const CUtensorMap& map, const CUtensorMap& smap, const GemmArgs& g, int grid, cudaStream_t st) {
+    const size_t smem = (size_t)Ring<BITS>::kSmem + 1024;
     cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    grouped_gemm_kernel<MODE, BITS><<<grid, kGemmThreads, smem, st>>>(g);
+    grouped_gemm_kernel<MODE, BITS><<<grid, kThreads, smem, st>>>(map, smap, g);
     return cudaGetLastError();
 }
 
@@ -500,29 +660,24 @@ cudaError_t launch_prefill_gemm(int mode, const Shapes& s, const PrefillScratch&
     GemmArgs g{};
     g.H = s.hidden;
     g.E = s.n_experts;
-    g.k = s.top_k;
     g.T = a.T;
-    g.P = a.T * s.top_k;
     g.inter = s.inter;
     g.shared_inter = a.shared_blob ? s.shared_inter : 0;
-    g.slices0 = s.h_stride / 128;
+    g.per = mode == 0 ? s.h_stride / 128 : s.hidden / 256;
     g.h_rows = p.h_rows;
-    g.chunks = p.chunks;
+    g.chunks = mode == 0 ? p.chunks : p.chunks1;
     g.n_chunks = p.n_chunks;
-    g.perm = p.perm;
-    g.x_bf = p.two_stage ? p.x3 : p.x_bf;
-    g.x_stride = p.two_stage ? 3 * s.hidden : s.hidden;
+    g.tok_sorted = p.tok_sorted;
+    g.w_sorted = p.w_sorted;
     g.h_hi = p.h_hi;
     g.h_lo = p.h_lo;
-    g.w = p.w;
     g.sigma = p.sigma;
     g.y = a.y;
-    g.dir = a.dir;
-    g.shared_blob = a.shared_blob;
     g.status = p.status_dev;
     g.timeout_ns = a.timeout_ns;
-    if (mode == 0) return s.bits == 4 ? launch_mode<0, 4>(g, p.sms, st) : launch_mode<0, 8>(g, p.sms, st);
-    return s.bits == 4 ? launch_mode<1, 4>(g, p.sms, st) : launch_mode<1, 8>(g, p.sms, st);
+    const CUtensorMap &m = p.x_map, &ms = p.xs_map;
+    if (mode == 0) return s.bits == 4 ? launch_mode<0, 4>(m, ms, g, p.sms, st) : launch_mode<0, 8>(m, ms, g, p.sms, st);
+    return s.bits == 4 ? launch_mode<1, 4>(m, ms, g, p.sms, st) : launch_mode<1, 8>(m, ms, g, p.sms, st);
 }
 
 }  // namespace moe

@@ -8,11 +8,13 @@
 //   3. hist_kernel     pairs (token, slot) counted per (expert, block of 1024
 //                      pairs) and ranked inside their block (warp match)
 //   4. scan_kernel     block counts -> first sorted position of every
-//                      (expert, block); expert offsets; the chunk list that
-//                      drives both grouped GEMMs
-//   5. scatter_kernel  perm[sorted position] = pair id (stable: pairs of one
-//                      expert keep ascending pair order)
-//   6. grouped GEMM gate/up, 7. grouped GEMM down (prefill_gemm.cu)
+//                      (expert, block); expert offsets; the chunk lists that
+//                      drive the two grouped GEMMs
+//   5. scatter_kernel  pair id, token and routing weight of every sorted
+//                      position (stable: pairs of one expert keep ascending
+//                      pair order)
+//   6. gather_kernel   bf16 token rows in sorted pair order
+//   7. grouped GEMM gate/up, 8. grouped GEMM down (prefill_gemm.cu)
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -239,17 +241,77 @@ __device__ __forceinline__ int block_excl_scan(int v, int* ws, int* total) {
     return r;
 }
 
+// Stable rank of this thread's partial chunk among all partial chunks, by size
+// r descending then owner (thread) ascending, sizes 1..nb-1 (0 = no partial
+// chunk): a counting sort on r.  Every thread of the block calls it.  Shared
+// scratch: wcnt[32 * nb], start[nb]; returns the rank (meaningful for r > 0)
+// and the number of partial chunks in *n_part.
+__device__ int partial_rank(int r, int nb, int* wcnt, int* start, int* ws, int* n_part) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < 32 * nb; i += blockDim.x) wcnt[i] = 0;
+    __syncthreads();
+    const unsigned same = __match_any_sync(kFullMask, r);
+    if (r > 0 && lane == __ffs(same) - 1) wcnt[warp * nb + r] = __popc(same);
+    __syncthreads();
+    // thread i < nb owns size nb-1-i: prefix of that size over the warps, then
+    // a scan over the sizes in descending order gives each size's first rank
+    const int sz = nb - 1 - tid;
+    int tot_sz = 0;
+    if (tid < nb && sz > 0)
+        for (int w = 0; w < 32; ++w) {
+            const int v = wcnt[w * nb + sz];
+            wcnt[w * nb + sz] = tot_sz;
+            tot_sz += v;
+        }
+    const int first = block_excl_scan(tot_sz, ws, n_part);
+    if (tid < nb) start[sz] = first;
+    __syncthreads();
+    const unsigned below = same & ((1u << lane) - 1u);
+    return r > 0 ? start[r] + wcnt[warp * nb + r] + __popc(below) : 0;
+}
+
+__device__ __forceinline__ void put_chunk(ChunkRec* list, int i, int e, int row0, int n, int hrow0,
+                                          const uint8_t* blob) {
+    ChunkRec c;
+    c.e = e;
+    c.row0 = row0;
+    c.n = n;
+    c.hrow0 = hrow0;
+    c.blob = blob;
+    c.pad[0] = c.pad[1] = 0;
+    list[i] = c;
+}
+
+// full chunks of every owner in owner order, then the partial chunks by size
+// descending (ties: lower owner first), so a static round-robin over the CTAs
+// hands out the longest tiles first
+template <int CL>
+__device__ void chunk_list(int NE, const int* tot, const int* off, int hoff, const uint8_t* blob, int* wcnt,
+                           int* start, int* ws, ChunkRec* list, int32_t* n_list) {
+    const int tid = threadIdx.x;
+    const int t = tid < NE ? tot[tid] : 0;
+    const int nf = t / CL;
+    int n_full = 0, n_part = 0;
+    const int fpos = block_excl_scan(nf, ws, &n_full);
+    for (int i = 0; i < nf; ++i) put_chunk(list, fpos + i, tid, off[tid] + i * CL, CL, hoff + i * CL, blob);
+    const int r = t % CL;
+    const int rank = partial_rank(r, CL, wcnt, start, ws, &n_part);
+    if (r > 0) put_chunk(list, n_full + rank, tid, off[tid] + nf * CL, r, hoff + nf * CL, blob);
+    if (tid == 0) *n_list = n_full + n_part;
+}
+
 // ---------------------------------------------------------------------------
-// 4. scan: per-(expert, block) first positions, expert offsets, chunk list.
-// Chunks: every full 256-row chunk of every expert (expert order), then the
-// partial chunks ordered by size descending (ties: lower expert first), so a
-// static round-robin over the CTAs hands out the longest tiles first.  The
-// shared expert (id E) covers tokens 0..T-1 in order.
+// 4. scan: per-(expert, block) first positions, expert offsets, the two chunk
+// lists (kChunk rows for gate/up, kChunk1 rows for down).  The shared expert
+// (owner E) covers tokens 0..T-1 in order.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ cnt, int E, int n_hist, int T,
-                                                    int has_shared, int32_t* __restrict__ offsets,
-                                                    int4* __restrict__ chunks, int32_t* __restrict__ n_chunks) {
-    __shared__ int tot[1025], off[1025], rem[1025];
+                                                    const uint8_t* const* __restrict__ dir,
+                                                    const uint8_t* __restrict__ shared_blob,
+                                                    int32_t* __restrict__ offsets, ChunkRec* __restrict__ chunks,
+                                                    ChunkRec* __restrict__ chunks1, int32_t* __restrict__ n_chunks) {
+    __shared__ int tot[1025], off[1025];
+    __shared__ int wcnt[32 * kChunk], start[kChunk];
     __shared__ int ws[32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // block counts -> first positions within each expert: a warp takes 8 of its
@@ -279,7 +341,8 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ cnt, i
         }
     }
     __syncthreads();
-    const int NE = E + (has_shared ? 1 : 0);  // chunk owners
+    const int has_shared = shared_blob != nullptr;
+    const int NE = E + has_shared;  // chunk owners
     int total = 0;
     {
         const int v = tid < E ? tot[tid] : 0;
@@ -296,47 +359,57 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ cnt, i
     }
     __syncthreads();
     for (size_t i = tid; i < (size_t)E * n_hist; i += 1024) cnt[i] += off[i / n_hist];
-    // first row of every expert in the SwiGLU buffers (segments padded to 16 rows)
+    // first row of every owner in the SwiGLU buffers (segments padded to 16 rows)
     int h_used = 0;
     const int hoff = block_excl_scan(tid < NE ? (tot[tid] + 15) & ~15 : 0, ws, &h_used);
-    // full chunks
-    const int nf = tid < NE ? tot[tid] / kChunk : 0;
-    int n_full = 0;
-    const int fpos = block_excl_scan(nf, ws, &n_full);
-    if (tid < NE) {
-        for (int i = 0; i < nf; ++i)
-            chunks[fpos + i] = make_int4(tid, off[tid] + i * kChunk, kChunk, hoff + i * kChunk);
-        rem[tid] = tot[tid] % kChunk;
-    }
-    __syncthreads();
-    int n_part = 0;
-    {
-        const int r = tid < NE ? rem[tid] : 0;
-        const int has = r > 0 ? 1 : 0;
-        block_excl_scan(has, ws, &n_part);
-        if (has) {
-            int rank = 0;
-            for (int e2 = 0; e2 < NE; ++e2) {
-                const int r2 = rem[e2];
-                rank += (r2 > r || (r2 == r && e2 < tid)) ? 1 : 0;
-            }
-            chunks[n_full + rank] = make_int4(tid, off[tid] + nf * kChunk, r, hoff + nf * kChunk);
-        }
-    }
-    if (tid == 0) *n_chunks = n_full + n_part;
+    const uint8_t* blob = tid < E ? dir[tid] : (tid == E ? shared_blob : nullptr);
+    chunk_list<kChunk>(NE, tot, off, hoff, blob, wcnt, start, ws, chunks, n_chunks);
+    chunk_list<kChunk1>(NE, tot, off, hoff, blob, wcnt, start, ws, chunks1, n_chunks + 1);
 }
 
 // ---------------------------------------------------------------------------
-// 5. scatter: perm[first position of (expert, block) + rank in block] = pair
+// 5. scatter: the pair at sorted position (first position of its (expert,
+// block) + its rank in the block): its id, token and routing weight
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kHistThreads) scatter_kernel(const int32_t* __restrict__ idx,
                                                                const int32_t* __restrict__ local_rank,
-                                                               const int32_t* __restrict__ cnt, int P, int n_hist,
-                                                               int32_t* __restrict__ perm) {
+                                                               const int32_t* __restrict__ cnt,
+                                                               const float* __restrict__ w, int P, int k, int n_hist,
+                                                               int32_t* __restrict__ perm,
+                                                               int32_t* __restrict__ tok_sorted,
+                                                               float* __restrict__ w_sorted) {
     const int p = blockIdx.x * kHistThreads + threadIdx.x;
     if (p >= P) return;
     const int e = idx[p];
-    perm[cnt[(size_t)e * n_hist + blockIdx.x] + local_rank[p]] = p;
+    const int pos = cnt[(size_t)e * n_hist + blockIdx.x] + local_rank[p];
+    perm[pos] = p;
+    tok_sorted[pos] = p / k;
+    w_sorted[pos] = w[p];
+}
+
+// ---------------------------------------------------------------------------
+// 6. gather: the bf16 token row of every sorted position, so that the gate/up
+// GEMM loads each chunk's rows as one rectangular TMA box per k-block.  A warp
+// copies one row of H/8 16-byte units per step.
+// ---------------------------------------------------------------------------
+constexpr int kGatherThreads = 512;
+__global__ void __launch_bounds__(kGatherThreads) gather_kernel(const int32_t* __restrict__ tok_sorted,
+                                                                const uint16_t* __restrict__ x, int x_stride, int P,
+                                                                int H, uint16_t* __restrict__ xs) {
+    const int lane = threadIdx.x & 31;
+    const int units = H / 8;  // <= 256
+    const int step = gridDim.x * (kGatherThreads / 32);
+    for (int row = blockIdx.x * (kGatherThreads / 32) + (threadIdx.x >> 5); row < P; row += step) {
+        const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)__ldg(tok_sorted + row) * x_stride);
+        uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)row * H);
+        uint4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (lane + 32 * i < units) v[i] = __ldg(src + lane + 32 * i);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (lane + 32 * i < units) dst[lane + 32 * i] = v[i];
+    }
 }
 
 template <class T>
@@ -357,6 +430,41 @@ cudaError_t launch_logits(const uint16_t* w_r, const float* bias, const float* x
     return cudaGetLastError();
 }
 
+// TMA maps of the gate/up GEMM's token operand (bf16, boxes of 64 x 64):
+// x_map over bf16(x) [max_tokens][hidden] with row stride x_stride (x_bf, or
+// the first third of each x3 row), xs_map over x_sorted [max_tokens * k][hidden]
+static bool encode_x_maps(PrefillScratch& p, const Shapes& s, int max_tokens, std::string& err) {
+    typedef CUresult (*EncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        !fn || q != cudaDriverEntryPointSuccess) {
+        cudaGetLastError();
+        err = "the driver has no cuTensorMapEncodeTiled";
+        return false;
+    }
+    auto encode = [&](CUtensorMap* m, void* base, size_t rows, size_t stride_elems) {
+        const cuuint64_t dims[2] = {(cuuint64_t)s.hidden, (cuuint64_t)rows};
+        const cuuint64_t strides[1] = {(cuuint64_t)stride_elems * 2};
+        const cuuint32_t box[2] = {64, 64}, estr[2] = {1, 1};
+        return ((EncodeFn)fn)(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    };
+    const size_t x_stride = p.two_stage ? 3 * (size_t)s.hidden : (size_t)s.hidden;
+    CUresult r = encode(&p.x_map, p.two_stage ? (void*)p.x3 : (void*)p.x_bf, max_tokens, x_stride);
+    if (r == CUDA_SUCCESS) r = encode(&p.xs_map, p.x_sorted, (size_t)max_tokens * s.top_k, s.hidden);
+    if (r != CUDA_SUCCESS) {
+        char buf[96];
+        snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+        err = buf;
+        return false;
+    }
+    return true;
+}
+
 std::string prefill_check(const Shapes& s) {
     if (s.hidden % 256 || s.hidden > 256 * kMaxNC) return "prefill needs hidden to be a multiple of 256, at most 2048";
     if (s.inter % 128 || s.shared_inter % 128) return "prefill needs inter and shared_inter to be multiples of 128";
@@ -374,6 +482,7 @@ int prefill_alloc(PrefillScratch& p, const Shapes& s, int max_tokens, int device
     p.max_tokens = max_tokens;
     p.n_hist = (int)((P + kHistThreads - 1) / kHistThreads);
     p.max_chunks = (int)((P + T) / kChunk + E + 2);
+    p.max_chunks1 = (int)((P + T) / kChunk1 + E + 2);
     p.h_rows = (int)((P + T + 16 * (E + 1) + 15) / 16 * 16);
     p.two_stage = router_two_stage_ok(s);
     cudaDeviceProp prop;
@@ -385,8 +494,9 @@ int prefill_alloc(PrefillScratch& p, const Shapes& s, int max_tokens, int device
     p.sms = prop.multiProcessorCount;
     if (dalloc(&p.logits, T * E) || dalloc(&p.x_bf, T * H) || dalloc(&p.idx, P) || dalloc(&p.w, P) ||
         dalloc(&p.sigma, T) || dalloc(&p.local_rank, P) || dalloc(&p.cnt, E * p.n_hist) ||
-        dalloc(&p.offsets, E + 1) || dalloc(&p.perm, P) || dalloc(&p.chunks, (size_t)p.max_chunks) ||
-        dalloc(&p.n_chunks, 1) || dalloc(&p.h_hi, (size_t)p.h_rows * s.h_stride) ||
+        dalloc(&p.offsets, E + 1) || dalloc(&p.perm, P) || dalloc(&p.tok_sorted, P) || dalloc(&p.x_sorted, P * H) ||
+        dalloc(&p.w_sorted, P) || dalloc(&p.chunks, (size_t)p.max_chunks) ||
+        dalloc(&p.chunks1, (size_t)p.max_chunks1) || dalloc(&p.n_chunks, 2) || dalloc(&p.h_hi, (size_t)p.h_rows * s.h_stride) ||
         dalloc(&p.h_lo, (size_t)p.h_rows * s.h_stride) ||
         (router_two_stage_ok(s) && (dalloc(&p.x3, T * 3 * H) || dalloc(&p.xnorm, T) || dalloc(&p.wnorm, E)))) {
         cudaGetLastError();
@@ -404,6 +514,10 @@ int prefill_alloc(PrefillScratch& p, const Shapes& s, int max_tokens, int device
         return MOE_ENOMEM;
     }
     *p.status_host = 0;
+    if (!encode_x_maps(p, s, max_tokens, err)) {
+        prefill_free(p);
+        return MOE_ECUDA;
+    }
     // rows past an expert's last row (up to its 16-row padding) feed MMA columns
     // that are never read back; zero them once so they hold finite values
     if (cudaMemset(p.h_hi, 0, (size_t)p.h_rows * s.h_stride * 2) != cudaSuccess ||
@@ -426,7 +540,11 @@ void prefill_free(PrefillScratch& p) {
     cudaFree(p.cnt);
     cudaFree(p.offsets);
     cudaFree(p.perm);
+    cudaFree(p.tok_sorted);
+    cudaFree(p.x_sorted);
+    cudaFree(p.w_sorted);
     cudaFree(p.chunks);
+    cudaFree(p.chunks1);
     cudaFree(p.n_chunks);
     cudaFree(p.h_hi);
     cudaFree(p.h_lo);
@@ -469,10 +587,17 @@ cudaError_t launch_prefill(const Shapes& s, PrefillScratch& p, const PrefillArgs
         ++*launches;
     }
     if ((e = stamp())) return e;
-    scan_kernel<<<1, 1024, 0, st>>>(p.cnt, E, n_hist, T, a.shared_blob ? 1 : 0, p.offsets, p.chunks, p.n_chunks);
+    scan_kernel<<<1, 1024, 0, st>>>(p.cnt, E, n_hist, T, a.dir, a.shared_blob, p.offsets, p.chunks, p.chunks1,
+                                    p.n_chunks);
     ++*launches;
     if ((e = stamp())) return e;
-    scatter_kernel<<<n_hist, kHistThreads, 0, st>>>(p.idx, p.local_rank, p.cnt, P, n_hist, p.perm);
+    scatter_kernel<<<n_hist, kHistThreads, 0, st>>>(p.idx, p.local_rank, p.cnt, p.w, P, k, n_hist, p.perm,
+                                                    p.tok_sorted, p.w_sorted);
+    ++*launches;
+    if ((e = cudaGetLastError())) return e;
+    if ((e = stamp())) return e;
+    gather_kernel<<<4 * p.sms, kGatherThreads, 0, st>>>(p.tok_sorted, p.two_stage ? p.x3 : p.x_bf,
+                                                        p.two_stage ? 3 * H : H, P, H, p.x_sorted);
     ++*launches;
     if ((e = cudaGetLastError())) return e;
     if ((e = stamp())) return e;
