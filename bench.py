@@ -496,9 +496,11 @@ def run_stress(args):
         step = 0
         at64 = None
 
-        def one_step():
+        def one_step(bias=None):
             nonlocal step, at64
-            if step > 0:
+            if bias is not None:
+                moe.moe_set_router_bias_all(ctx, bias, st)
+            elif step > 0:
                 drift.advance(ctx, st)
             moe.moe_forward_decode_stack(ctx, 0, L, X[step % n_ring], 1, y, 1e-6, None, None, None, st)
             step += 1
@@ -507,6 +509,8 @@ def run_stress(args):
 
         for _ in range(args.warmup):
             one_step()
+        # the drifted router biases of the timed steps, computed ahead like the token batches
+        sched = drift.schedule(args.steps)
         torch.cuda.synchronize()
         if pg:
             pg.barrier()
@@ -517,8 +521,8 @@ def run_stress(args):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         e0.record(st)
-        for _ in range(args.steps):
-            one_step()
+        for i in range(args.steps):
+            one_step(sched[i])
         e1.record(st)
         torch.cuda.synchronize()
         clocks = clk.stop()
@@ -548,11 +552,12 @@ def run_stress(args):
             yh = torch.empty((1, H)).pin_memory()
             xd = torch.empty((1, H), device="cuda")
             n_e2e = min(args.steps, 64)
+            sched_e2e = drift.schedule(n_e2e)
             torch.cuda.synchronize()
             t0 = time.perf_counter()
             for i in range(n_e2e):
                 xd.copy_(xh[(step + i) % n_ring], non_blocking=True)
-                drift.advance(ctx, st)
+                moe.moe_set_router_bias_all(ctx, sched_e2e[i], st)
                 moe.moe_forward_decode_stack(ctx, 0, L, xd, 1, y, 1e-6, None, None, None, st)
                 yh.copy_(y, non_blocking=True)
                 st.synchronize()
@@ -567,7 +572,9 @@ def run_stress(args):
             "config": {"workload": (f"stress: {L}-layer 80B-shaped decode stack, int{bits} group-64, batch 1, "
                                     f"{w.pool_slots} of {w.n_experts} slots per layer in HBM, full store in pinned "
                                     f"host memory, Zipf(1.1) routing with {w.drift_swaps} adjacent-rank swaps per "
-                                    "layer per step, misses by cudaMemcpyAsync on a side stream, pool starts cold"),
+                                    "layer per step (biases of the timed steps computed before timing and sent with "
+                                    "one moe_set_router_bias_all per step), misses by cudaMemcpyAsync on a side "
+                                    "stream, pool starts cold"),
                        "batch": 1, "layers": L, "bits": bits, "pool_slots": w.pool_slots,
                        "parallelism": "replicas" if world > 1 else "single-gpu",
                        "l2": "inputs larger than L2: each step reads its experts from the HBM pool or the host"},

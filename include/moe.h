@@ -161,8 +161,16 @@ int moe_load_experts(moe_ctx* ctx, int32_t layer, const void* blobs_host, size_t
                      const void* shared_blob_host, const uint16_t* router_w_host,
                      const uint16_t* shared_gate_host, const float* router_bias_host);
 
-/* Replace one layer's router bias (fp32 [n_experts], host).  Ordered on `stream`. */
+/* Replace one layer's router bias (fp32 [n_experts], host).  Ordered on
+ * `stream` and asynchronous: the values are staged in a pinned ring of the
+ * context (the call waits only if the copy that last used the staging slot,
+ * eight updates earlier, has not yet run).  The caller may reuse bias_host
+ * as soon as the call returns. */
 int moe_set_router_bias(moe_ctx* ctx, int32_t layer, const float* router_bias_host, void* stream);
+/* The same for every layer at once: fp32 [n_layers x n_experts], host, one copy.
+ * MOE_ESTATE if a layer has not been loaded.  (The pages have no counterpart:
+ * a benchmark with drifting expert popularity sets all biases per step.) */
+int moe_set_router_bias_all(moe_ctx* ctx, const float* router_bias_host, void* stream);
 
 /* ------------------------------------------------------------------ */
 /* forward                                                              */

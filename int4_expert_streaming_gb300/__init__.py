@@ -28,7 +28,7 @@ _ERRNAMES = {MOE_EINVAL: "MOE_EINVAL", MOE_ENOMEM: "MOE_ENOMEM", MOE_ECUDA: "MOE
 # every symbol include/moe.h declares
 EXPORTS = (
     "moe_blob_bytes", "moe_blob_stride", "moe_pack_expert", "moe_create", "moe_destroy", "moe_load_experts",
-    "moe_set_router_bias", "moe_forward_decode", "moe_forward_decode_stack", "moe_forward_prefill",
+    "moe_set_router_bias", "moe_set_router_bias_all", "moe_forward_decode", "moe_forward_decode_stack", "moe_forward_prefill",
     "moe_pool_stats", "moe_pool_trace", "moe_launch_count", "moe_prefill_profile", "moe_prefill_kernel_ms", "moe_route_noalloc", "moe_last_error", "moe_slotpool_create", "moe_slotpool_destroy",
     "moe_slotpool_request",
 )
@@ -79,6 +79,7 @@ def load_library(path: str | None = None):
         lib.moe_destroy.restype = None
         lib.moe_load_experts.argtypes = [vp, i32, vp, sz, vp, vp, vp, vp]
         lib.moe_set_router_bias.argtypes = [vp, i32, vp, vp]
+        lib.moe_set_router_bias_all.argtypes = [vp, vp, vp]
         lib.moe_forward_decode.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp]
         lib.moe_forward_decode_stack.argtypes = [vp, i32, i32, vp, i32, vp, c.c_float, vp, vp, vp, vp]
         lib.moe_forward_prefill.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp]
@@ -188,6 +189,11 @@ def moe_load_experts(ctx, layer: int, blobs, stride: int, shared_blob, router_w,
 
 def moe_set_router_bias(ctx, layer: int, bias_host, stream=None):
     _check(load_library().moe_set_router_bias(ctx, layer, _ptr(bias_host), _stream(stream)), ctx)
+
+
+def moe_set_router_bias_all(ctx, bias_host, stream=None):
+    """bias_host: contiguous fp32 host array [n_layers, n_experts]."""
+    _check(load_library().moe_set_router_bias_all(ctx, _ptr(bias_host), _stream(stream)), ctx)
 
 
 def moe_forward_decode(ctx, layer: int, x, B: int, y, topk_idx=None, topk_w=None, stream=None):

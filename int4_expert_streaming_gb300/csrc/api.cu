@@ -17,6 +17,7 @@
 // which is this library's explicit hazard management between slot refills and
 // the kernels that read them.
 #include <algorithm>
+#include <atomic>
 #include <chrono>
 #include <cstdarg>
 #include <cstdio>
@@ -68,6 +69,16 @@ struct moe_ctx {
     float* part = nullptr;  // [max_pairs][H] weighted down rows of each pair
     float* xbuf = nullptr;  // [2][max_batch][H]
     float* ybuf = nullptr;  // [max_batch][H]
+    // streaming, whole-stack calls: each layer's input [n_layers][max_batch][H],
+    // the last layer's output, and one CUDA graph per layer (and one for the
+    // first routing) for the call's batch size
+    float* xring = nullptr;
+    float* yout = nullptr;
+    std::vector<cudaGraphExec_t> graphs;  // [0] first routing, [1 + l] layer l's dispatch .. next routing
+    int graph_B = 0;
+    float graph_eps = 0.0f;
+    bool graphs_off = false;
+    cudaStream_t cap = nullptr;
     void* disp_mem = nullptr;
     moe::Dispatch disp{};
     moe::TokenDigits xd{};
@@ -82,15 +93,26 @@ struct moe_ctx {
 
     // host
     uint8_t* store = nullptr;
-    const uint8_t** dir_host = nullptr;
-    int32_t* idx_host = nullptr;
+    const uint8_t** dir_host = nullptr;  // streaming: the host's directory (pinned), copied to dir on misses
+    // streaming: mapped pinned block: ready [n_layers] (uint32, written by the
+    // publish kernel), the call's epoch (written by the host), then the
+    // published routing [max_batch * top_k]
+    void* gate_mem = nullptr;
+    moe::HostGate gate_host{}, gate_dev{};
+    uint32_t epoch = 0;
+    // router-bias updates go through a pinned ring, so they never synchronise
+    static constexpr int kBiasSlots = 8;
+    float* bias_stage = nullptr;  // [kBiasSlots][n_layers * n_experts]
+    cudaEvent_t bias_ev[kBiasSlots] = {};
+    bool bias_used[kBiasSlots] = {};
+    int bias_next = 0;
+    int pending_timing_layer = -1;  // layer whose miss-copy events are not yet harvested
     std::vector<uint8_t> loaded;
     std::vector<moe_slotpool*> pools;
     std::vector<LayerStats> stats;
     std::vector<int32_t> trace;
     cudaStream_t side = nullptr;
-    cudaEvent_t ev_idx = nullptr, ev_copy0 = nullptr, ev_copy1 = nullptr;
-    int pending_timing_layer = -1;
+    cudaEvent_t ev_copy0 = nullptr, ev_copy1 = nullptr;
     int64_t miss_copies = 0;
     bool fault_timeout_armed = false;
     uint64_t launches = 0;
@@ -189,8 +211,8 @@ const uint8_t* shared_blob(moe_ctx* c, int layer) {
     return c->cfg.shared_inter > 0 ? c->shared_pool + (size_t)layer * c->shared_stride : nullptr;
 }
 
-// Account the device time of the previous call's miss copies (already complete
-// once the compute stream has passed the point the host just waited for).
+// Account the device time of the previous layer's miss copies (complete once
+// a later routing has been published: the compute stream waited for them).
 void harvest_copy_timing(moe_ctx* c) {
     if (c->pending_timing_layer < 0) return;
     float ms = 0.0f;
@@ -201,19 +223,35 @@ void harvest_copy_timing(moe_ctx* c) {
     c->pending_timing_layer = -1;
 }
 
-// Streaming: read back the routing, run the pool policy, fetch misses.
-int resolve_pool(moe_ctx* c, int layer, int B, cudaStream_t st) {
+// Streaming, host side of one layer: wait until the layer's routing has been
+// published (mapped memory, polled), run the slot pool policy on it, copy each
+// missed expert's blob into its slot with cudaMemcpyAsync on the side stream
+// (the compute stream waits on an event after the copies) and write the
+// layer's directory, which the dispatch kernel launched next reads.
+int serve_layer(moe_ctx* c, int layer, int B, uint32_t epoch, cudaStream_t st) {
     const int k = c->cfg.top_k, E = c->cfg.n_experts;
-    CUDA_TRY(c, cudaMemcpyAsync(c->idx_host, c->idx, sizeof(int32_t) * B * k, cudaMemcpyDeviceToHost, st));
-    CUDA_TRY(c, cudaEventRecord(c->ev_idx, st));
-    int rc = wait_event(c, c->ev_idx);
-    if (rc) return rc;
+    if (c->fault_timeout_armed) {
+        c->fault_timeout_armed = false;
+        return fail(c, MOE_ETIMEOUT, "host wait timed out (injected)");
+    }
+    const auto deadline = std::chrono::steady_clock::now() + std::chrono::milliseconds(timeout_ms(c));
+    for (uint32_t spin = 0; c->gate_host.ready[layer] != epoch; ++spin) {
+        if ((spin & 255u) == 255u) {
+            if (std::chrono::steady_clock::now() > deadline)
+                return fail(c, MOE_ETIMEOUT, "the routing of layer %d was not published within %d ms", layer,
+                            timeout_ms(c));
+            const cudaError_t e = cudaStreamQuery(st);
+            if (e != cudaSuccess && e != cudaErrorNotReady)
+                return fail(c, MOE_ECUDA, "compute stream failed: %s", cudaGetErrorString(e));
+        }
+    }
+    std::atomic_thread_fence(std::memory_order_acquire);
     harvest_copy_timing(c);
-    std::vector<int32_t> req(c->idx_host, c->idx_host + B * k);
+    std::vector<int32_t> req(c->gate_host.idx, c->gate_host.idx + B * k);
     std::sort(req.begin(), req.end());
     req.erase(std::unique(req.begin(), req.end()), req.end());
     std::vector<int32_t> ev(4 * req.size());
-    rc = moe_slotpool_request(c->pools[layer], req.data(), (int32_t)req.size(), ev.data());
+    int rc = moe_slotpool_request(c->pools[layer], req.data(), (int32_t)req.size(), ev.data());
     if (rc < 0)
         return fail(c, rc, "slot pool request of %zu experts failed (pool has %d slots)", req.size(),
                     c->cfg.pool_slots);
@@ -244,6 +282,7 @@ int resolve_pool(moe_ctx* c, int layer, int B, cudaStream_t st) {
             return fail(c, MOE_ECUDA, "miss copy %d failed (injected)", c->cfg.fault_arg);
         }
         c->miss_copies++;
+        // the slot's previous expert was last read before this routing was published
         CUDA_TRY(c, cudaMemcpyAsync(dst, src, c->stride, cudaMemcpyHostToDevice, c->side));
         S.h2d_bytes += c->stride;
         dirh[e] = dst;
@@ -252,11 +291,17 @@ int resolve_pool(moe_ctx* c, int layer, int B, cudaStream_t st) {
         CUDA_TRY(c, cudaEventRecord(c->ev_copy1, c->side));
         CUDA_TRY(c, cudaStreamWaitEvent(st, c->ev_copy1, 0));
         c->pending_timing_layer = layer;
+        // the layer's device directory, read by the dispatch enqueued next (the
+        // source is pinned; the host rewrites it only after a later routing of
+        // this layer has been published, i.e. after this copy has run)
+        CUDA_TRY(c, cudaMemcpyAsync(c->dir + (size_t)layer * E, dirh, sizeof(void*) * E, cudaMemcpyHostToDevice, st));
     }
-    CUDA_TRY(c, cudaMemcpyAsync(c->dir + (size_t)layer * E, dirh, sizeof(void*) * E, cudaMemcpyHostToDevice, st));
+    std::atomic_thread_fence(std::memory_order_release);
+    S.calls++;
     return MOE_OK;
 }
 
+// Enqueues one layer of an all-resident context.
 int decode_layer(moe_ctx* c, int layer, const float* x, int B, float* y, int32_t* uidx, float* uw,
                  cudaStream_t st) {
     const moe::Shapes& s = c->sh;
@@ -267,22 +312,147 @@ int decode_layer(moe_ctx* c, int layer, const float* x, int B, float* y, int32_t
     const uint8_t* const* dir = c->dir + (size_t)layer * E;
     CUDA_TRY(c, moe::launch_router(s, wr, bias, x, B, c->logits, st));
     c->launches += 6;  // router, top-k (per token), dispatch, gate/up, down, combine
-    if (c->resident) {
-        CUDA_TRY(c, moe::launch_route_dispatch(s, 3, c->logits, x, wsg, B, c->idx, c->w, c->sigma, uidx, uw, dir,
-                                               shared_blob(c, layer), c->disp, c->xd, c->hits_dev + layer, st));
-    } else {
-        CUDA_TRY(c, moe::launch_route_dispatch(s, 1, c->logits, x, wsg, B, c->idx, c->w, c->sigma, uidx, uw, dir,
-                                               shared_blob(c, layer), c->disp, c->xd, nullptr, st));
-        int rc = resolve_pool(c, layer, B, st);
-        if (rc) return rc;
-        CUDA_TRY(c, moe::launch_route_dispatch(s, 2, c->logits, x, wsg, B, c->idx, c->w, c->sigma, nullptr,
-                                               nullptr, dir, shared_blob(c, layer), c->disp, c->xd, nullptr, st));
-    }
+    CUDA_TRY(c, moe::launch_route_dispatch(s, 3, c->logits, x, wsg, B, c->idx, c->w, c->sigma, uidx, uw, dir,
+                                           shared_blob(c, layer), c->disp, c->xd, c->hits_dev + layer, st));
     CUDA_TRY(c, moe::launch_gateup_batched(s, c->disp, c->xd, c->h, st));
     CUDA_TRY(c, moe::launch_down_batched(s, c->disp, c->h, c->part, st));
     CUDA_TRY(c, moe::launch_combine(s, c->disp, c->part, y, B, c->cfg.shared_inter > 0, st));
     c->stats[layer].calls++;
     return MOE_OK;
+}
+
+// Streaming, enqueue helpers.  Routing of layer l: router, top-k and the
+// publication of the routing to the host.
+int enq_route(moe_ctx* c, int l, const float* xin, int B, int32_t* uidx, float* uw, cudaStream_t st) {
+    const moe::Shapes& s = c->sh;
+    const int H = c->cfg.hidden, k = c->cfg.top_k, E = c->cfg.n_experts;
+    const uint16_t* wr = c->router_w + (size_t)l * E * H;
+    const float* bias = c->router_bias + (size_t)l * E;
+    const uint16_t* wsg = c->cfg.shared_inter > 0 ? c->shared_gate + (size_t)l * H : nullptr;
+    CUDA_TRY(c, moe::launch_router(s, wr, bias, xin, B, c->logits, st));
+    CUDA_TRY(c, moe::launch_route_dispatch(s, 1, c->logits, xin, wsg, B, c->idx, c->w, c->sigma, uidx, uw, nullptr,
+                                           nullptr, c->disp, c->xd, nullptr, st, &c->gate_dev, l));
+    (void)k;
+    return MOE_OK;
+}
+
+// ... and the rest of layer l once the host has served it: dispatch (reading
+// the directory the host has just written), gate/up, down, combine into yl.
+int enq_post(moe_ctx* c, int l, const float* xin, int B, float* yl, cudaStream_t st) {
+    const moe::Shapes& s = c->sh;
+    const int H = c->cfg.hidden, E = c->cfg.n_experts;
+    const uint16_t* wsg = c->cfg.shared_inter > 0 ? c->shared_gate + (size_t)l * H : nullptr;
+    CUDA_TRY(c, moe::launch_route_dispatch(s, 2, c->logits, xin, wsg, B, c->idx, c->w, c->sigma, nullptr, nullptr,
+                                           c->dir + (size_t)l * E, shared_blob(c, l), c->disp, c->xd, nullptr, st));
+    CUDA_TRY(c, moe::launch_gateup_batched(s, c->disp, c->xd, c->h, st));
+    CUDA_TRY(c, moe::launch_down_batched(s, c->disp, c->h, c->part, st));
+    CUDA_TRY(c, moe::launch_combine(s, c->disp, c->part, yl, B, c->cfg.shared_inter > 0, st));
+    return MOE_OK;
+}
+
+// One CUDA graph per layer for whole-stack calls of B tokens: [0] routes layer
+// 0 from xring[0]; [1 + l] runs layer l's dispatch .. combine and, below the
+// last layer, renormalises into xring[l + 1] and routes layer l + 1.
+int build_graphs(moe_ctx* c, int B, float eps) {
+    const int L = c->cfg.n_layers, H = c->cfg.hidden;
+    const size_t tok = (size_t)c->cfg.max_batch * H;
+    for (cudaGraphExec_t g : c->graphs)
+        if (g) cudaGraphExecDestroy(g);
+    c->graphs.assign(L + 1, nullptr);
+    c->graph_B = 0;
+    auto capture = [&](int idx, auto&& body) -> int {
+        cudaGraph_t g = nullptr;
+        CUDA_TRY(c, cudaStreamBeginCapture(c->cap, cudaStreamCaptureModeThreadLocal));
+        const int rc = body();
+        const cudaError_t e = cudaStreamEndCapture(c->cap, &g);
+        if (rc || e != cudaSuccess) {
+            if (g) cudaGraphDestroy(g);
+            cudaGetLastError();
+            return rc ? rc : fail(c, MOE_ECUDA, "graph capture failed: %s", cudaGetErrorString(e));
+        }
+        const cudaError_t ei = cudaGraphInstantiate(&c->graphs[idx], g, 0);
+        cudaGraphDestroy(g);
+        if (ei != cudaSuccess) return fail(c, MOE_ECUDA, "cudaGraphInstantiate failed: %s", cudaGetErrorString(ei));
+        return MOE_OK;
+    };
+    int rc = capture(0, [&] { return enq_route(c, 0, c->xring, B, nullptr, nullptr, c->cap); });
+    for (int l = 0; l < L && !rc; ++l) {
+        rc = capture(1 + l, [&]() -> int {
+            const float* xl = c->xring + (size_t)l * tok;
+            if (l == L - 1) return enq_post(c, l, xl, B, c->yout, c->cap);
+            int r = enq_post(c, l, xl, B, c->ybuf, c->cap);
+            if (r) return r;
+            float* xn = c->xring + (size_t)(l + 1) * tok;
+            CUDA_TRY(c, moe::launch_renorm(c->ybuf, xn, B, H, eps, c->cap));
+            return enq_route(c, l + 1, xn, B, nullptr, nullptr, c->cap);
+        });
+    }
+    if (!rc) {
+        c->graph_B = B;
+        c->graph_eps = eps;
+    }
+    return rc;
+}
+
+// Streaming: layers layer0 .. layer0+n-1 of one call.  Per layer, the routing
+// (router, top-k, publication) is enqueued; the host polls for it, serves the
+// slot pool (miss copies on the side stream, the compute stream ordered after
+// them by an event) and then enqueues the dispatch, gate/up, down, combine and
+// the next layer's routing -- one graph launch per layer for whole-stack calls.
+// No kernel ever waits on the host or on another stream.
+int stream_layers(moe_ctx* c, int layer0, int n, const float* x, int B, float* y, float eps, float* x_trace,
+                  int32_t* idx_trace, float* y_trace, int32_t* uidx, float* uw, cudaStream_t st) {
+    const int H = c->cfg.hidden, k = c->cfg.top_k, L = c->cfg.n_layers;
+    const size_t tok = (size_t)B * H;
+    const uint32_t epoch = ++c->epoch ? c->epoch : ++c->epoch;  // never 0
+    *const_cast<volatile uint32_t*>(c->gate_host.epoch) = epoch;
+    std::atomic_thread_fence(std::memory_order_seq_cst);
+    const bool whole = layer0 == 0 && n == L && !x_trace && !idx_trace && !y_trace && !uidx && !uw;
+    if (whole && !c->graphs_off && (c->graph_B != B || c->graph_eps != eps)) {
+        if (build_graphs(c, B, eps)) {
+            c->graphs_off = true;  // fall back to launches for the rest of the context's life
+            c->err.clear();
+        }
+    }
+    if (whole && !c->graphs_off) {
+        CUDA_TRY(c, cudaMemcpyAsync(c->xring, x, tok * sizeof(float), cudaMemcpyDeviceToDevice, st));
+        CUDA_TRY(c, cudaGraphLaunch(c->graphs[0], st));
+        c->launches += 3;
+        for (int l = 0; l < n; ++l) {
+            int rc = serve_layer(c, l, B, epoch, st);
+            if (rc) return rc;
+            CUDA_TRY(c, cudaGraphLaunch(c->graphs[1 + l], st));
+            c->launches += l == L - 1 ? 4 : 8;
+        }
+        CUDA_TRY(c, cudaMemcpyAsync(y, c->yout, tok * sizeof(float), cudaMemcpyDeviceToDevice, st));
+        return MOE_OK;
+    }
+    const float* xin = x;
+    auto route = [&](int i) -> int {
+        if (x_trace) CUDA_TRY(c, cudaMemcpyAsync(x_trace + i * tok, xin, tok * sizeof(float), cudaMemcpyDeviceToDevice, st));
+        c->launches += 3;
+        return enq_route(c, layer0 + i, xin, B, idx_trace ? idx_trace + (size_t)i * B * k : uidx, idx_trace ? nullptr : uw,
+                         st);
+    };
+    int rc = route(0);
+    for (int i = 0; i < n && !rc; ++i) {
+        const int l = layer0 + i;
+        if ((rc = serve_layer(c, l, B, epoch, st))) break;
+        const bool last = i == n - 1;
+        float* yl = last ? y : (y_trace ? y_trace + i * tok : c->ybuf);
+        if ((rc = enq_post(c, l, xin, B, yl, st))) break;
+        c->launches += 4;
+        if (last) {
+            if (y_trace) CUDA_TRY(c, cudaMemcpyAsync(y_trace + i * tok, y, tok * sizeof(float), cudaMemcpyDeviceToDevice, st));
+            break;
+        }
+        float* xn = c->xbuf + (size_t)(i & 1) * c->cfg.max_batch * H;
+        CUDA_TRY(c, moe::launch_renorm(yl, xn, B, H, eps, st));
+        c->launches += 1;
+        xin = xn;
+        rc = route(i + 1);
+    }
+    return rc;
 }
 
 // Adds the kernel times of recorded prefill call i (ring slot i % kProfRing).
@@ -335,6 +505,11 @@ extern "C" void moe_destroy(moe_ctx* c) {
     cudaFree(c->part);
     cudaFree(c->xbuf);
     cudaFree(c->ybuf);
+    for (cudaGraphExec_t g : c->graphs)
+        if (g) cudaGraphExecDestroy(g);
+    cudaFree(c->xring);
+    cudaFree(c->yout);
+    if (c->cap) cudaStreamDestroy(c->cap);
     cudaFree(c->disp_mem);
     cudaFree(c->xd.words);
     cudaFree(c->xd.sums);
@@ -344,11 +519,13 @@ extern "C" void moe_destroy(moe_ctx* c) {
     for (cudaEvent_t e : c->prof_ev) cudaEventDestroy(e);
     if (c->store) cudaFreeHost(c->store);
     if (c->dir_host) cudaFreeHost(c->dir_host);
-    if (c->idx_host) cudaFreeHost(c->idx_host);
+    if (c->gate_mem) cudaFreeHost(c->gate_mem);
     for (auto* p : c->pools) moe_slotpool_destroy(p);
     if (c->side) cudaStreamDestroy(c->side);
-    if (c->ev_idx) cudaEventDestroy(c->ev_idx);
     if (c->ev_copy0) cudaEventDestroy(c->ev_copy0);
+    for (cudaEvent_t e : c->bias_ev)
+        if (e) cudaEventDestroy(e);
+    if (c->bias_stage) cudaFreeHost(c->bias_stage);
     if (c->ev_copy1) cudaEventDestroy(c->ev_copy1);
     cudaGetLastError();
     delete c;
@@ -465,28 +642,46 @@ extern "C" int moe_create(const moe_config* cfg, moe_ctx** out) {
             c->err = buf;
             return bail(MOE_ENOMEM);
         }
+        const size_t gate_bytes = sizeof(uint32_t) * ((size_t)L + 1) + sizeof(int32_t) * Bm * k;
         if (cudaHostAlloc(reinterpret_cast<void**>(&c->dir_host), sizeof(void*) * (size_t)L * E,
                           cudaHostAllocDefault) != cudaSuccess ||
-            cudaHostAlloc(reinterpret_cast<void**>(&c->idx_host), sizeof(int32_t) * Bm * k, cudaHostAllocDefault) !=
-                cudaSuccess) {
+            cudaHostAlloc(&c->gate_mem, gate_bytes, cudaHostAllocMapped) != cudaSuccess) {
             cudaGetLastError();
             c->err = "cudaHostAlloc failed";
             return bail(MOE_ENOMEM);
         }
         std::memset(c->dir_host, 0, sizeof(void*) * (size_t)L * E);
+        std::memset(c->gate_mem, 0, gate_bytes);
+        void* gate_dev = nullptr;
+        if (cudaHostGetDevicePointer(&gate_dev, c->gate_mem, 0) != cudaSuccess) {
+            cudaGetLastError();
+            c->err = "cudaHostGetDevicePointer failed";
+            return bail(MOE_ECUDA);
+        }
+        auto carve = [&](void* base, moe::HostGate& g) {
+            uint32_t* w = static_cast<uint32_t*>(base);
+            g.ready = w;
+            g.epoch = w + L;
+            g.idx = reinterpret_cast<int32_t*>(w + L + 1);
+        };
+        carve(c->gate_mem, c->gate_host);
+        carve(gate_dev, c->gate_dev);
         c->pools.assign(L, nullptr);
         for (int l = 0; l < L; ++l)
             if ((rc = moe_slotpool_create(g.pool_slots, E, g.policy, &c->pools[l]))) {
                 c->err = "slot pool creation failed";
                 return bail(rc);
             }
-        if (cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking) != cudaSuccess) {
+        if (cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&c->cap, cudaStreamNonBlocking) != cudaSuccess) {
             c->err = "cudaStreamCreate failed";
             return bail(MOE_ECUDA);
         }
+        if ((rc = dev_alloc(c, &c->xring, (size_t)L * Bm * H, "xring")) ||
+            (rc = dev_alloc(c, &c->yout, (size_t)Bm * H, "yout")))
+            return bail(rc);
     }
-    if (cudaEventCreateWithFlags(&c->ev_idx, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreate(&c->ev_copy0) != cudaSuccess || cudaEventCreate(&c->ev_copy1) != cudaSuccess) {
+    if (cudaEventCreate(&c->ev_copy0) != cudaSuccess || cudaEventCreate(&c->ev_copy1) != cudaSuccess) {
         c->err = "cudaEventCreate failed";
         return bail(MOE_ECUDA);
     }
@@ -533,15 +728,54 @@ extern "C" int moe_load_experts(moe_ctx* c, int32_t layer, const void* blobs, si
     return MOE_OK;
 }
 
+namespace {
+// Copies n floats of router bias from (any) host memory to dst through the
+// next pinned staging slot, asynchronously on the stream.
+int stage_bias(moe_ctx* c, float* dst, const float* src, size_t n, cudaStream_t st) {
+    const size_t slot_floats = (size_t)c->cfg.n_layers * c->cfg.n_experts;
+    if (!c->bias_stage) {
+        if (cudaHostAlloc(reinterpret_cast<void**>(&c->bias_stage), sizeof(float) * slot_floats * moe_ctx::kBiasSlots,
+                          cudaHostAllocDefault) != cudaSuccess) {
+            cudaGetLastError();
+            c->bias_stage = nullptr;
+            return fail(c, MOE_ENOMEM, "cudaHostAlloc of the router-bias staging ring failed");
+        }
+        for (auto& e : c->bias_ev) CUDA_TRY(c, cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+    }
+    const int slot = c->bias_next;
+    c->bias_next = (c->bias_next + 1) % moe_ctx::kBiasSlots;
+    if (c->bias_used[slot]) {
+        int rc = wait_event(c, c->bias_ev[slot]);  // the copy that last used the slot (long done)
+        if (rc) return rc;
+    }
+    float* stage = c->bias_stage + (size_t)slot * slot_floats;
+    std::memcpy(stage, src, sizeof(float) * n);
+    CUDA_TRY(c, cudaMemcpyAsync(dst, stage, sizeof(float) * n, cudaMemcpyHostToDevice, st));
+    CUDA_TRY(c, cudaEventRecord(c->bias_ev[slot], st));
+    c->bias_used[slot] = true;
+    return MOE_OK;
+}
+}  // namespace
+
 extern "C" int moe_set_router_bias(moe_ctx* c, int32_t layer, const float* bias_host, void* stream) {
     if (!c) return fail(nullptr, MOE_EINVAL, "ctx is NULL");
     int rc = check_layer(c, layer);
     if (rc) return rc;
     if (!bias_host) return fail(c, MOE_EINVAL, "bias is NULL");
-    CUDA_TRY(c, cudaMemcpyAsync(c->router_bias + (size_t)layer * c->cfg.n_experts, bias_host,
-                                sizeof(float) * c->cfg.n_experts, cudaMemcpyHostToDevice,
-                                static_cast<cudaStream_t>(stream)));
-    return MOE_OK;
+    CUDA_TRY(c, cudaSetDevice(c->cfg.device));
+    return stage_bias(c, c->router_bias + (size_t)layer * c->cfg.n_experts, bias_host, c->cfg.n_experts,
+                      static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int moe_set_router_bias_all(moe_ctx* c, const float* bias_host, void* stream) {
+    if (!c) return fail(nullptr, MOE_EINVAL, "ctx is NULL");
+    if (c->poisoned) return fail(c, MOE_ESTATE, "context is poisoned by an earlier CUDA error");
+    if (!bias_host) return fail(c, MOE_EINVAL, "bias is NULL");
+    for (int l = 0; l < c->cfg.n_layers; ++l)
+        if (!c->loaded[l]) return fail(c, MOE_ESTATE, "layer %d has not been loaded", l);
+    CUDA_TRY(c, cudaSetDevice(c->cfg.device));
+    return stage_bias(c, c->router_bias, bias_host, (size_t)c->cfg.n_layers * c->cfg.n_experts,
+                      static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int moe_forward_decode(moe_ctx* c, int32_t layer, const float* x, int32_t B, float* y,
@@ -552,7 +786,9 @@ extern "C" int moe_forward_decode(moe_ctx* c, int32_t layer, const float* x, int
     if (!x || !y || x == y) return fail(c, MOE_EINVAL, "x and y must be distinct device buffers");
     if (B < 1 || B > c->cfg.max_batch) return fail(c, MOE_EINVAL, "B=%d outside 1..max_batch", B);
     CUDA_TRY(c, cudaSetDevice(c->cfg.device));
-    return decode_layer(c, layer, x, B, y, topk_idx, topk_w, static_cast<cudaStream_t>(stream));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (!c->resident) return stream_layers(c, layer, 1, x, B, y, 1.0f, nullptr, nullptr, nullptr, topk_idx, topk_w, st);
+    return decode_layer(c, layer, x, B, y, topk_idx, topk_w, st);
 }
 
 extern "C" int moe_forward_decode_stack(moe_ctx* c, int32_t layer0, int32_t n, const float* x, int32_t B,
@@ -602,6 +838,7 @@ extern "C" int moe_forward_decode_stack(moe_ctx* c, int32_t layer0, int32_t n, c
         c->launches += 1;
         return MOE_OK;
     }
+    if (!c->resident) return stream_layers(c, layer0, n, x, B, y, eps, x_trace, idx_trace, y_trace, nullptr, nullptr, st);
     const float* xin = x;
     for (int l = layer0; l < layer0 + n; ++l) {
         const int i = l - layer0;

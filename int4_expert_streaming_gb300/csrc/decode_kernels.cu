@@ -82,8 +82,8 @@ __device__ void token_digits(const float* x, int H, int lane, uint32_t* words, i
 __global__ void __launch_bounds__(1024) route_dispatch_kernel(
     Shapes s, int mode, const float* __restrict__ logits, const float* __restrict__ x,
     const uint16_t* __restrict__ wsg, int B, int32_t* idx, float* w, float* sigma, int32_t* uidx, float* uw,
-    const uint8_t* const* __restrict__ dir, const uint8_t* shared_blob, Dispatch d, TokenDigits xd,
-    unsigned long long* hit_counter) {
+    const uint8_t* const* dir, const uint8_t* shared_blob, Dispatch d, TokenDigits xd,
+    unsigned long long* hit_counter, HostGate pub, int pub_layer) {
     const int E = s.n_experts, k = s.top_k, H = s.hidden;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
     __shared__ int32_t s_idx[kMaxB][kMaxK];
@@ -115,6 +115,14 @@ __global__ void __launch_bounds__(1024) route_dispatch_kernel(
                 token_digits<8>(x + (size_t)t * H, H, lane, xd.words + (size_t)t * nc * dwn, xd.sums + (size_t)t * nc,
                                 xd.exps + t);
         }
+    }
+    if ((mode & 1) && pub.ready) {
+        // streaming, single CTA: publish the routing to the host
+        __syncthreads();
+        for (int i = threadIdx.x; i < B * k; i += blockDim.x) pub.idx[i] = idx[i];
+        __threadfence_system();
+        __syncthreads();
+        if (threadIdx.x == 0) pub.ready[pub_layer] = *pub.epoch;
     }
     if (!(mode & 2)) return;
     __syncthreads();  // (mode 2 runs as a single CTA)
@@ -443,6 +451,15 @@ __global__ void __launch_bounds__(kRenormThreads) renorm_kernel(const float* __r
     for (int j = threadIdx.x; j < H; j += kRenormThreads) xn[(size_t)t * H + j] = __fmul_rn(yt[j], r);
 }
 
+// streaming: the routing of a layer to mapped host memory, then the call's epoch
+__global__ void publish_kernel(const int32_t* __restrict__ idx, int n, int32_t* out, volatile uint32_t* ready,
+                               const volatile uint32_t* epoch) {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) out[i] = idx[i];
+    __threadfence_system();
+    __syncthreads();
+    if (threadIdx.x == 0) *ready = *epoch;
+}
+
 }  // namespace
 
 cudaError_t launch_router(const Shapes& s, const uint16_t* w_r, const float* bias, const float* x, int B,
@@ -457,17 +474,27 @@ cudaError_t launch_route_dispatch(const Shapes& s, int mode, const float* logits
                                   const uint16_t* shared_gate_w, int B, int32_t* idx, float* w, float* sigma,
                                   int32_t* user_idx, float* user_w, const uint8_t* const* dir_layer,
                                   const uint8_t* shared_blob, Dispatch d, TokenDigits xd,
-                                  unsigned long long* hit_counter, cudaStream_t st) {
+                                  unsigned long long* hit_counter, cudaStream_t st, const HostGate* pub,
+                                  int pub_layer) {
+    // the top-k part publishes itself when it runs as one CTA, else a small kernel follows
+    const bool fused_pub = pub && (mode & 1) && (B + 7) / 8 == 1;
+    const HostGate none{};
     // the per-token part (top-k, weights, shared gate, digits: one warp per token) spread
     // over B/8 CTAs; the dispatch lists in one CTA of 1024 threads
     if (mode & 1) {
         route_dispatch_kernel<<<(B + 7) / 8, 256, 0, st>>>(s, mode & ~2, logits, x, shared_gate_w, B, idx, w, sigma,
                                                             user_idx, user_w, dir_layer, shared_blob, d, xd,
-                                                            hit_counter);
+                                                            hit_counter, fused_pub ? *pub : none, pub_layer);
+        if (pub && !fused_pub) {
+            cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+            publish_kernel<<<1, 256, 0, st>>>(idx, B * s.top_k, pub->idx, pub->ready + pub_layer, pub->epoch);
+        }
     }
     if (mode & 2) {
         route_dispatch_kernel<<<1, 1024, 0, st>>>(s, mode & ~1, logits, x, shared_gate_w, B, idx, w, sigma,
-                                                  user_idx, user_w, dir_layer, shared_blob, d, xd, hit_counter);
+                                                  user_idx, user_w, dir_layer, shared_blob, d, xd, hit_counter,
+                                                  none, 0);
     }
     return cudaGetLastError();
 }
@@ -481,8 +508,7 @@ cudaError_t launch_gateup_batched(const Shapes& s, Dispatch d, TokenDigits xd, f
     cudaError_t e = cudaSuccess;
 #define MOE_GU(B_, N_)                                                                                         \
     do {                                                                                                     \
-        e = cudaFuncSetAttribute(gateup_batched_kernel<B_, N_>, cudaFuncAttributeMaxDynamicSharedMemorySize,  \
-                                 (int)smem);                                                                  \
+        e = smem_limit(reinterpret_cast<const void*>(gateup_batched_kernel<B_, N_>), (int)smem);              \
         if (e == cudaSuccess) gateup_batched_kernel<B_, N_><<<grid, kThreads, smem, st>>>(s, d, xd, h);       \
     } while (0)
     if (s.bits == 4) {

@@ -1,12 +1,33 @@
 // moe_internal.h -- shared between the host runtime and the CUDA kernels.
 #pragma once
 
+#include <mutex>
+#include <tuple>
+#include <vector>
+
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "moe.h"
 
 namespace moe {
+
+// Raises a kernel's dynamic shared-memory limit to at least `bytes` on the
+// current device, once: the call costs host time on every launch otherwise,
+// and the launches of the streaming path are also captured into graphs.
+inline cudaError_t smem_limit(const void* kernel, int bytes) {
+    static std::mutex mu;
+    static std::vector<std::tuple<const void*, int, int>> done;  // (kernel, device, bytes)
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    for (auto& d : done)
+        if (std::get<0>(d) == kernel && std::get<1>(d) == dev && std::get<2>(d) >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.emplace_back(kernel, dev, bytes);
+    return e;
+}
 
 // Byte offsets of the six sections of one blob (layout v1, see moe.h).
 struct BlobLayout {
@@ -44,6 +65,15 @@ struct Dispatch {
     int32_t* n_work;       // [1]
 };
 
+// Publication of a streaming layer's routing to the host (device aliases of
+// mapped pinned host memory): the host polls ready[layer] for the call's epoch,
+// runs the slot pool on idx, and launches the layer's dispatch afterwards.
+struct HostGate {
+    volatile uint32_t* ready;        // [n_layers] epoch of the last routing published per layer
+    const volatile uint32_t* epoch;  // [1] the epoch of the current call, written by the host
+    int32_t* idx;                    // [max_batch * top_k] the published routing
+};
+
 struct Shapes {
     int hidden, n_experts, top_k, inter, shared_inter, bits, norm_topk;
     int max_act, max_pairs, h_stride;  // h_stride = max(inter, shared_inter)
@@ -66,7 +96,8 @@ cudaError_t launch_route_dispatch(const Shapes& s, int mode, const float* logits
                                   const uint16_t* shared_gate_w, int B, int32_t* idx, float* w, float* sigma,
                                   int32_t* user_idx, float* user_w, const uint8_t* const* dir_layer,
                                   const uint8_t* shared_blob, Dispatch d, TokenDigits xd,
-                                  unsigned long long* hit_counter, cudaStream_t st);
+                                  unsigned long long* hit_counter, cudaStream_t st,
+                                  const HostGate* publish = nullptr, int publish_layer = 0);
 cudaError_t launch_renorm(const float* y, float* x_next, int B, int hidden, float eps, cudaStream_t st);
 // batched per-layer path: gate/up per (expert, row block) with staged token digits,
 // down per (expert, row block) into part[pair][H], then the per-token combine

@@ -646,8 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
 template <int MODE, int BITS>
 cudaError_t launch_mode(const CUtensorMap& map, const CUtensorMap& smap, const GemmArgs& g, int grid, cudaStream_t st) {
     const size_t smem = (size_t)Ring<BITS>::kSmem + 1024;
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    cudaError_t e = smem_limit(reinterpret_cast<const void*>(grouped_gemm_kernel<MODE, BITS>), (int)smem);
     if (e != cudaSuccess) return e;
     grouped_gemm_kernel<MODE, BITS><<<grid, kThreads, smem, st>>>(map, smap, g);
     return cudaGetLastError();

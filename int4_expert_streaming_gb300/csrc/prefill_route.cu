@@ -422,7 +422,7 @@ cudaError_t dalloc(T** p, size_t n) {
 cudaError_t launch_logits(const uint16_t* w_r, const float* bias, const float* x, int T, int H, int E, int tok_tile,
                           float* logits, cudaStream_t st) {
     const size_t smem = (size_t)kLgStages * kLgStageTok * H * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = smem_limit(reinterpret_cast<const void*>(logits_kernel), (int)smem);
     if (e != cudaSuccess) return e;
     tok_tile = std::max(1, std::min(tok_tile, kLgTokens));
     dim3 grid((E + kLgExperts - 1) / kLgExperts, (T + tok_tile - 1) / tok_tile);
@@ -582,7 +582,7 @@ cudaError_t launch_prefill(const Shapes& s, PrefillScratch& p, const PrefillArgs
     if ((e = stamp())) return e;
     {
         const size_t smem = (size_t)32 * E * sizeof(uint16_t);
-        if ((e = cudaFuncSetAttribute(hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem))) return e;
+        if ((e = smem_limit(reinterpret_cast<const void*>(hist_kernel), (int)smem))) return e;
         hist_kernel<<<n_hist, kHistThreads, smem, st>>>(p.idx, P, E, n_hist, p.local_rank, p.cnt);
         ++*launches;
     }

@@ -303,7 +303,7 @@ cudaError_t launch_router_two_stage(const Shapes& s, const PrefillScratch& p, co
     split_kernel<<<T, 256, 0, st>>>(a.x, T, H, p.x3, p.xnorm, a.y);
     wnorm_kernel<<<(E + 7) / 8, 256, 0, st>>>(a.router_w, E, H, p.wnorm);
     const size_t smem = (size_t)kRS * 2 * kRTile + 1024;
-    cudaError_t e = cudaFuncSetAttribute(router_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = smem_limit(reinterpret_cast<const void*>(router_gemm_kernel), (int)smem);
     if (e != cudaSuccess) return e;
     router_gemm_kernel<<<dim3(E / 128, (T + 127) / 128), kRT, smem, st>>>(a.router_w, p.x3, T, H, E, p.logits,
                                                                          p.status_dev, a.timeout_ns);

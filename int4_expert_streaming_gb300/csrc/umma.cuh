@@ -63,23 +63,34 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst_smem, const void* src, uin
                  : "memory");
 }
 
+// As bar_try_wait, but the thread may sleep up to hint_ns until the phase
+// completes (it resumes as soon as it does), so a waiting warp leaves its
+// issue slots to the warps that work.
+__device__ __forceinline__ bool bar_try_wait_sleep(uint64_t* b, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(b)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait for the phase of the given parity: false once *abort is set or
 // the wait has lasted timeout_ns (the clock starts at the first slow check).
+// Each slow check sleeps on the barrier for up to 20 us.
 __device__ __forceinline__ bool bar_wait(uint64_t* b, uint32_t parity, unsigned long long timeout_ns,
                                          const volatile int* abort) {
     if (bar_try_wait(b, parity)) return true;
     unsigned long long deadline = 0;
-    uint32_t spins = 0;
     for (;;) {
-        if (bar_try_wait(b, parity)) return true;
-        if ((++spins & 63u) == 0) {
-            if (*abort) return false;
-            const unsigned long long now = globaltimer();
-            if (!deadline)
-                deadline = now + timeout_ns;
-            else if (now > deadline)
-                return false;
-        }
+        if (bar_try_wait_sleep(b, parity, 20000u)) return true;
+        if (*abort) return false;
+        const unsigned long long now = globaltimer();
+        if (!deadline)
+            deadline = now + timeout_ns;
+        else if (now > deadline)
+            return false;
     }
 }
 

@@ -82,6 +82,10 @@ class Drift:
     def bias(self, layer: int) -> np.ndarray:
         return synth.zipf_bias(self.perm[layer], self.w.zipf_s)
 
+    def biases(self) -> np.ndarray:
+        """The current bias of every layer, fp32 [n_layers, n_experts]."""
+        return np.stack([self.bias(l) for l in range(self.w.n_layers)]).astype(np.float32)
+
     def advance(self, ctx=None, stream=None) -> None:
         from . import moe_set_router_bias
         self.step += 1
@@ -89,3 +93,13 @@ class Drift:
             synth.drift_step(self.w.seed, l, self.step, self.perm[l], self.w.drift_swaps)
             if ctx is not None:
                 moe_set_router_bias(ctx, l, self.bias(l), stream)
+
+    def schedule(self, n_steps: int) -> np.ndarray:
+        """Advances n_steps times without a context and returns the biases of
+        those steps, fp32 [n_steps, n_layers, n_experts] (inputs computed ahead,
+        like the token batches; send step i with moe_set_router_bias_all)."""
+        out = np.empty((n_steps, self.w.n_layers, self.w.n_experts), np.float32)
+        for i in range(n_steps):
+            self.advance()
+            out[i] = self.biases()
+        return out
