@@ -41,7 +41,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=0, help="timed steps (default: 2048 decode, 1024 stress, 50 prefill)")
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="35b", choices=["35b", "80b", "80b-prefill", "stress"])
+    ap.add_argument("--config", default="35b", choices=["tiny", "35b", "80b", "80b-prefill", "stress"])
     ap.add_argument("--tokens", type=int, default=0, help="prefill tokens per step (default: the workload's)")
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--bits", type=int, default=0)
@@ -178,6 +178,19 @@ def cpu_baseline(w, bits, n_samples):
                       f"threads; {secs:.1f} s wall"}
 
 
+def max_over_ranks(ms: float, pg) -> float:
+    """The slowest replica's time in ms (gloo all-reduce MAX, then a barrier);
+    the identity on a single process."""
+    if not pg:
+        return ms
+    import torch
+
+    t = torch.tensor([ms], dtype=torch.float64)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    pg.barrier()
+    return float(t.item())
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -259,11 +272,7 @@ def run_ours(args):
         clocks = clk.stop()
         launches = moe.moe_launch_count(ctx) - l0
         ms = e0.elapsed_time(e1)
-        if pg:
-            t = torch.tensor([ms])
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            ms = float(t.item())
-            pg.barrier()
+        ms = max_over_ranks(ms, pg)
         secs = ms / 1e3
         value = args.steps * B * world / secs
         gbs = expert_bytes * args.steps / secs / 1e9
@@ -387,11 +396,7 @@ def run_prefill(args):
         kms, calls = moe.moe_prefill_kernel_ms(ctx)
         moe.moe_prefill_profile(ctx, False)
         ms = e0.elapsed_time(e1)
-        if pg:
-            t = torch.tensor([ms])
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            ms = float(t.item())
-            pg.barrier()
+        ms = max_over_ranks(ms, pg)
         secs = ms / 1e3
         value = args.steps * T * world / secs
         per_kernel = {n: v / calls for n, v in kms.items()}
@@ -529,11 +534,7 @@ def run_stress(args):
         launches = moe.moe_launch_count(ctx) - l0
         ms = e0.elapsed_time(e1)
         s1 = moe.moe_pool_stats(ctx)
-        if pg:
-            t = torch.tensor([ms])
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            ms = float(t.item())
-            pg.barrier()
+        ms = max_over_ranks(ms, pg)
         secs = ms / 1e3
         value = args.steps * world / secs
 
