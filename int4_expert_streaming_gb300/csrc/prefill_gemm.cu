@@ -47,6 +47,7 @@
 // operands are bf16 (weights dequantised in shared memory), accumulation fp32.
 #include <cuda_bf16.h>
 
+#include "gemm_common.cuh"
 #include "gemv.cuh"
 #include "prefill.h"
 #include "umma.cuh"
@@ -55,6 +56,7 @@ namespace moe {
 namespace {
 
 using namespace umma;
+using namespace gemmc;
 
 constexpr int kLoadWarp = 1;
 constexpr int kEpiWarp0 = 2, kEpiWarps = 8;
@@ -184,117 +186,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t* b, uint32_t parity, const Ge
     int ok = 1;
     if (lane == 0) ok = bar_wait(b, parity, a.timeout_ns, abort) ? 1 : 0;
     return __shfl_sync(kFullMask, ok, 0) != 0;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
-// packed fp32 pairs (one register pair, two IEEE operations per instruction)
-__device__ __forceinline__ uint64_t f2(uint32_t lo, uint32_t hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
-    return r;
-}
-__device__ __forceinline__ uint64_t add_f2(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ uint64_t fma_f2(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
-__device__ __forceinline__ uint32_t bf16x2_of(uint64_t v) {
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-    return pack_bf16(lo, hi);
-}
-
-// code byte i of v as the bits of the float 2^23 + q (exact)
-__device__ __forceinline__ uint32_t code_bits(uint32_t v, int i) { return __byte_perm(v, 0x4B000000u, 0x7440u | i); }
-
-// bf16(fma(s, q, b)) of code bytes (x byte i, y byte j) as a bf16 pair;
-// m2 = (-2^23, -2^23)
-__device__ __forceinline__ uint32_t dq_pair(uint32_t x, int i, uint32_t y, int j, uint64_t s2, uint64_t b2,
-                                            uint64_t m2) {
-    return bf16x2_of(fma_f2(s2, add_f2(f2(code_bits(x, i), code_bits(y, j)), m2), b2));
-}
-
-// 8 consecutive int4 columns (one code word, column c in nibble c)
-__device__ __forceinline__ uint4 dq8_int4(uint32_t wd, uint64_t s2, uint64_t b2, uint64_t m2) {
-    const uint32_t lo = wd & 0x0F0F0F0Fu, hi = (wd >> 4) & 0x0F0F0F0Fu;  // even / odd columns
-    return make_uint4(dq_pair(lo, 0, hi, 0, s2, b2, m2), dq_pair(lo, 1, hi, 1, s2, b2, m2),
-                      dq_pair(lo, 2, hi, 2, s2, b2, m2), dq_pair(lo, 3, hi, 3, s2, b2, m2));
-}
-
-// 8 consecutive int8 columns (two code words, column c in byte c)
-__device__ __forceinline__ uint4 dq8_int8(uint32_t w0, uint32_t w1, uint64_t s2, uint64_t b2, uint64_t m2) {
-    return make_uint4(dq_pair(w0, 0, w0, 1, s2, b2, m2), dq_pair(w0, 2, w0, 3, s2, b2, m2),
-                      dq_pair(w1, 0, w1, 1, s2, b2, m2), dq_pair(w1, 2, w1, 3, s2, b2, m2));
-}
-
-__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                 : "memory");
-}
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr)
-                 : "memory");
-    return v;
-}
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-    uint32_t v;
-    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-    return v;
-}
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-// TMA: the box at (column x, row y) of a 2D map to shared memory, completion
-// counted on the mbarrier
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* b) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            dst),
-        "l"(map), "r"(x), "r"(y), "r"(smem_u32(b))
-        : "memory");
-}
-__device__ __forceinline__ void bar_arrive_expect_tx(uint64_t* b, uint32_t bytes) {
-    asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 st, [%0], %1;\n}" ::"r"(
-                     smem_u32(b)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-// element offset of (row, col) in a pre-swizzled SwiGLU buffer: planes of 64
-// columns, [plane][row][64], 16-byte chunks swizzled by row & 7
-__device__ __forceinline__ size_t h_offset(int rows, int row, int col) {
-    return ((size_t)(col >> 6) * rows + row) * 64 + ((((col >> 3) ^ row) & 7) << 3) + (col & 7);
-}
-
-// 32 lanes x 16 consecutive 32-bit tensor-memory columns
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
-          "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-        : "r"(taddr));
 }
 
 // Dequantiser thread (weight row r of the tile, column half hf): the address
@@ -607,10 +498,19 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             uint4 o[4];
             if (BITS == 4) {
                 const uint4 w = lds128(base + dt * 16);
-                o[0] = dq8_int4(w.x, s2, b2, m2);
-                o[1] = dq8_int4(w.y, s2, b2, m2);
-                o[2] = dq8_int4(w.z, s2, b2, m2);
-                o[3] = dq8_int4(w.w, s2, b2, m2);
+                float cb;
+                if (shifted_bias(s, b, cb)) {
+                    const uint64_t c2 = f2(__float_as_uint(cb), __float_as_uint(cb));
+                    o[0] = dq8_int4_fast(w.x, s2, c2);
+                    o[1] = dq8_int4_fast(w.y, s2, c2);
+                    o[2] = dq8_int4_fast(w.z, s2, c2);
+                    o[3] = dq8_int4_fast(w.w, s2, c2);
+                } else {
+                    o[0] = dq8_int4(w.x, s2, b2, m2);
+                    o[1] = dq8_int4(w.y, s2, b2, m2);
+                    o[2] = dq8_int4(w.z, s2, b2, m2);
+                    o[3] = dq8_int4(w.w, s2, b2, m2);
+                }
             } else {
                 const uint4 w0 = lds128(base + dt * 16), w1 = lds128(base + (kDqThreads + dt) * 16);
                 o[0] = dq8_int8(w0.x, w0.y, s2, b2, m2);

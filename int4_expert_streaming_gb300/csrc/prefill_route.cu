@@ -445,17 +445,21 @@ static bool encode_x_maps(PrefillScratch& p, const Shapes& s, int max_tokens, st
         err = "the driver has no cuTensorMapEncodeTiled";
         return false;
     }
-    auto encode = [&](CUtensorMap* m, void* base, size_t rows, size_t stride_elems) {
-        const cuuint64_t dims[2] = {(cuuint64_t)s.hidden, (cuuint64_t)rows};
+    auto encode = [&](CUtensorMap* m, void* base, size_t cols, size_t rows, size_t stride_elems, uint32_t box_rows,
+                      CUtensorMapSwizzle swz) {
+        const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
         const cuuint64_t strides[1] = {(cuuint64_t)stride_elems * 2};
-        const cuuint32_t box[2] = {64, 64}, estr[2] = {1, 1};
+        const cuuint32_t box[2] = {64, box_rows}, estr[2] = {1, 1};
         return ((EncodeFn)fn)(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     };
     const size_t x_stride = p.two_stage ? 3 * (size_t)s.hidden : (size_t)s.hidden;
-    CUresult r = encode(&p.x_map, p.two_stage ? (void*)p.x3 : (void*)p.x_bf, max_tokens, x_stride);
-    if (r == CUDA_SUCCESS) r = encode(&p.xs_map, p.x_sorted, (size_t)max_tokens * s.top_k, s.hidden);
+    void* xb = p.two_stage ? (void*)p.x3 : (void*)p.x_bf;
+    const size_t P = (size_t)max_tokens * s.top_k;
+    const CUtensorMapSwizzle SW = CU_TENSOR_MAP_SWIZZLE_128B;
+    CUresult r = encode(&p.x_map, xb, s.hidden, max_tokens, x_stride, 64, SW);
+    if (r == CUDA_SUCCESS) r = encode(&p.xs_map, p.x_sorted, s.hidden, P, s.hidden, 64, SW);
     if (r != CUDA_SUCCESS) {
         char buf[96];
         snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (%d)", (int)r);
