@@ -185,6 +185,44 @@ def test_streaming_stack_matches_resident_stack():
         moe.moe_destroy(st)
 
 
+def test_router_bias_updates_all_layers_at_once():
+    """moe_set_router_bias_all equals one moe_set_router_bias per layer (the
+    staged copies run in stream order), on a streaming and on a resident
+    context; a context with a layer not yet loaded refuses it."""
+    w = dataclasses.replace(TINY, n_layers=3, zipf_s=1.1)
+    B = 2
+    a = _ctx(w, max_batch=B, pool_slots=5)
+    b = _ctx(w, max_batch=B, pool_slots=5)
+    r = _ctx(w, max_batch=B)
+    rng = np.random.default_rng(41)
+    try:
+        for step in range(6):
+            bias = (rng.standard_normal((w.n_layers, w.n_experts)) * 2.0).astype(np.float32)
+            for l in range(w.n_layers):
+                moe.moe_set_router_bias(a, l, np.ascontiguousarray(bias[l]))
+            moe.moe_set_router_bias_all(b, bias)
+            moe.moe_set_router_bias_all(r, bias)
+            bias[:] = 0.0  # the host buffer may be reused at once
+            x = torch.from_numpy(synth.tokens(w.seed, 50 + step, B, w.hidden)).cuda()
+            ya, yb, yr = torch.empty_like(x), torch.empty_like(x), torch.empty_like(x)
+            moe.moe_forward_decode_stack(a, 0, w.n_layers, x, B, ya)
+            moe.moe_forward_decode_stack(b, 0, w.n_layers, x, B, yb)
+            moe.moe_forward_decode_stack(r, 0, w.n_layers, x, B, yr)
+            torch.cuda.synchronize()
+            assert torch.equal(ya, yb) and torch.equal(ya, yr)
+        assert np.array_equal(moe.moe_pool_trace(a), moe.moe_pool_trace(b))
+    finally:
+        for c in (a, b, r):
+            moe.moe_destroy(c)
+    part = workload.create_loaded(w, max_batch=B, layers=[0])
+    try:
+        with pytest.raises(moe.MoeError) as e:
+            moe.moe_set_router_bias_all(part, np.zeros((w.n_layers, w.n_experts), np.float32))
+        assert e.value.code == moe.MOE_ESTATE
+    finally:
+        moe.moe_destroy(part)
+
+
 def test_decode_argument_errors():
     w = dataclasses.replace(TINY, n_layers=2)
     ctx = workload.create_loaded(w, max_batch=2, layers=[0])
