@@ -24,7 +24,7 @@ _lock = threading.Lock()
 _lib = None
 
 OK, EINVAL, EMISSING, EPOOL = 0, -1, -2, -3
-POLICY_LFU_RECENCY, POLICY_LRU = 0, 1
+POLICY_LFU_RECENCY, POLICY_LRU, POLICY_LFU_PERSIST, POLICY_LFU_AGED = 0, 1, 2, 3
 HIT, MISS = 0, 1
 
 
@@ -96,7 +96,8 @@ def _load():
         lib.orc_pack_blob.restype = c.c_int
         lib.orc_unpack_blob.argtypes = [c.c_int, c.c_int, c.c_int, vp, vp, vp, vp, vp, vp, vp]
         lib.orc_unpack_blob.restype = c.c_int
-        lib.orc_pool_request.argtypes = [c.c_int, c.c_int, c.c_int, vp, vp, vp, vp, c.c_int64, vp, c.c_int, vp]
+        lib.orc_pool_request.argtypes = [c.c_int, c.c_int, c.c_int, c.c_int, vp, vp, vp, vp, vp, c.c_int64, vp,
+                                          c.c_int, vp]
         lib.orc_pool_request.restype = c.c_int
         _lib = lib
         return lib
@@ -309,14 +310,17 @@ class Layer:
 # --------------------------------------------------------------------------
 
 class PoolSim:
-    """Per-layer LFU+recency (or LRU) slot pool; see orc_pool_request."""
+    """Per-layer slot pool: LFU + recency, LRU, persistent-count LFU or aged LFU
+    (halving every `aging_period` calls); see orc_pool_request."""
 
-    def __init__(self, slots: int, n_experts: int, policy: int = POLICY_LFU_RECENCY, preload: bool = False):
-        self.slots, self.n_experts, self.policy = slots, n_experts, policy
+    def __init__(self, slots: int, n_experts: int, policy: int = POLICY_LFU_RECENCY, preload: bool = False,
+                 aging_period: int = 64):
+        self.slots, self.n_experts, self.policy, self.aging_period = slots, n_experts, policy, aging_period
         self.slot_expert = np.full(slots, -1, np.int32)
         self.slot_freq = np.zeros(slots, np.int64)
         self.slot_last = np.full(slots, -1, np.int64)
         self.expert_slot = np.full(n_experts, -1, np.int32)
+        self.expert_count = np.zeros(n_experts, np.int64)
         self.clock = 0
         if preload:
             if slots < n_experts:
@@ -330,9 +334,10 @@ class PoolSim:
         clock; returns events [(expert, kind, slot, evicted)]."""
         req = np.array(sorted(set(int(e) for e in experts)), np.int32)
         ev = np.empty((max(len(req), 1), 4), np.int32)
-        n = _load().orc_pool_request(self.slots, self.n_experts, self.policy, _p(self.slot_expert),
-                                     _p(self.slot_freq), _p(self.slot_last), _p(self.expert_slot),
-                                     self.clock, _p(req), len(req), _p(ev))
+        n = _load().orc_pool_request(self.slots, self.n_experts, self.policy, self.aging_period,
+                                     _p(self.slot_expert), _p(self.slot_freq), _p(self.slot_last),
+                                     _p(self.expert_slot), _p(self.expert_count), self.clock, _p(req), len(req),
+                                     _p(ev))
         if n < 0:
             raise ValueError(f"orc_pool_request failed ({n})")
         self.clock += 1

@@ -470,15 +470,32 @@ int orc_unpack_blob(int hidden, int inter, int bits, const uint8_t* blob, uint8_
  *    smallest (last, slot index) (policy 1, LRU).  The loaded expert starts
  *    with freq = 1, last = t.  Counts live only while resident.
  *  - |R| > slots is an error.
+ * Two variants of the count [reading of the pages' remark that the counts
+ * could persist across evictions or age over time; neither is specified]:
+ *  - policy 2, persistent LFU: expert_count[e] counts every call that ever
+ *    requested e (incremented for all of R when the call starts, kept across
+ *    evictions); the victim minimises (expert_count of its expert, last,
+ *    slot index).
+ *  - policy 3, aged LFU: policy 0, except that a call whose clock t is a
+ *    positive multiple of aging_period first halves (rounding down) the
+ *    count of every occupied slot.
  * Events (expert, kind 0 = HIT / 1 = MISS, slot, evicted expert or -1) are
  * written in ascending expert order; returns their count.
  */
-int orc_pool_request(int slots, int n_experts, int policy, int32_t* slot_expert, int64_t* slot_freq,
-                     int64_t* slot_last, int32_t* expert_slot, int64_t t, const int32_t* req, int n_req,
-                     int32_t* events) {
+int orc_pool_request(int slots, int n_experts, int policy, int aging_period, int32_t* slot_expert,
+                     int64_t* slot_freq, int64_t* slot_last, int32_t* expert_slot, int64_t* expert_count,
+                     int64_t t, const int32_t* req, int n_req, int32_t* events) {
+    if (policy < 0 || policy > 3 || (policy == 3 && aging_period < 1)) return ORC_EINVAL;
     if (n_req > slots) return ORC_EPOOL;
     for (int i = 0; i < n_req; ++i) {
         if (req[i] < 0 || req[i] >= n_experts || (i > 0 && req[i] <= req[i - 1])) return ORC_EINVAL;
+    }
+    if (policy == 3 && t > 0 && t % aging_period == 0) {
+        for (int k = 0; k < slots; ++k)
+            if (slot_expert[k] >= 0) slot_freq[k] /= 2;
+    }
+    if (policy == 2) {
+        for (int i = 0; i < n_req; ++i) expert_count[req[i]] += 1;
     }
     for (int i = 0; i < n_req; ++i) {
         int e = req[i];
@@ -508,11 +525,16 @@ int orc_pool_request(int slots, int n_experts, int policy, int32_t* slot_expert,
                     continue;
                 }
                 int better;
-                if (policy == 0)
-                    better = slot_freq[k] < slot_freq[victim] ||
-                             (slot_freq[k] == slot_freq[victim] && slot_last[k] < slot_last[victim]);
-                else
+                if (policy == 1) {
                     better = slot_last[k] < slot_last[victim];
+                } else {
+                    int64_t fk = slot_freq[k], fv = slot_freq[victim];
+                    if (policy == 2) {
+                        fk = expert_count[slot_expert[k]];
+                        fv = expert_count[slot_expert[victim]];
+                    }
+                    better = fk < fv || (fk == fv && slot_last[k] < slot_last[victim]);
+                }
                 if (better) victim = k;
             }
             if (victim < 0) return ORC_EPOOL;

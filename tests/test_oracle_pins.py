@@ -3,7 +3,7 @@ hand-derived examples, closed forms, textbook special cases, error bounds and
 invariants.  CPU only."""
 import math
 import os
-from collections import OrderedDict
+from collections import Counter, OrderedDict
 
 import numpy as np
 import pytest
@@ -455,7 +455,8 @@ def _golden_traces():
             continue
         tok = line.split()
         if tok[0] == "policy":
-            cur = {"policy": tok[1], "slots": int(tok[3]), "experts": int(tok[5]), "calls": []}
+            cur = {"policy": tok[1], "slots": int(tok[3]), "experts": int(tok[5]),
+                   "aging": int(tok[7]) if len(tok) > 7 and tok[6] == "aging" else 64, "calls": []}
         elif tok[0] == "call":
             cur["calls"].append(([int(t) for t in tok[2:]], []))
         elif tok[0] == "ev":
@@ -466,13 +467,84 @@ def _golden_traces():
     return blocks
 
 
-@pytest.mark.parametrize("block", range(3))
+_POLICY = {"lfu": oracle.POLICY_LFU_RECENCY, "lru": oracle.POLICY_LRU, "persist": oracle.POLICY_LFU_PERSIST,
+           "aged": oracle.POLICY_LFU_AGED}
+
+
+@pytest.mark.parametrize("block", range(5))
 def test_pool_sim_hand_traces(block):
     b = _golden_traces()[block]
-    pol = oracle.POLICY_LFU_RECENCY if b["policy"] == "lfu" else oracle.POLICY_LRU
-    sim = oracle.PoolSim(b["slots"], b["experts"], pol)
+    sim = oracle.PoolSim(b["slots"], b["experts"], _POLICY[b["policy"]], aging_period=b["aging"])
     for req, want in b["calls"]:
         assert sim.request(req) == want, req
+
+
+def test_pool_golden_covers_every_policy():
+    assert sorted(b["policy"] for b in _golden_traces()) == ["aged", "lfu", "lfu", "lru", "persist"]
+
+
+def test_pool_persistent_lfu_equals_brute_force_perfect_lfu():
+    """Single-expert requests: persistent-count LFU is 'perfect LFU' (all-time
+    counts, kept across evictions) with least-recent use as the tie-break."""
+    rng = np.random.default_rng(11)
+    S, E = 4, 12
+    sim = oracle.PoolSim(S, E, oracle.POLICY_LFU_PERSIST)
+    count, last, slot_of = Counter(), {}, {}
+    for t in range(800):
+        e = int(min(rng.zipf(1.3), E) - 1)
+        (ev,) = sim.request([e])
+        count[e] += 1
+        if e in slot_of:
+            assert ev == (e, oracle.HIT, slot_of[e], -1)
+        else:
+            if len(slot_of) < S:
+                evicted, slot = -1, min(set(range(S)) - set(slot_of.values()))
+            else:
+                evicted = min(slot_of, key=lambda r: (count[r], last[r]))
+                slot = slot_of.pop(evicted)
+            slot_of[e] = slot
+            assert ev == (e, oracle.MISS, slot, evicted)
+        last[e] = t
+
+
+def test_pool_aged_lfu_without_an_aging_call_is_lfu_recency():
+    rng = np.random.default_rng(12)
+    a = oracle.PoolSim(6, 20, oracle.POLICY_LFU_AGED, aging_period=1000)
+    b = oracle.PoolSim(6, 20, oracle.POLICY_LFU_RECENCY)
+    for _ in range(400):
+        req = rng.choice(20, size=int(rng.integers(1, 4)), replace=False)
+        assert a.request(req) == b.request(req)
+
+
+def _belady_hits(stream, S):
+    """Belady's MIN (evict the resident expert whose next request is furthest
+    away): the most hits any policy can reach on single-expert requests."""
+    resident, hits = set(), 0
+    for t, e in enumerate(stream):
+        if e in resident:
+            hits += 1
+            continue
+        if len(resident) == S:
+            def next_use(r):
+                for u in range(t + 1, len(stream)):
+                    if stream[u] == r:
+                        return u
+                return len(stream)
+            resident.remove(max(resident, key=next_use))
+        resident.add(e)
+    return hits
+
+
+@pytest.mark.parametrize("policy", range(4))
+def test_pool_hits_bounded_by_belady_and_compulsory_misses(policy):
+    rng = np.random.default_rng(13 + policy)
+    stream = [int(min(rng.zipf(1.2), 16) - 1) for _ in range(600)]
+    sim = oracle.PoolSim(5, 16, policy, aging_period=8)
+    hits = sum(sim.request([e])[0][1] == oracle.HIT for e in stream)
+    assert hits <= _belady_hits(stream, 5)
+    big = oracle.PoolSim(16, 16, policy, aging_period=8)  # room for every expert: only first requests miss
+    misses = sum(big.request([e])[0][1] == oracle.MISS for e in stream)
+    assert misses == len(set(stream))
 
 
 def test_pool_lru_equals_textbook_lru():
