@@ -71,6 +71,8 @@ extern "C" {
 
 #define MOE_EVICT_LFU_RECENCY 0 /* victim = min (use count, last use, slot) */
 #define MOE_EVICT_LRU 1         /* victim = min (last use, slot) */
+#define MOE_EVICT_LFU_PERSIST 2 /* min (all-time request count of the expert, last use, slot) */
+#define MOE_EVICT_LFU_AGED 3    /* MOE_EVICT_LFU_RECENCY, counts halved every aging_period calls */
 
 /* fault_flags: host-side fault injection for tests (0 in production). */
 #define MOE_FAULT_PINNED_ALLOC 0x1u /* pretend the pinned store allocation failed */
@@ -90,13 +92,14 @@ typedef struct {
     int32_t group_size;   /* 64 only */
     int32_t pool_slots;   /* slots per layer; == n_experts => all resident, no host sync */
     int32_t norm_topk;    /* 1 = renormalise the k weights (softmax over chosen), 0 = full softmax */
-    int32_t policy;       /* MOE_EVICT_LFU_RECENCY or MOE_EVICT_LRU */
+    int32_t policy;       /* MOE_EVICT_* */
     int32_t device;       /* CUDA device ordinal */
     int32_t max_batch;    /* largest B of a decode call, 1..64 */
     int32_t max_tokens;   /* largest T of a prefill call (0 = no prefill) */
     uint32_t fault_flags; /* MOE_FAULT_* (tests only) */
     int32_t fault_arg;
     int32_t timeout_ms;   /* bound on every host wait (<= 0: 10000) */
+    int32_t aging_period; /* MOE_EVICT_LFU_AGED: layer calls between halvings (<= 0: 64) */
 } moe_config;
 
 typedef struct {
@@ -244,6 +247,20 @@ int moe_route_noalloc(moe_ctx* ctx, int32_t layer, const float* x_dev, int32_t B
 int moe_pool_stats(moe_ctx* ctx, int32_t layer, moe_pool_stats_t* out);
 
 /*
+ * Streaming contexts only: empty every layer's pool (the next call of each
+ * layer starts cold), use the first `slots` of the pool_slots slots that
+ * moe_create reserved, and evict by `policy` (MOE_EVICT_*; aging_period as in
+ * moe_config).  Zeroes the counters of moe_pool_stats and the trace; the
+ * per-layer clock restarts at 0.  Synchronises the caller's stream and the
+ * side stream first, so no copy into a slot is in flight.  The size and
+ * policy sweep of the pages' cache section (hit rate moves with pool size
+ * while throughput barely does) runs on one loaded store this way.
+ * MOE_EINVAL: slots outside top_k..pool_slots or unknown policy;
+ * MOE_ESTATE: all-resident context or poisoned context.
+ */
+int moe_pool_reset(moe_ctx* ctx, int32_t slots, int32_t policy, int32_t aging_period, void* stream);
+
+/*
  * Streaming contexts: copy the pool event trace, oldest first, as rows of six
  * int32 (call number of that layer, layer, expert, kind 0 = HIT / 1 = MISS,
  * slot, evicted expert or -1), at most `cap` rows into buf_host; *n_out = rows
@@ -279,13 +296,20 @@ const char* moe_last_error(moe_ctx* ctx);
 
 typedef struct moe_slotpool moe_slotpool;
 
-int moe_slotpool_create(int32_t slots, int32_t n_experts, int32_t policy, moe_slotpool** out);
+/* aging_period: calls between count halvings of MOE_EVICT_LFU_AGED (<= 0: 64) */
+int moe_slotpool_create(int32_t slots, int32_t n_experts, int32_t policy, int32_t aging_period,
+                        moe_slotpool** out);
 void moe_slotpool_destroy(moe_slotpool* p);
 
 /*
  * One request of distinct expert ids, ascending (req_host[n]).  Hits update
  * use count and recency; each miss takes the lowest free slot or evicts the
- * policy's victim among slots not requested in this call.  events_host
+ * policy's victim among slots not requested in this call.  Counts are kept
+ * per slot while resident (LFU_RECENCY, LFU_AGED: a call whose clock is a
+ * positive multiple of the aging period first halves every occupied slot's
+ * count, rounding down) or per expert over all calls (LFU_PERSIST: every
+ * request of the call raises its expert's count before any victim is
+ * chosen).  events_host
  * receives n rows of (expert, kind 0 = HIT / 1 = MISS, slot, evicted or -1)
  * in ascending expert order.  Returns n, or MOE_EPOOL if n > slots,
  * MOE_EINVAL if req is not ascending and in range.

@@ -470,8 +470,10 @@ int orc_unpack_blob(int hidden, int inter, int bits, const uint8_t* blob, uint8_
  *    smallest (last, slot index) (policy 1, LRU).  The loaded expert starts
  *    with freq = 1, last = t.  Counts live only while resident.
  *  - |R| > slots is an error.
- * Two variants of the count [reading of the pages' remark that the counts
- * could persist across evictions or age over time; neither is specified]:
+ * Two variants of the count, not on the pages, for comparison with the
+ * pages' policy (the article's section 3 reports hit rates of 43-70% with
+ * speed nearly flat in cache size; the pages say "LFU" without fixing whether
+ * a count outlives an eviction, so both lifetimes are given a definition):
  *  - policy 2, persistent LFU: expert_count[e] counts every call that ever
  *    requested e (incremented for all of R when the call starts, kept across
  *    evictions); the victim minimises (expert_count of its expert, last,
