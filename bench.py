@@ -49,7 +49,18 @@ def parse_args():
     ap.add_argument("--cpu-samples", type=int, default=64, help="(token, layer) samples of the oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--slots", type=int, default=0, help="stress: slots per layer (default: the workload's 128)")
+    ap.add_argument("--policy", default="lfu", choices=list(POLICIES), help="stress: eviction policy")
+    ap.add_argument("--aging", type=int, default=64, help="stress: calls between halvings of the aged LFU")
+    ap.add_argument("--pool-sweep", action="store_true",
+                    help="stress: one JSON line per (slots, policy) point on one loaded store instead of the bench line")
+    ap.add_argument("--sweep-slots", default="16,32,64,128,256")
+    ap.add_argument("--sweep-policies", default="lfu,lru,persist,aged")
     return ap.parse_args()
+
+
+# eviction policies by name (MOE_EVICT_* values of the C ABI)
+POLICIES = {"lfu": 0, "lru": 1, "persist": 2, "aged": 3}
 
 
 def dist_env():
@@ -489,7 +500,13 @@ def run_stress(args):
     L, H, k = w.n_layers, w.hidden, w.top_k
     moe.build()
     link_peak = host_link_probe_gbs()
-    ctx = workload.create_loaded(w, bits, max_batch=1)
+    if args.pool_sweep:
+        if world > 1:
+            raise SystemExit("--pool-sweep runs on one GPU")
+        return run_pool_sweep(args, w, bits, link_peak)
+    slots = args.slots or w.pool_slots
+    ctx = workload.create_loaded(w, bits, max_batch=1, pool_slots=slots, policy=POLICIES[args.policy],
+                                 aging_period=args.aging)
     try:
         drift = workload.Drift(w)
         n_ring = 256
@@ -571,12 +588,13 @@ def run_stress(args):
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": (f"stress: {L}-layer 80B-shaped decode stack, int{bits} group-64, batch 1, "
-                                    f"{w.pool_slots} of {w.n_experts} slots per layer in HBM, full store in pinned "
+                                    f"{slots} of {w.n_experts} slots per layer in HBM ({args.policy} eviction), "
+                                    "full store in pinned "
                                     f"host memory, Zipf(1.1) routing with {w.drift_swaps} adjacent-rank swaps per "
                                     "layer per step (biases of the timed steps computed before timing and sent with "
                                     "one moe_set_router_bias_all per step), misses by cudaMemcpyAsync on a side "
                                     "stream, pool starts cold"),
-                       "batch": 1, "layers": L, "bits": bits, "pool_slots": w.pool_slots,
+                       "batch": 1, "layers": L, "bits": bits, "pool_slots": slots, "policy": args.policy,
                        "parallelism": "replicas" if world > 1 else "single-gpu",
                        "l2": "inputs larger than L2: each step reads its experts from the HBM pool or the host"},
             "pool": {"hit_rate_all": rate(None, s1), "hit_rate_after_step64": rate(at64, s1) if at64 else None,
@@ -600,6 +618,69 @@ def run_stress(args):
         moe.moe_destroy(ctx)
         if pg:
             pg.destroy_process_group()
+
+
+def run_pool_sweep(args, w, bits, link_peak):
+    """Hit rate and throughput of the streaming stack against pool size and
+    eviction policy.  One context reserves the largest size; before each point
+    moe_pool_reset empties every layer's pool and switches size and policy, and
+    the same token batches and the same drifting router biases replay from
+    step 0.  Each point runs `warmup` untimed steps from the cold pool, then
+    `steps` timed steps, and prints one JSON line."""
+    import torch
+
+    import int4_expert_streaming_gb300 as moe
+    from int4_expert_streaming_gb300 import workload
+
+    sizes = [int(v) for v in args.sweep_slots.split(",")]
+    pols = args.sweep_policies.split(",")
+    L, H = w.n_layers, w.hidden
+    ctx = workload.create_loaded(w, bits, max_batch=1, pool_slots=max(sizes))
+    try:
+        n = args.warmup + args.steps
+        drift = workload.Drift(w)
+        bias = np.concatenate([drift.biases()[None], drift.schedule(n - 1)])  # the bias of every step, from step 0
+        n_ring = 256
+        X = torch.from_numpy(np.stack([synth.tokens(w.seed, s, 1, H) for s in range(n_ring)])).cuda()
+        y = torch.empty((1, H), device="cuda")
+        st = torch.cuda.current_stream()
+        for pol in pols:
+            for S in sizes:
+                moe.moe_pool_reset(ctx, S, POLICIES[pol], args.aging, st)
+
+                def step(i):
+                    moe.moe_set_router_bias_all(ctx, bias[i], st)
+                    moe.moe_forward_decode_stack(ctx, 0, L, X[i % n_ring], 1, y, 1e-6, None, None, None, st)
+
+                for i in range(args.warmup):
+                    step(i)
+                torch.cuda.synchronize()
+                s0 = moe.moe_pool_stats(ctx)
+                clk = ClockSampler(0)
+                clk.start()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(st)
+                for i in range(args.warmup, n):
+                    step(i)
+                e1.record(st)
+                torch.cuda.synchronize()
+                clocks = clk.stop()
+                ms = e0.elapsed_time(e1)
+                s1 = moe.moe_pool_stats(ctx)
+                hits, misses = s1["hits"] - s0["hits"], s1["misses"] - s0["misses"]
+                h2d = s1["h2d_bytes"] - s0["h2d_bytes"]
+                print(json.dumps({
+                    "sweep": "pool", "policy": pol, "slots": S, "n_experts": w.n_experts, "layers": L, "bits": bits,
+                    "aging_period": args.aging if pol == "aged" else None, "warmup": args.warmup,
+                    "steps": args.steps, "value": args.steps / (ms / 1e3), "unit": "tok/s",
+                    "ms_per_step": ms / args.steps, "hit_rate_timed": hits / max(1, hits + misses),
+                    "hit_rate_all": s1["hits"] / max(1, s1["hits"] + s1["misses"]),
+                    "misses_per_step": misses / args.steps, "h2d_gb_per_step": h2d / args.steps / 1e9,
+                    "host_link_gbs_wall": h2d / (ms / 1e3) / 1e9,
+                    "host_link_gbs_during_copies": h2d / max(s1["h2d_ms"] - s0["h2d_ms"], 1e-9) / 1e6,
+                    "host_link_probe_gbs": link_peak, "clocks": clocks}), flush=True)
+    finally:
+        moe.moe_destroy(ctx)
 
 
 def main():

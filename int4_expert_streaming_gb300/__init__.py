@@ -20,7 +20,7 @@ import numpy as np
 from ._build import LIB as _LIB_PATH, build  # noqa: F401
 
 MOE_OK, MOE_EINVAL, MOE_ENOMEM, MOE_ECUDA, MOE_EPOOL, MOE_ETIMEOUT, MOE_ESTATE = 0, -1, -2, -3, -4, -5, -6
-MOE_EVICT_LFU_RECENCY, MOE_EVICT_LRU = 0, 1
+MOE_EVICT_LFU_RECENCY, MOE_EVICT_LRU, MOE_EVICT_LFU_PERSIST, MOE_EVICT_LFU_AGED = 0, 1, 2, 3
 MOE_FAULT_PINNED_ALLOC, MOE_FAULT_MISS_COPY, MOE_FAULT_WAIT_TIMEOUT = 0x1, 0x2, 0x4
 _ERRNAMES = {MOE_EINVAL: "MOE_EINVAL", MOE_ENOMEM: "MOE_ENOMEM", MOE_ECUDA: "MOE_ECUDA", MOE_EPOOL: "MOE_EPOOL",
              MOE_ETIMEOUT: "MOE_ETIMEOUT", MOE_ESTATE: "MOE_ESTATE"}
@@ -29,7 +29,7 @@ _ERRNAMES = {MOE_EINVAL: "MOE_EINVAL", MOE_ENOMEM: "MOE_ENOMEM", MOE_ECUDA: "MOE
 EXPORTS = (
     "moe_blob_bytes", "moe_blob_stride", "moe_pack_expert", "moe_create", "moe_destroy", "moe_load_experts",
     "moe_set_router_bias", "moe_set_router_bias_all", "moe_forward_decode", "moe_forward_decode_stack", "moe_forward_prefill",
-    "moe_pool_stats", "moe_pool_trace", "moe_launch_count", "moe_prefill_profile", "moe_prefill_kernel_ms", "moe_route_noalloc", "moe_last_error", "moe_slotpool_create", "moe_slotpool_destroy",
+    "moe_pool_stats", "moe_pool_reset", "moe_pool_trace", "moe_launch_count", "moe_prefill_profile", "moe_prefill_kernel_ms", "moe_route_noalloc", "moe_last_error", "moe_slotpool_create", "moe_slotpool_destroy",
     "moe_slotpool_request",
 )
 
@@ -44,7 +44,8 @@ class moe_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "n_layers", "hidden", "n_experts", "top_k", "inter", "shared_inter", "bits", "group_size", "pool_slots",
         "norm_topk", "policy", "device", "max_batch", "max_tokens")] + [
-        ("fault_flags", ctypes.c_uint32), ("fault_arg", ctypes.c_int32), ("timeout_ms", ctypes.c_int32)]
+        ("fault_flags", ctypes.c_uint32), ("fault_arg", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
+        ("aging_period", ctypes.c_int32)]
 
 
 class moe_pool_stats_t(ctypes.Structure):
@@ -84,6 +85,7 @@ def load_library(path: str | None = None):
         lib.moe_forward_decode_stack.argtypes = [vp, i32, i32, vp, i32, vp, c.c_float, vp, vp, vp, vp]
         lib.moe_forward_prefill.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp]
         lib.moe_pool_stats.argtypes = [vp, i32, c.POINTER(moe_pool_stats_t)]
+        lib.moe_pool_reset.argtypes = [vp, i32, i32, i32, vp]
         lib.moe_pool_trace.argtypes = [vp, vp, sz, c.POINTER(sz)]
         lib.moe_launch_count.argtypes = [vp, c.POINTER(c.c_uint64)]
         lib.moe_prefill_profile.argtypes = [vp, i32]
@@ -91,7 +93,7 @@ def load_library(path: str | None = None):
         lib.moe_prefill_kernel_ms.argtypes = [vp, c.POINTER(c.c_double), c.POINTER(c.c_int64)]
         lib.moe_last_error.argtypes = [vp]
         lib.moe_last_error.restype = c.c_char_p
-        lib.moe_slotpool_create.argtypes = [i32, i32, i32, c.POINTER(vp)]
+        lib.moe_slotpool_create.argtypes = [i32, i32, i32, i32, c.POINTER(vp)]
         lib.moe_slotpool_destroy.argtypes = [vp]
         lib.moe_slotpool_destroy.restype = None
         lib.moe_slotpool_request.argtypes = [vp, vp, i32, vp]
@@ -220,6 +222,11 @@ def moe_route_noalloc(ctx, layer: int, x, B: int, topk_idx, topk_w, stream=None)
                                             _dev(topk_w, "float32"), _stream(stream)), ctx)
 
 
+def moe_pool_reset(ctx, slots: int, policy: int = MOE_EVICT_LFU_RECENCY, aging_period: int = 0, stream=None) -> None:
+    """Empty every layer's pool, use `slots` of the reserved slots and evict by `policy` (streaming contexts)."""
+    _check(load_library().moe_pool_reset(ctx, slots, policy, aging_period, _stream(stream)), ctx)
+
+
 def moe_pool_stats(ctx, layer: int = -1) -> dict:
     s = moe_pool_stats_t()
     _check(load_library().moe_pool_stats(ctx, layer, ctypes.byref(s)), ctx)
@@ -261,9 +268,9 @@ def moe_last_error(ctx=None) -> str:
     return m.decode() if m else ""
 
 
-def moe_slotpool_create(slots: int, n_experts: int, policy: int = MOE_EVICT_LFU_RECENCY):
+def moe_slotpool_create(slots: int, n_experts: int, policy: int = MOE_EVICT_LFU_RECENCY, aging_period: int = 0):
     h = ctypes.c_void_p()
-    _check(load_library().moe_slotpool_create(slots, n_experts, policy, ctypes.byref(h)))
+    _check(load_library().moe_slotpool_create(slots, n_experts, policy, aging_period, ctypes.byref(h)))
     return h.value
 
 
@@ -282,7 +289,7 @@ def moe_slotpool_request(pool, req) -> list:
 
 def make_config(n_layers, hidden, n_experts, top_k, inter, shared_inter, bits=4, pool_slots=None, norm_topk=True,
                 policy=MOE_EVICT_LFU_RECENCY, device=0, max_batch=1, max_tokens=0, fault_flags=0, fault_arg=0,
-                timeout_ms=0) -> moe_config:
+                timeout_ms=0, aging_period=0) -> moe_config:
     return moe_config(n_layers, hidden, n_experts, top_k, inter, shared_inter, bits, 64,
                       n_experts if pool_slots is None else pool_slots, int(norm_topk), policy, device, max_batch,
-                      max_tokens, fault_flags, fault_arg, timeout_ms)
+                      max_tokens, fault_flags, fault_arg, timeout_ms, aging_period)

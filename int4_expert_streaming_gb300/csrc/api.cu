@@ -109,6 +109,7 @@ struct moe_ctx {
     int pending_timing_layer = -1;  // layer whose miss-copy events are not yet harvested
     std::vector<uint8_t> loaded;
     std::vector<moe_slotpool*> pools;
+    int32_t active_slots = 0;  // slots in use per layer (<= cfg.pool_slots, the reserved stride)
     std::vector<LayerStats> stats;
     std::vector<int32_t> trace;
     cudaStream_t side = nullptr;
@@ -181,7 +182,7 @@ int check_config(const moe_config* g) {
     if (g->group_size != 64) return fail(nullptr, MOE_EINVAL, "group_size must be 64");
     if (g->pool_slots < g->top_k || g->pool_slots > g->n_experts)
         return fail(nullptr, MOE_EINVAL, "pool_slots must be in top_k..n_experts");
-    if (g->policy != MOE_EVICT_LFU_RECENCY && g->policy != MOE_EVICT_LRU)
+    if (g->policy < MOE_EVICT_LFU_RECENCY || g->policy > MOE_EVICT_LFU_AGED)
         return fail(nullptr, MOE_EINVAL, "unknown eviction policy");
     if (g->max_batch < 1 || g->max_batch > 64) return fail(nullptr, MOE_EINVAL, "max_batch must be in 1..64");
     if (g->max_tokens < 0 || g->max_tokens > (1 << 20)) return fail(nullptr, MOE_EINVAL, "max_tokens out of range");
@@ -254,7 +255,7 @@ int serve_layer(moe_ctx* c, int layer, int B, uint32_t epoch, cudaStream_t st) {
     int rc = moe_slotpool_request(c->pools[layer], req.data(), (int32_t)req.size(), ev.data());
     if (rc < 0)
         return fail(c, rc, "slot pool request of %zu experts failed (pool has %d slots)", req.size(),
-                    c->cfg.pool_slots);
+                    c->active_slots);
     LayerStats& S = c->stats[layer];
     const int64_t call_no = S.calls;
     const uint8_t** dirh = c->dir_host + (size_t)layer * E;
@@ -667,8 +668,9 @@ extern "C" int moe_create(const moe_config* cfg, moe_ctx** out) {
         carve(c->gate_mem, c->gate_host);
         carve(gate_dev, c->gate_dev);
         c->pools.assign(L, nullptr);
+        c->active_slots = g.pool_slots;
         for (int l = 0; l < L; ++l)
-            if ((rc = moe_slotpool_create(g.pool_slots, E, g.policy, &c->pools[l]))) {
+            if ((rc = moe_slotpool_create(g.pool_slots, E, g.policy, g.aging_period, &c->pools[l]))) {
                 c->err = "slot pool creation failed";
                 return bail(rc);
             }
@@ -970,6 +972,40 @@ extern "C" int moe_pool_stats(moe_ctx* c, int32_t layer, moe_pool_stats_t* out) 
         out->calls += S.calls;
         out->resident += c->resident ? (c->loaded[l] ? g.n_experts : 0) : moe_slotpool_resident(c->pools[l]);
     }
+    return MOE_OK;
+}
+
+extern "C" int moe_pool_reset(moe_ctx* c, int32_t slots, int32_t policy, int32_t aging_period, void* stream) {
+    if (!c) return fail(nullptr, MOE_EINVAL, "ctx is NULL");
+    if (c->poisoned) return fail(c, MOE_ESTATE, "context poisoned by an earlier CUDA error");
+    const moe_config& g = c->cfg;
+    if (c->resident) return fail(c, MOE_ESTATE, "an all-resident context has no pool to reset");
+    if (slots < g.top_k || slots > g.pool_slots)
+        return fail(c, MOE_EINVAL, "slots %d outside top_k..pool_slots (%d..%d)", slots, g.top_k, g.pool_slots);
+    if (policy < MOE_EVICT_LFU_RECENCY || policy > MOE_EVICT_LFU_AGED)
+        return fail(c, MOE_EINVAL, "unknown eviction policy %d", policy);
+    CUDA_TRY(c, cudaSetDevice(g.device));
+    CUDA_TRY(c, cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+    CUDA_TRY(c, cudaStreamSynchronize(c->side));
+    harvest_copy_timing(c);
+    const int L = g.n_layers, E = g.n_experts;
+    std::vector<moe_slotpool*> fresh(L, nullptr);
+    for (int l = 0; l < L; ++l) {
+        const int rc = moe_slotpool_create(slots, E, policy, aging_period, &fresh[l]);
+        if (rc) {
+            for (auto* p : fresh) moe_slotpool_destroy(p);
+            return fail(c, rc, "slot pool creation failed");
+        }
+    }
+    for (auto* p : c->pools) moe_slotpool_destroy(p);
+    c->pools = fresh;
+    c->active_slots = slots;
+    c->cfg.policy = policy;
+    c->cfg.aging_period = aging_period;
+    std::memset(c->dir_host, 0, sizeof(void*) * (size_t)L * E);
+    CUDA_TRY(c, cudaMemset(c->dir, 0, sizeof(void*) * (size_t)L * E));
+    c->stats.assign(L, LayerStats{});
+    c->trace.clear();
     return MOE_OK;
 }
 

@@ -185,6 +185,77 @@ def test_streaming_stack_matches_resident_stack():
         moe.moe_destroy(st)
 
 
+@pytest.mark.parametrize("slots,policy,aging", [(8, 0, 0), (5, 1, 0), (6, 2, 0), (4, 3, 3)])
+def test_pool_reset_size_and_policy_replay_oracle(slots, policy, aging):
+    """moe_pool_reset re-sizes and re-polices a loaded streaming context: after
+    a first run under LFU + recency on all 8 reserved slots, the reset starts
+    every layer cold; then, over whole-stack calls (the graph path), the pool
+    events of each (call, layer) equal the oracle simulator under the new
+    size, policy and aging period fed the routing of an all-resident context,
+    and every output is bitwise the resident context's."""
+    w = dataclasses.replace(TINY, n_layers=2, zipf_s=1.1)
+    B, L, k = 2, 2, TINY.top_k
+    res = _ctx(w, max_batch=B)
+    st = _ctx(w, max_batch=B, pool_slots=8)
+    try:
+        def step(s, ctx, idx_tr=None):
+            x = torch.from_numpy(synth.tokens(w.seed, 300 + s, B, w.hidden)).cuda()
+            y = torch.empty_like(x)
+            moe.moe_forward_decode_stack(ctx, 0, L, x, B, y, 1e-6, None, idx_tr, None)
+            return y
+
+        for s in range(5):
+            step(s, st)
+        moe.moe_pool_reset(st, slots, policy, aging)
+        z = moe.moe_pool_stats(st)
+        assert (z["hits"], z["misses"], z["calls"], z["resident"]) == (0, 0, 0, 0)
+        assert len(moe.moe_pool_trace(st)) == 0
+        sims = [oracle.PoolSim(slots, w.n_experts, policy, aging_period=aging if aging > 0 else 64)
+                for _ in range(L)]
+        idx_tr = torch.empty((L, B, k), dtype=torch.int32, device="cuda")
+        routes = []
+        for s in range(16):
+            ya = step(s, res, idx_tr)
+            yb = step(s, st)
+            torch.cuda.synchronize()
+            assert torch.equal(ya, yb), s
+            routes.append(idx_tr.cpu().numpy().copy())
+        tr = moe.moe_pool_trace(st)
+        tr = tr[np.lexsort((tr[:, 1], tr[:, 0]))]
+        pos = 0
+        for s in range(16):
+            for l in range(L):
+                want = sims[l].request(routes[s][l].reshape(-1))
+                rows = tr[pos:pos + len(want)]
+                assert all(int(r[0]) == s and int(r[1]) == l for r in rows), (s, l)
+                assert [tuple(int(v) for v in r[2:]) for r in rows] == want, (s, l)
+                pos += len(want)
+        assert pos == len(tr)
+        st1 = moe.moe_pool_stats(st)
+        assert st1["misses"] > 0 and st1["resident"] <= L * slots and st1["calls"] == 16 * L
+    finally:
+        moe.moe_destroy(res)
+        moe.moe_destroy(st)
+
+
+def test_pool_reset_errors():
+    w = TINY
+    st = _ctx(w, max_batch=1, pool_slots=6)
+    res = _ctx(w, max_batch=1)
+    try:
+        for args in ((7, 0, 0), (w.top_k - 1, 0, 0), (6, 4, 0), (6, -1, 0)):
+            with pytest.raises(moe.MoeError) as e:
+                moe.moe_pool_reset(st, *args)
+            assert e.value.code == moe.MOE_EINVAL, args
+        with pytest.raises(moe.MoeError) as e:
+            moe.moe_pool_reset(res, 6, 0, 0)
+        assert e.value.code == moe.MOE_ESTATE
+        moe.moe_pool_reset(st, 6, moe.MOE_EVICT_LFU_AGED, 0)  # still usable after refused resets
+    finally:
+        moe.moe_destroy(st)
+        moe.moe_destroy(res)
+
+
 def test_router_bias_updates_all_layers_at_once():
     """moe_set_router_bias_all equals one moe_set_router_bias per layer (the
     staged copies run in stream order), on a streaming and on a resident

@@ -58,15 +58,17 @@ def test_packer_rejects_bad_input(lib):
     assert moe.moe_blob_stride(100, 64, 4) == 0 and moe.moe_blob_stride(256, 64, 3) == 0
 
 
-@pytest.mark.parametrize("policy", [moe.MOE_EVICT_LFU_RECENCY, moe.MOE_EVICT_LRU])
+@pytest.mark.parametrize("policy", [moe.MOE_EVICT_LFU_RECENCY, moe.MOE_EVICT_LRU, moe.MOE_EVICT_LFU_PERSIST,
+                                    moe.MOE_EVICT_LFU_AGED])
 @pytest.mark.parametrize("slots,E,kmax", [(4, 16, 3), (128, 512, 10), (8, 8, 8), (2, 6, 2)])
 def test_slotpool_replays_oracle_pool_sim(lib, policy, slots, E, kmax):
-    """Random Zipf-skewed request streams: events identical to the oracle simulator."""
+    """Random Zipf-skewed request streams: events identical to the oracle simulator
+    (aging every 7 calls, so the aged policy halves many times in 400 calls)."""
     rng = np.random.default_rng(slots * 1000 + E + policy)
     p = 1.0 / np.arange(1, E + 1) ** 1.1
     p /= p.sum()
-    pool = moe.moe_slotpool_create(slots, E, policy)
-    sim = oracle.PoolSim(slots, E, policy)
+    pool = moe.moe_slotpool_create(slots, E, policy, aging_period=7)
+    sim = oracle.PoolSim(slots, E, policy, aging_period=7)
     try:
         for _ in range(400):
             n = int(rng.integers(1, min(kmax, slots) + 1))
@@ -92,10 +94,29 @@ def test_slotpool_errors(lib):
         moe.moe_slotpool_destroy(pool)
     with pytest.raises(moe.MoeError):
         moe.moe_slotpool_create(0, 4)
+    with pytest.raises(moe.MoeError):
+        moe.moe_slotpool_create(2, 4, 4)
+
+
+def test_slotpool_default_aging_period_is_64(lib):
+    """aging_period <= 0 means 64: identical events to an explicit 64."""
+    rng = np.random.default_rng(3)
+    a = moe.moe_slotpool_create(6, 24, moe.MOE_EVICT_LFU_AGED, 0)
+    b = moe.moe_slotpool_create(6, 24, moe.MOE_EVICT_LFU_AGED, 64)
+    sim = oracle.PoolSim(6, 24, oracle.POLICY_LFU_AGED, aging_period=64)
+    try:
+        for _ in range(300):
+            req = sorted(int(v) for v in rng.choice(24, size=3, replace=False))
+            want = sim.request(req)
+            assert moe.moe_slotpool_request(a, req) == want == moe.moe_slotpool_request(b, req)
+    finally:
+        moe.moe_slotpool_destroy(a)
+        moe.moe_slotpool_destroy(b)
 
 
 @pytest.mark.parametrize("field,value", [("hidden", 100), ("bits", 3), ("group_size", 32), ("top_k", 0),
-                                         ("top_k", 17), ("pool_slots", 1), ("max_batch", 65), ("inter", 96)])
+                                         ("top_k", 17), ("pool_slots", 1), ("max_batch", 65), ("inter", 96),
+                                         ("policy", 4), ("policy", -1)])
 def test_create_rejects_bad_config_before_any_gpu_work(lib, field, value):
     cfg = moe.make_config(2, 256, 16, 2, 128, 128)
     setattr(cfg, field, value)
