@@ -69,6 +69,11 @@ struct moe_ctx {
     float* part = nullptr;  // [max_pairs][H] weighted down rows of each pair
     float* xbuf = nullptr;  // [2][max_batch][H]
     float* ybuf = nullptr;  // [max_batch][H]
+    // streaming through the persistent kernel: routing of the layer in flight,
+    // double-buffered by layer parity (idx, w [2][max_batch*top_k], sigma [2][max_batch])
+    int32_t* sr_idx = nullptr;
+    float* sr_w = nullptr;
+    float* sr_sig = nullptr;
     // streaming, whole-stack calls: each layer's input [n_layers][max_batch][H],
     // the last layer's output, and one CUDA graph per layer (and one for the
     // first routing) for the call's batch size
@@ -229,7 +234,7 @@ void harvest_copy_timing(moe_ctx* c) {
 // missed expert's blob into its slot with cudaMemcpyAsync on the side stream
 // (the compute stream waits on an event after the copies) and write the
 // layer's directory, which the dispatch kernel launched next reads.
-int serve_layer(moe_ctx* c, int layer, int B, uint32_t epoch, cudaStream_t st) {
+int serve_layer(moe_ctx* c, int layer, int B, uint32_t epoch, cudaStream_t st, bool* stopped) {
     const int k = c->cfg.top_k, E = c->cfg.n_experts;
     if (c->fault_timeout_armed) {
         c->fault_timeout_armed = false;
@@ -247,8 +252,12 @@ int serve_layer(moe_ctx* c, int layer, int B, uint32_t epoch, cudaStream_t st) {
         }
     }
     std::atomic_thread_fence(std::memory_order_acquire);
+    // behind a persistent launch: did it stop at this layer (else it ran on,
+    // having found every expert of the layer in the directory)?
+    if (stopped) *stopped = c->gate_host.stop[layer] == epoch;
     harvest_copy_timing(c);
-    std::vector<int32_t> req(c->gate_host.idx, c->gate_host.idx + B * k);
+    const int32_t* pub = c->gate_host.idx + (size_t)layer * c->gate_host.idx_stride;
+    std::vector<int32_t> req(pub, pub + B * k);
     std::sort(req.begin(), req.end());
     req.erase(std::unique(req.begin(), req.end()), req.end());
     std::vector<int32_t> ev(4 * req.size());
@@ -256,6 +265,14 @@ int serve_layer(moe_ctx* c, int layer, int B, uint32_t epoch, cudaStream_t st) {
     if (rc < 0)
         return fail(c, rc, "slot pool request of %zu experts failed (pool has %d slots)", req.size(),
                     c->active_slots);
+    if (stopped && !*stopped)
+        for (size_t i = 0; i < req.size(); ++i)
+            if (ev[4 * i + 1] != 0) {  // pool and device directory disagree: nothing later can be trusted
+                fail(c, MOE_ESTATE, "layer %d ran on the device without expert %d, which the pool lacks", layer,
+                     ev[4 * i]);
+                c->poisoned = true;
+                return MOE_ESTATE;
+            }
     LayerStats& S = c->stats[layer];
     const int64_t call_no = S.calls;
     const uint8_t** dirh = c->dir_host + (size_t)layer * E;
@@ -351,6 +368,47 @@ int enq_post(moe_ctx* c, int l, const float* xin, int B, float* yl, cudaStream_t
     return MOE_OK;
 }
 
+// Streaming stacks of a few tokens run on the persistent kernel from layer l
+// to the end of the call, stopping only at a layer with an absent expert
+// (the kernel checks the device directory after publishing the routing).
+// Layer l's routing is given: the route kernels' output when l is the call's
+// first layer, else what the stopped launch left.  Results are bitwise those
+// of the all-resident persistent kernel.
+bool stream_stack_ok(const moe_ctx* c, int B) {
+    return !c->resident && B <= moe::kStackPreferMaxB && moe::stack_supported(c->sh, c->stack, B);
+}
+
+int enq_stack_from(moe_ctx* c, int l, int lend, bool first, const float* x, int B, float eps, float* y,
+                   cudaStream_t st) {
+    moe::StackArgs a{};
+    a.layer0 = l;
+    a.n_layers = lend - l;
+    a.B = B;
+    a.eps = eps;
+    a.x = first ? x : c->xbuf;  // a stopped launch leaves the layer's x in xbuf
+    a.y = y;
+    a.router_w = c->router_w;
+    a.router_bias = c->router_bias;
+    a.shared_gate = c->cfg.shared_inter > 0 ? c->shared_gate : nullptr;
+    a.dir = c->dir;
+    a.shared_pool = c->cfg.shared_inter > 0 ? c->shared_pool : nullptr;
+    a.shared_stride = c->shared_stride;
+    a.rin_idx = first ? c->idx : c->sr_idx;
+    a.rin_w = first ? c->w : c->sr_w;
+    a.rin_sig = first ? c->sigma : c->sr_sig;
+    // the launch reads x and rin_* in its first layer and writes these only
+    // at a later layer's stop, after every CTA has passed its first layer
+    a.x_out = c->xbuf;
+    a.rout_idx = c->sr_idx;
+    a.rout_w = c->sr_w;
+    a.rout_sig = c->sr_sig;
+    a.pub = &c->gate_dev;
+    const cudaError_t e = moe::launch_stack(c->sh, c->stack, a, st);
+    if (e != cudaSuccess) return fail(c, MOE_ECUDA, "decode stack launch failed: %s", cudaGetErrorString(e));
+    c->launches += 1;
+    return MOE_OK;
+}
+
 // One CUDA graph per layer for whole-stack calls of B tokens: [0] routes layer
 // 0 from xring[0]; [1 + l] runs layer l's dispatch .. combine and, below the
 // last layer, renormalises into xring[l + 1] and routes layer l + 1.
@@ -408,10 +466,29 @@ int stream_layers(moe_ctx* c, int layer0, int n, const float* x, int B, float* y
     const uint32_t epoch = ++c->epoch ? c->epoch : ++c->epoch;  // never 0
     *const_cast<volatile uint32_t*>(c->gate_host.epoch) = epoch;
     std::atomic_thread_fence(std::memory_order_seq_cst);
+    const bool plain = !x_trace && !idx_trace && !y_trace && !uidx && !uw;
+    if (plain && stream_stack_ok(c, B)) {
+        // route the first layer, serve it, then one persistent launch that the
+        // host relaunches only from layers that miss
+        c->launches += 3;
+        int rc = enq_route(c, layer0, x, B, nullptr, nullptr, st);
+        if (!rc) rc = serve_layer(c, layer0, B, epoch, st, nullptr);
+        if (!rc) rc = enq_stack_from(c, layer0, layer0 + n, true, x, B, eps, y, st);
+        for (int l = layer0 + 1; l < layer0 + n && !rc; ++l) {
+            bool stopped = false;
+            rc = serve_layer(c, l, B, epoch, st, &stopped);
+            if (!rc && stopped) rc = enq_stack_from(c, l, layer0 + n, false, x, B, eps, y, st);
+        }
+        return rc;
+    }
     const bool whole = layer0 == 0 && n == L && !x_trace && !idx_trace && !y_trace && !uidx && !uw;
     if (whole && !c->graphs_off && (c->graph_B != B || c->graph_eps != eps)) {
+        const bool was_poisoned = c->poisoned;
         if (build_graphs(c, B, eps)) {
-            c->graphs_off = true;  // fall back to launches for the rest of the context's life
+            // a launch that cannot be captured failed on the capture stream
+            // only: fall back to plain launches for the rest of the context's life
+            c->graphs_off = true;
+            c->poisoned = was_poisoned;
             c->err.clear();
         }
     }
@@ -420,7 +497,7 @@ int stream_layers(moe_ctx* c, int layer0, int n, const float* x, int B, float* y
         CUDA_TRY(c, cudaGraphLaunch(c->graphs[0], st));
         c->launches += 3;
         for (int l = 0; l < n; ++l) {
-            int rc = serve_layer(c, l, B, epoch, st);
+            int rc = serve_layer(c, l, B, epoch, st, nullptr);
             if (rc) return rc;
             CUDA_TRY(c, cudaGraphLaunch(c->graphs[1 + l], st));
             c->launches += l == L - 1 ? 4 : 8;
@@ -438,7 +515,7 @@ int stream_layers(moe_ctx* c, int layer0, int n, const float* x, int B, float* y
     int rc = route(0);
     for (int i = 0; i < n && !rc; ++i) {
         const int l = layer0 + i;
-        if ((rc = serve_layer(c, l, B, epoch, st))) break;
+        if ((rc = serve_layer(c, l, B, epoch, st, nullptr))) break;
         const bool last = i == n - 1;
         float* yl = last ? y : (y_trace ? y_trace + i * tok : c->ybuf);
         if ((rc = enq_post(c, l, xin, B, yl, st))) break;
@@ -506,6 +583,9 @@ extern "C" void moe_destroy(moe_ctx* c) {
     cudaFree(c->part);
     cudaFree(c->xbuf);
     cudaFree(c->ybuf);
+    cudaFree(c->sr_idx);
+    cudaFree(c->sr_w);
+    cudaFree(c->sr_sig);
     for (cudaGraphExec_t g : c->graphs)
         if (g) cudaGraphExecDestroy(g);
     cudaFree(c->xring);
@@ -581,6 +661,9 @@ extern "C" int moe_create(const moe_config* cfg, moe_ctx** out) {
         (rc = dev_alloc(c, &c->part, (size_t)s.max_pairs * H, "down partials")) ||
         (rc = dev_alloc(c, &c->xbuf, (size_t)2 * Bm * H, "xbuf")) ||
         (rc = dev_alloc(c, &c->ybuf, (size_t)Bm * H, "ybuf")) ||
+        (rc = dev_alloc(c, &c->sr_idx, (size_t)2 * Bm * k, "streamed routing")) ||
+        (rc = dev_alloc(c, &c->sr_w, (size_t)2 * Bm * k, "streamed routing weights")) ||
+        (rc = dev_alloc(c, &c->sr_sig, (size_t)2 * Bm, "streamed shared gates")) ||
         (rc = dev_alloc(c, &c->xd.words, (size_t)Bm * H * 3 / 4, "token digits")) ||
         (rc = dev_alloc(c, &c->xd.sums, (size_t)Bm * H / 16, "token digit sums")) ||
         (rc = dev_alloc(c, &c->xd.exps, (size_t)Bm, "token exponents")))
@@ -626,10 +709,11 @@ extern "C" int moe_create(const moe_config* cfg, moe_ctx** out) {
         rc = moe::prefill_alloc(c->pre, s, g.max_tokens, g.device, c->err);
         if (rc) return bail(rc);
     }
-    if (c->resident) {
-        rc = moe::stack_alloc(c->stack, s, L, Bm, g.device, c->err);
-        if (rc) return bail(rc);
-    } else {
+    // the persistent kernel serves all-resident stacks and, one layer per
+    // launch, streaming stacks of a few tokens
+    rc = moe::stack_alloc(c->stack, s, L, Bm, g.device, c->err);
+    if (rc) return bail(rc);
+    if (!c->resident) {
         if (g.fault_flags & MOE_FAULT_PINNED_ALLOC) {
             c->err = "pinned store allocation failed (injected)";
             return bail(MOE_ENOMEM);
@@ -643,7 +727,7 @@ extern "C" int moe_create(const moe_config* cfg, moe_ctx** out) {
             c->err = buf;
             return bail(MOE_ENOMEM);
         }
-        const size_t gate_bytes = sizeof(uint32_t) * ((size_t)L + 1) + sizeof(int32_t) * Bm * k;
+        const size_t gate_bytes = sizeof(uint32_t) * (2 * (size_t)L + 1) + sizeof(int32_t) * (size_t)L * Bm * k;
         if (cudaHostAlloc(reinterpret_cast<void**>(&c->dir_host), sizeof(void*) * (size_t)L * E,
                           cudaHostAllocDefault) != cudaSuccess ||
             cudaHostAlloc(&c->gate_mem, gate_bytes, cudaHostAllocMapped) != cudaSuccess) {
@@ -663,7 +747,9 @@ extern "C" int moe_create(const moe_config* cfg, moe_ctx** out) {
             uint32_t* w = static_cast<uint32_t*>(base);
             g.ready = w;
             g.epoch = w + L;
-            g.idx = reinterpret_cast<int32_t*>(w + L + 1);
+            g.stop = w + L + 1;
+            g.idx = reinterpret_cast<int32_t*>(w + 2 * L + 1);
+            g.idx_stride = Bm * k;
         };
         carve(c->gate_mem, c->gate_host);
         carve(gate_dev, c->gate_dev);
@@ -810,7 +896,7 @@ extern "C" int moe_forward_decode_stack(moe_ctx* c, int32_t layer0, int32_t n, c
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int H = c->cfg.hidden, k = c->cfg.top_k;
     const size_t tok = (size_t)B * H;
-    if (c->resident && moe::stack_last_status(c->stack))
+    if (moe::stack_last_status(c->stack))
         return fail(c, MOE_ETIMEOUT, "a device-side wait of an earlier decode-stack launch ran out (status %d)",
                     moe::stack_last_status(c->stack)) == MOE_ETIMEOUT
                    ? (c->poisoned = true, MOE_ETIMEOUT)

@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(1024) route_dispatch_kernel(
     if ((mode & 1) && pub.ready) {
         // streaming, single CTA: publish the routing to the host
         __syncthreads();
-        for (int i = threadIdx.x; i < B * k; i += blockDim.x) pub.idx[i] = idx[i];
+        for (int i = threadIdx.x; i < B * k; i += blockDim.x) pub.idx[(size_t)pub_layer * pub.idx_stride + i] = idx[i];
         __threadfence_system();
         __syncthreads();
         if (threadIdx.x == 0) pub.ready[pub_layer] = *pub.epoch;
@@ -488,7 +488,8 @@ cudaError_t launch_route_dispatch(const Shapes& s, int mode, const float* logits
         if (pub && !fused_pub) {
             cudaError_t e = cudaGetLastError();
             if (e != cudaSuccess) return e;
-            publish_kernel<<<1, 256, 0, st>>>(idx, B * s.top_k, pub->idx, pub->ready + pub_layer, pub->epoch);
+            publish_kernel<<<1, 256, 0, st>>>(idx, B * s.top_k, pub->idx + (size_t)pub_layer * pub->idx_stride,
+                                              pub->ready + pub_layer, pub->epoch);
         }
     }
     if (mode & 2) {

@@ -71,7 +71,9 @@ struct Dispatch {
 struct HostGate {
     volatile uint32_t* ready;        // [n_layers] epoch of the last routing published per layer
     const volatile uint32_t* epoch;  // [1] the epoch of the current call, written by the host
-    int32_t* idx;                    // [max_batch * top_k] the published routing
+    volatile uint32_t* stop;         // [n_layers] epoch of the call whose persistent launch stopped there
+    int32_t* idx;                    // [n_layers][idx_stride] the published routing of each layer
+    int idx_stride;                  // max_batch * top_k
 };
 
 struct Shapes {

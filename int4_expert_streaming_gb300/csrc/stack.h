@@ -1,4 +1,5 @@
-// stack.h -- the persistent decode-stack kernel (all experts resident).
+// stack.h -- the persistent decode-stack kernel (all-resident stacks, and
+// streaming stacks that stop for the host only at layers that miss).
 #pragma once
 
 #include <string>
@@ -34,6 +35,18 @@ struct StackArgs {
     const uint8_t* const* dir;
     const uint8_t* shared_pool;
     size_t shared_stride;
+    // streaming: the first layer's routing is given (idx and w [B*k], shared
+    // gate [B]); later layers publish their routing through `pub` and run on
+    // while their experts are resident; the launch stops at the first layer
+    // that is not, leaving that layer's x and routing in x_out / rout_*
+    const int32_t* rin_idx;
+    const float* rin_w;
+    const float* rin_sig;
+    float* x_out;
+    int32_t* rout_idx;
+    float* rout_w;
+    float* rout_sig;
+    const HostGate* pub;
 };
 
 // largest batch the decode stack sends to the persistent kernel (measured crossover)

@@ -26,6 +26,17 @@
 // section "Capability boundaries", README introduction) and keeps HBM busy
 // with bulk copies issued as soon as routing is known.
 //
+// Streaming contexts use it with the host's slot pool behind it.  A launch's
+// first layer takes its routing from a buffer (rin_*: written by the route
+// kernels or by the launch before) instead of computing it.  Every later
+// layer publishes its routing to mapped host memory, where the host runs the
+// pool's bookkeeping in order, and then checks its experts against the
+// device directory: when all are resident the launch simply goes on; at the
+// first layer with an absent expert it leaves that layer's x and routing for
+// the next launch, marks the layer as stopped and exits.  The host copies the
+// missing experts on its side stream and launches again from that layer, so
+// it is on the critical path only for layers that miss.
+//
 // Every wait is bounded (%globaltimer): a poll or an mbarrier wait that does
 // not complete within kWaitNs sets the status word; every CTA then stops at
 // its next wait, drains its outstanding copies (again bounded) and exits.  The
@@ -68,6 +79,25 @@ struct Params {
     unsigned* sync;             // [1] CTAs finished, [2] epoch base
     int* status;
     int* status_host;
+    // streaming launch (rin_idx non-null): the first layer's routing is given
+    // (idx, w [B*k], sigma [B]); every later layer's routing is published to
+    // mapped host memory (pub_idx row l, then pub_ready[l] = *pub_epoch).  A
+    // layer whose experts are all resident (non-null directory entries) runs
+    // on; at the first one that is not, the launch writes that layer's x and
+    // routing for the next launch (x_out [B*H], rout_* like rin_*), sets
+    // pub_stop[l] = *pub_epoch before the ready word, and stops.
+    const int32_t* rin_idx;
+    const float* rin_w;
+    const float* rin_sig;
+    float* x_out;
+    int32_t* rout_idx;
+    float* rout_w;
+    float* rout_sig;
+    int32_t* pub_idx;
+    int pub_stride;
+    volatile uint32_t* pub_ready;
+    volatile uint32_t* pub_stop;
+    const volatile uint32_t* pub_epoch;
     // shared-memory plan
     int rE, rS, jn;
     int p_bytes;
@@ -373,6 +403,8 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const Params p) {
     for (int l = p.layer0; l < lend && ok; ++l) {
         const int li = l - p.layer0, par = l & 1;
         const uint32_t ep = ep0 + (uint32_t)li;
+        const bool given = l == p.layer0 && p.rin_idx != nullptr;  // routing from rin_*
+        const bool streamed = l > p.layer0 && p.rin_idx != nullptr;  // routing published, residency checked
         // the next layer's router and shared rows do not depend on this layer:
         // fetch them now (their buffer was last read in the previous layer)
         if (l + 1 < lend) {
@@ -464,9 +496,11 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const Params p) {
         // router rows and shared rows (prefetched), the shared gate
         {
             const uint8_t* pb = Pbuf + par * p.p_bytes;
-            const int n_tasks = ne + ns + B;
+            // given routing: no router rows and no shared gate
+            const int na = given ? 0 : ne, nb = ns;
+            const int n_tasks = na + nb + (given ? 0 : B);
             for (int task = warp; task < n_tasks; task += kSW) {
-                if (task < ne) {
+                if (task < na) {
                     const int e = e0 + task;
                     const float bias = p.router_bias[(size_t)l * E + e];
                     const uint16_t* row = reinterpret_cast<const uint16_t*>(pb + (size_t)task * 2 * H);
@@ -474,8 +508,8 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const Params p) {
                         const float v = router_logit(row, xs + t * H, H, bias, lane);
                         if (lane == 0) ll_store(p.lg_ll + (size_t)par * kMaxB * E + (size_t)t * E + e, v, ep);
                     }
-                } else if (task < ne + ns) {
-                    const int rr = task - ne;
+                } else if (task < na + nb) {
+                    const int rr = task - na;
                     const uint8_t* sq = pb + (size_t)p.rE * 2 * H;
                     const uint8_t* gq = sq + (size_t)rr * qb;
                     const uint8_t* uq = sq + (size_t)(p.rS + rr) * qb;
@@ -492,7 +526,7 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const Params p) {
                                      silu_mul(g, u), ep);
                     }
                 } else {
-                    const int t = task - ne - ns;
+                    const int t = task - na - nb;
                     const float sg =
                         p.Is > 0 ? shared_gate(p.shared_gate + (size_t)l * H, xs + t * H, H, lane) : 0.0f;
                     if (lane == 0) ds->sig[t] = sg;
@@ -509,6 +543,13 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const Params p) {
         uint32_t* c_key = reinterpret_cast<uint32_t*>(tp);  // [B][C]
         tp += r16i(B * C * 4);
         int32_t* c_idx = reinterpret_cast<int32_t*>(tp);  // [B][C], -1 = empty
+        if (given) {
+            for (int i = tid; i < B * k; i += kST) {
+                ds->idx[i / k][i % k] = p.rin_idx[i];
+                ds->w[i / k][i % k] = p.rin_w[i];
+            }
+            if (tid < B) ds->sig[tid] = p.Is > 0 ? p.rin_sig[tid] : 0.0f;
+        } else {
         {
             const bool got = ll_read(p.lg_ll + (size_t)par * kMaxB * E, B * E, ep, s_lg, tid, kST, p.status);
             if (!__syncthreads_and(got ? 1 : 0)) {
@@ -589,7 +630,34 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const Params p) {
             __syncwarp();
             topk_weights(s_lg + t * E, E, k, p.norm_topk, lane, ds->val[t], ds->w[t]);
         }
+        }  // routing computed
         __syncthreads();
+        if (streamed) {
+            // residency of the layer's experts: the same answer in every CTA
+            const bool absent = tid < B * k && p.dir[(size_t)l * E + ds->idx[tid / k][tid % k]] == nullptr;
+            const bool stop = __syncthreads_or(absent ? 1 : 0) != 0;
+            if (c == 0) {
+                int32_t* row = p.pub_idx + (size_t)l * p.pub_stride;
+                for (int i = tid; i < B * k; i += kST) row[i] = ds->idx[i / k][i % k];
+                if (stop) {
+                    for (int i = tid; i < B * H; i += kST) p.x_out[i] = xs[i];
+                    for (int i = tid; i < B * k; i += kST) {
+                        p.rout_idx[i] = ds->idx[i / k][i % k];
+                        p.rout_w[i] = ds->w[i / k][i % k];
+                    }
+                    if (tid < B) p.rout_sig[tid] = ds->sig[tid];
+                }
+                __threadfence_system();
+                __syncthreads();
+                if (tid == 0) {
+                    const uint32_t e = *p.pub_epoch;
+                    if (stop) p.pub_stop[l] = e;
+                    __threadfence_system();
+                    p.pub_ready[l] = e;
+                }
+            }
+            if (stop) break;  // the host fetches the missing experts and launches again from this layer
+        }
         if (p.idx_trace && c == 0 && tid < B * k) p.idx_trace[(size_t)li * B * k + tid] = ds->idx[tid / k][tid % k];
         // dispatch (warp 0): pairs sorted by (expert, token) by rank (pair key
         // expert << 3 | token), then active experts in ascending id
@@ -1012,6 +1080,14 @@ cudaError_t launch_stack(const Shapes& sh, StackScratch& s, const StackArgs& a, 
     p.shared_pool = a.shared_pool, p.shared_stride = a.shared_stride;
     p.lg_ll = s.lg_ll, p.h_ll = s.h_ll, p.y_ll = s.y_ll, p.h_stride = sh.h_stride, p.hp = s.hp;
     p.sync = s.sync, p.status = s.status, p.status_host = s.status_host_dev;
+    if (a.rin_idx) {
+        if (!a.rin_w || !a.rin_sig || !a.pub || !a.x_out || !a.rout_idx || !a.rout_w || !a.rout_sig)
+            return cudaErrorInvalidValue;
+        p.rin_idx = a.rin_idx, p.rin_w = a.rin_w, p.rin_sig = a.rin_sig;
+        p.x_out = a.x_out, p.rout_idx = a.rout_idx, p.rout_w = a.rout_w, p.rout_sig = a.rout_sig;
+        p.pub_idx = a.pub->idx, p.pub_stride = a.pub->idx_stride;
+        p.pub_ready = a.pub->ready, p.pub_stop = a.pub->stop, p.pub_epoch = a.pub->epoch;
+    }
     void* f = select_kernel(sh.bits, nper_of(sh.hidden, sh.bits));
     void* args[] = {&p};
     return cudaLaunchCooperativeKernel(f, dim3(s.grid), dim3(kST), args, (size_t)p.smem_bytes, st);

@@ -166,20 +166,31 @@ def test_streaming_pool_trace_and_placement_invariance():
         moe.moe_destroy(st)
 
 
-def test_streaming_stack_matches_resident_stack():
-    w = dataclasses.replace(TINY, n_layers=2)
-    B = 3
-    res = _ctx(w, max_batch=B)
-    st = _ctx(w, max_batch=B, pool_slots=6, policy=moe.MOE_EVICT_LRU)
+@pytest.mark.parametrize("B,L,max_batch,slots", [(3, 2, 3, 6), (1, 4, 1, 6), (2, 3, 8, 6), (5, 2, 8, 12)])
+def test_streaming_stack_matches_resident_stack(B, L, max_batch, slots):
+    """Whole-stack calls of a streaming context equal the resident context's
+    bitwise: up to 3 tokens through the persistent kernel one layer per launch
+    (routing handed between launches), more through the per-layer kernels."""
+    w = dataclasses.replace(TINY, n_layers=L)
+    res = _ctx(w, max_batch=max_batch)
+    st = _ctx(w, max_batch=max_batch, pool_slots=slots, policy=moe.MOE_EVICT_LRU)
     try:
-        for step in range(4):
+        for step in range(6):
             x = torch.from_numpy(synth.tokens(w.seed, 7 + step, B, w.hidden)).cuda()
             ya, yb = torch.empty_like(x), torch.empty_like(x)
-            moe.moe_forward_decode_stack(res, 0, 2, x, B, ya)
-            moe.moe_forward_decode_stack(st, 0, 2, x, B, yb)
+            moe.moe_forward_decode_stack(res, 0, L, x, B, ya)
+            moe.moe_forward_decode_stack(st, 0, L, x, B, yb)
             torch.cuda.synchronize()
-            assert torch.equal(ya, yb)
-        assert moe.moe_pool_stats(st)["misses"] > 0
+            assert torch.equal(ya, yb), step
+        s = moe.moe_pool_stats(st)
+        assert s["misses"] > 0 and s["calls"] == 6 * L
+        # a call over the upper layers only
+        x = torch.from_numpy(synth.tokens(w.seed, 99, B, w.hidden)).cuda()
+        ya, yb = torch.empty_like(x), torch.empty_like(x)
+        moe.moe_forward_decode_stack(res, 1, L - 1, x, B, ya)
+        moe.moe_forward_decode_stack(st, 1, L - 1, x, B, yb)
+        torch.cuda.synchronize()
+        assert torch.equal(ya, yb)
     finally:
         moe.moe_destroy(res)
         moe.moe_destroy(st)
