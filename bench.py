@@ -31,6 +31,10 @@ import synth  # noqa: E402
 
 METRIC = "MoE-stack decode tok/s; expert-weight HBM GB/s as fraction of GB300 peak"
 FALLBACK_HBM_GBS = 6800.0
+# DRAM bytes (read + write) of one decode-stack launch per layer: an ncu capture
+# of the 35B-shaped int4 stack at batch 1 (4 layers, 68.064512 + 1.394432 MB),
+# scaled by the layer count; valid for that workload and the current kernel
+STACK_35B_DRAM_BYTES_PER_LAYER = 69.458944e6 / 4
 FALLBACK_BF16_TFLOPS = 1700.0
 PREFILL_METRIC = "MoE prefill tok/s; grouped-GEMM bf16 TFLOP/s as fraction of GB300 dense peak"
 
@@ -315,7 +319,10 @@ def run_ours(args):
                        "l2": f"inputs larger than L2: {expert_bytes / 1e6:.1f} MB of expert weights per step"},
             "expert_gbs": gbs, "hbm_frac": gbs / peak,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
-                         "peak_kind": peak_kind, "traffic": None,
+                         "peak_kind": peak_kind,
+                         "traffic": (STACK_35B_DRAM_BYTES_PER_LAYER * L
+                                     if (w.name, B, bits, w.hidden, w.n_experts) == ("35b", 1, 4, 2048, 256) else None),
+                         "traffic_unit": "DRAM bytes per launch (ncu, 4-layer capture scaled by layers)",
                          "kernel": "decode stack (one forward_decode_stack call per step)",
                          "bytes_per_launch": expert_bytes, "router_bytes_per_launch": router_bytes},
             "gpu_launches": int(launches),
