@@ -161,6 +161,33 @@ def test_prefill_single_token_equals_decode_to_bf16():
         moe.moe_destroy(ctx)
 
 
+@pytest.mark.parametrize("w,T", [(TINY_ZIPF, 200), (WIDE, 160)])
+def test_prefill_equals_decode_batches(w, T):
+    """One prefill of T tokens against the same tokens decoded in batches of up
+    to 64 (the full-sequence against incremental check, for the MoE layer):
+    identical experts, routing weights to a few fp32 roundings, outputs within the
+    bf16 rounding of the prefill operands (rel-L2 below 2^-7)."""
+    ctx = workload.create_loaded(w, max_tokens=T, max_batch=64)
+    try:
+        x_np = synth.tokens(w.seed, 21, T, w.hidden)
+        y_p, i_p, w_p = _prefill(ctx, w, x_np)
+        ys, idxs, ws = [], [], []
+        for t0 in range(0, T, 64):
+            xb = torch.from_numpy(x_np[t0:t0 + 64]).cuda()
+            B = xb.shape[0]
+            y = torch.empty_like(xb)
+            idx = torch.empty((B, w.top_k), dtype=torch.int32, device="cuda")
+            wt = torch.empty((B, w.top_k), dtype=torch.float32, device="cuda")
+            moe.moe_forward_decode(ctx, 0, xb, B, y, idx, wt, torch.cuda.current_stream())
+            torch.cuda.synchronize()
+            ys.append(y.cpu().numpy()), idxs.append(idx.cpu().numpy()), ws.append(wt.cpu().numpy())
+        assert np.array_equal(i_p, np.concatenate(idxs))
+        np.testing.assert_allclose(w_p, np.concatenate(ws), rtol=5e-6, atol=2e-7)  # each is within 2e-6 of the oracle
+        assert_close(y_p, np.concatenate(ys), rel_l2=2.0 ** -7, max_abs_frac=2.0 ** -5)
+    finally:
+        moe.moe_destroy(ctx)
+
+
 def test_wide_prefill_sampled_rows():
     """Hidden 2048 / inter 512 (the 80B expert shape), 64 experts, Zipf-skewed
     routing; 600 tokens, oracle on a seeded sample of 48 rows plus all routes."""
