@@ -68,6 +68,7 @@ extern "C" {
 #define MOE_EPOOL -4    /* a call needs more distinct experts than the pool has slots */
 #define MOE_ETIMEOUT -5 /* a bounded host or device wait ran out */
 #define MOE_ESTATE -6   /* wrong call order, unloaded layer, or poisoned context */
+#define MOE_EIO -7      /* an expert container could not be opened, read or written, or is malformed */
 
 #define MOE_EVICT_LFU_RECENCY 0 /* victim = min (use count, last use, slot) */
 #define MOE_EVICT_LRU 1         /* victim = min (last use, slot) */
@@ -78,6 +79,9 @@ extern "C" {
 #define MOE_FAULT_PINNED_ALLOC 0x1u /* pretend the pinned store allocation failed */
 #define MOE_FAULT_MISS_COPY 0x2u    /* fail the fault_arg-th miss copy (0-based), without issuing it */
 #define MOE_FAULT_WAIT_TIMEOUT 0x4u /* treat the next host wait as timed out */
+
+/* store_flags */
+#define MOE_STORE_DIRECT 0x1u /* read blobs with O_DIRECT (buffered where the file system has none) */
 
 typedef struct moe_ctx moe_ctx;
 
@@ -100,6 +104,9 @@ typedef struct {
     int32_t fault_arg;
     int32_t timeout_ms;   /* bound on every host wait (<= 0: 10000) */
     int32_t aging_period; /* MOE_EVICT_LFU_AGED: layer calls between halvings (<= 0: 64) */
+    uint32_t store_flags; /* MOE_STORE_* */
+    const char* store_path; /* streaming only: expert container (moe_store_create) that holds the routed
+                               blobs; NULL = a pinned host store filled by moe_load_experts */
 } moe_config;
 
 typedef struct {
@@ -140,7 +147,9 @@ int moe_pack_expert(int32_t hidden, int32_t inter, int32_t bits, const uint8_t* 
  * Validate cfg, allocate the HBM slot pool (n_layers x pool_slots x stride,
  * 64-bit offsets), the device directory, scratch and, when streaming, the
  * pinned host store (n_layers x n_experts x stride) and the side stream.
- * Errors: MOE_EINVAL (bad config, nothing allocated), MOE_ENOMEM, MOE_ECUDA.
+ * Errors: MOE_EINVAL (bad config, nothing allocated), MOE_ENOMEM, MOE_ECUDA,
+ * MOE_EIO (store_path cannot be opened, or its header does not match the
+ * config's n_layers, n_experts, hidden, inter and bits).
  */
 int moe_create(const moe_config* cfg, moe_ctx** out);
 
@@ -158,6 +167,9 @@ void moe_destroy(moe_ctx* ctx);
  *   router_bias_host fp32 [n_experts] or NULL (= zeros)
  * All-resident: blobs go straight to their HBM slots (slot = expert id).
  * Streaming: blobs go to the pinned store; the layer's pool starts empty.
+ * Streaming from an expert container (store_path): blobs_host must be NULL
+ * (the container holds them; each miss is one positioned read of it into a
+ * pinned staging buffer, then the copy to the slot).
  * Synchronous (returns when the copies are done).
  */
 int moe_load_experts(moe_ctx* ctx, int32_t layer, const void* blobs_host, size_t stride,
@@ -289,6 +301,29 @@ int moe_prefill_kernel_ms(moe_ctx* ctx, double* ms_out, int64_t* calls);
 int moe_launch_count(moe_ctx* ctx, uint64_t* out);
 
 const char* moe_last_error(moe_ctx* ctx);
+
+/* ------------------------------------------------------------------ */
+/* expert container: routed blobs on disk, one positioned read per blob  */
+/* ------------------------------------------------------------------ */
+/*
+ * [Swiftlet article, section 2 "Fixed-stride pread reads"; README, "How it
+ * works": routed experts repacked into a container of fixed-stride blobs, one
+ * pread per expert, no mmap.]  Layout (this library's): a 4096-byte little-
+ * endian header (magic "MOEXPRT1", version 1, n_layers, n_experts, hidden,
+ * inter, bits, group size 64, stride, data offset 4096), then blob (l, e) at
+ * 4096 + (l * n_experts + e) * stride, stride = moe_blob_stride(hidden,
+ * inter, bits).  Host only; MOE_EIO on any I/O failure, a bad header or a
+ * file shorter than its header says.
+ */
+/* Create (or truncate) a container sized for every blob (unwritten blobs read as zeros). */
+int moe_store_create(const char* path, int32_t n_layers, int32_t n_experts, int32_t hidden, int32_t inter,
+                     int32_t bits);
+/* Write all blobs of one layer: blobs_host [n_experts][stride]. */
+int moe_store_write_layer(const char* path, int32_t layer, const void* blobs_host, size_t stride);
+/* shape_out[5] = {n_layers, n_experts, hidden, inter, bits}; *stride_out = stride. */
+int moe_store_info(const char* path, int32_t* shape_out, uint64_t* stride_out);
+/* Read one blob (stride bytes) into dst_host (cap >= stride). */
+int moe_store_read(const char* path, int32_t layer, int32_t expert, void* dst_host, size_t cap);
 
 /* ------------------------------------------------------------------ */
 /* the slot-pool policy on its own (host only; used by the context)      */

@@ -19,18 +19,19 @@ import numpy as np
 
 from ._build import LIB as _LIB_PATH, build  # noqa: F401
 
-MOE_OK, MOE_EINVAL, MOE_ENOMEM, MOE_ECUDA, MOE_EPOOL, MOE_ETIMEOUT, MOE_ESTATE = 0, -1, -2, -3, -4, -5, -6
+MOE_OK, MOE_EINVAL, MOE_ENOMEM, MOE_ECUDA, MOE_EPOOL, MOE_ETIMEOUT, MOE_ESTATE, MOE_EIO = 0, -1, -2, -3, -4, -5, -6, -7
+MOE_STORE_DIRECT = 0x1
 MOE_EVICT_LFU_RECENCY, MOE_EVICT_LRU, MOE_EVICT_LFU_PERSIST, MOE_EVICT_LFU_AGED = 0, 1, 2, 3
 MOE_FAULT_PINNED_ALLOC, MOE_FAULT_MISS_COPY, MOE_FAULT_WAIT_TIMEOUT = 0x1, 0x2, 0x4
 _ERRNAMES = {MOE_EINVAL: "MOE_EINVAL", MOE_ENOMEM: "MOE_ENOMEM", MOE_ECUDA: "MOE_ECUDA", MOE_EPOOL: "MOE_EPOOL",
-             MOE_ETIMEOUT: "MOE_ETIMEOUT", MOE_ESTATE: "MOE_ESTATE"}
+             MOE_ETIMEOUT: "MOE_ETIMEOUT", MOE_ESTATE: "MOE_ESTATE", MOE_EIO: "MOE_EIO"}
 
 # every symbol include/moe.h declares
 EXPORTS = (
     "moe_blob_bytes", "moe_blob_stride", "moe_pack_expert", "moe_create", "moe_destroy", "moe_load_experts",
     "moe_set_router_bias", "moe_set_router_bias_all", "moe_forward_decode", "moe_forward_decode_stack", "moe_forward_prefill",
     "moe_pool_stats", "moe_pool_reset", "moe_pool_trace", "moe_launch_count", "moe_prefill_profile", "moe_prefill_kernel_ms", "moe_route_noalloc", "moe_last_error", "moe_slotpool_create", "moe_slotpool_destroy",
-    "moe_slotpool_request",
+    "moe_slotpool_request", "moe_store_create", "moe_store_write_layer", "moe_store_info", "moe_store_read",
 )
 
 
@@ -45,7 +46,7 @@ class moe_config(ctypes.Structure):
         "n_layers", "hidden", "n_experts", "top_k", "inter", "shared_inter", "bits", "group_size", "pool_slots",
         "norm_topk", "policy", "device", "max_batch", "max_tokens")] + [
         ("fault_flags", ctypes.c_uint32), ("fault_arg", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
-        ("aging_period", ctypes.c_int32)]
+        ("aging_period", ctypes.c_int32), ("store_flags", ctypes.c_uint32), ("store_path", ctypes.c_char_p)]
 
 
 class moe_pool_stats_t(ctypes.Structure):
@@ -97,6 +98,10 @@ def load_library(path: str | None = None):
         lib.moe_slotpool_destroy.argtypes = [vp]
         lib.moe_slotpool_destroy.restype = None
         lib.moe_slotpool_request.argtypes = [vp, vp, i32, vp]
+        lib.moe_store_create.argtypes = [c.c_char_p, i32, i32, i32, i32, i32]
+        lib.moe_store_write_layer.argtypes = [c.c_char_p, i32, vp, sz]
+        lib.moe_store_info.argtypes = [c.c_char_p, c.POINTER(c.c_int32), c.POINTER(c.c_uint64)]
+        lib.moe_store_read.argtypes = [c.c_char_p, i32, i32, vp, sz]
         for name in EXPORTS:
             if name not in ("moe_destroy", "moe_slotpool_destroy", "moe_blob_bytes", "moe_blob_stride",
                             "moe_last_error"):
@@ -289,7 +294,37 @@ def moe_slotpool_request(pool, req) -> list:
 
 def make_config(n_layers, hidden, n_experts, top_k, inter, shared_inter, bits=4, pool_slots=None, norm_topk=True,
                 policy=MOE_EVICT_LFU_RECENCY, device=0, max_batch=1, max_tokens=0, fault_flags=0, fault_arg=0,
-                timeout_ms=0, aging_period=0) -> moe_config:
+                timeout_ms=0, aging_period=0, store_path=None, store_flags=0) -> moe_config:
+    """store_path: an expert container (moe_store_create) for a streaming context; the
+    library copies the path, and ctypes keeps the encoded string alive with the struct."""
     return moe_config(n_layers, hidden, n_experts, top_k, inter, shared_inter, bits, 64,
                       n_experts if pool_slots is None else pool_slots, int(norm_topk), policy, device, max_batch,
-                      max_tokens, fault_flags, fault_arg, timeout_ms, aging_period)
+                      max_tokens, fault_flags, fault_arg, timeout_ms, aging_period, store_flags,
+                      os.fsencode(store_path) if store_path is not None else None)
+
+
+# --------------------------------------------------------------------------
+# expert container (routed blobs on disk; host only)
+# --------------------------------------------------------------------------
+
+def moe_store_create(path, n_layers: int, n_experts: int, hidden: int, inter: int, bits: int) -> None:
+    _check(load_library().moe_store_create(os.fsencode(path), n_layers, n_experts, hidden, inter, bits))
+
+
+def moe_store_write_layer(path, layer: int, blobs, stride: int) -> None:
+    """blobs: host uint8 [n_experts * stride] (the layer's packed routed blobs)."""
+    b = np.ascontiguousarray(blobs, np.uint8)
+    _check(load_library().moe_store_write_layer(os.fsencode(path), layer, _ptr(b), stride))
+
+
+def moe_store_info(path) -> dict:
+    shape = (ctypes.c_int32 * 5)()
+    stride = ctypes.c_uint64()
+    _check(load_library().moe_store_info(os.fsencode(path), shape, ctypes.byref(stride)))
+    return dict(zip(("n_layers", "n_experts", "hidden", "inter", "bits"), list(shape)), stride=stride.value)
+
+
+def moe_store_read(path, layer: int, expert: int, stride: int) -> np.ndarray:
+    out = np.empty(stride, np.uint8)
+    _check(load_library().moe_store_read(os.fsencode(path), layer, expert, _ptr(out), stride))
+    return out

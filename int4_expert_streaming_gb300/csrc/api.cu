@@ -15,7 +15,10 @@
 // fixed-stride container (article section 2; explainer "Flujo de Inferencia"
 // steps 3-6).  The compute stream waits on an event recorded after the copies,
 // which is this library's explicit hazard management between slot refills and
-// the kernels that read them.
+// the kernels that read them.  A streaming context can instead take its
+// routed blobs from an expert container on disk (store.cpp): a miss is then
+// one positioned read of the blob into a pinned staging buffer followed by the
+// same copy, which is Swiftlet's own fetch path.
 #include <algorithm>
 #include <atomic>
 #include <chrono>
@@ -29,6 +32,7 @@
 #include <vector>
 
 #include "moe_internal.h"
+#include "store.h"
 #include "prefill.h"
 #include "stack.h"
 
@@ -98,6 +102,15 @@ struct moe_ctx {
 
     // host
     uint8_t* store = nullptr;
+    // streaming from an expert container: the open file and a pinned staging
+    // ring, each buffer reused only after its copy to the slot has run
+    moe::StoreFile file{};
+    std::string store_path;
+    static constexpr int kStage = 16;
+    uint8_t* stage = nullptr;  // [kStage][stride]
+    cudaEvent_t stage_ev[kStage] = {};
+    bool stage_used[kStage] = {};
+    int stage_next = 0;
     const uint8_t** dir_host = nullptr;  // streaming: the host's directory (pinned), copied to dir on misses
     // streaming: mapped pinned block: ready [n_layers] (uint32, written by the
     // publish kernel), the call's epoch (written by the host), then the
@@ -190,6 +203,9 @@ int check_config(const moe_config* g) {
     if (g->policy < MOE_EVICT_LFU_RECENCY || g->policy > MOE_EVICT_LFU_AGED)
         return fail(nullptr, MOE_EINVAL, "unknown eviction policy");
     if (g->max_batch < 1 || g->max_batch > 64) return fail(nullptr, MOE_EINVAL, "max_batch must be in 1..64");
+    if (g->store_flags & ~MOE_STORE_DIRECT) return fail(nullptr, MOE_EINVAL, "unknown store_flags");
+    if (g->store_path && g->pool_slots == g->n_experts)
+        return fail(nullptr, MOE_EINVAL, "store_path needs a streaming context (pool_slots < n_experts)");
     if (g->max_tokens < 0 || g->max_tokens > (1 << 20)) return fail(nullptr, MOE_EINVAL, "max_tokens out of range");
     return MOE_OK;
 }
@@ -290,7 +306,20 @@ int serve_layer(moe_ctx* c, int layer, int B, uint32_t epoch, cudaStream_t st, b
             dirh[evicted] = nullptr;
         }
         uint8_t* dst = c->pool + ((size_t)layer * c->cfg.pool_slots + slot) * c->stride;
-        const uint8_t* src = c->store + ((size_t)layer * E + e) * c->stride;
+        const uint8_t* src = c->store ? c->store + ((size_t)layer * E + e) * c->stride : nullptr;
+        int stage_i = -1;
+        if (!src) {  // expert container: one positioned read into the next staging buffer
+            stage_i = c->stage_next;
+            c->stage_next = (stage_i + 1) % moe_ctx::kStage;
+            if (c->stage_used[stage_i]) CUDA_TRY(c, cudaEventSynchronize(c->stage_ev[stage_i]));
+            uint8_t* buf = c->stage + (size_t)stage_i * c->stride;
+            if (moe::store_read_blob(c->file, layer, e, buf) != MOE_OK) {
+                fail(c, MOE_EIO, "reading expert %d of layer %d from %s failed", e, layer, c->store_path.c_str());
+                c->poisoned = true;  // the pool already counts the expert as resident
+                return MOE_EIO;
+            }
+            src = buf;
+        }
         if (!any_miss) {
             CUDA_TRY(c, cudaEventRecord(c->ev_copy0, c->side));
             any_miss = true;
@@ -302,6 +331,10 @@ int serve_layer(moe_ctx* c, int layer, int B, uint32_t epoch, cudaStream_t st, b
         c->miss_copies++;
         // the slot's previous expert was last read before this routing was published
         CUDA_TRY(c, cudaMemcpyAsync(dst, src, c->stride, cudaMemcpyHostToDevice, c->side));
+        if (stage_i >= 0) {
+            CUDA_TRY(c, cudaEventRecord(c->stage_ev[stage_i], c->side));
+            c->stage_used[stage_i] = true;
+        }
         S.h2d_bytes += c->stride;
         dirh[e] = dst;
     }
@@ -599,6 +632,10 @@ extern "C" void moe_destroy(moe_ctx* c) {
     moe::prefill_free(c->pre);
     for (cudaEvent_t e : c->prof_ev) cudaEventDestroy(e);
     if (c->store) cudaFreeHost(c->store);
+    moe::store_close(c->file);
+    if (c->stage) cudaFreeHost(c->stage);
+    for (cudaEvent_t e : c->stage_ev)
+        if (e) cudaEventDestroy(e);
     if (c->dir_host) cudaFreeHost(c->dir_host);
     if (c->gate_mem) cudaFreeHost(c->gate_mem);
     for (auto* p : c->pools) moe_slotpool_destroy(p);
@@ -620,6 +657,10 @@ extern "C" int moe_create(const moe_config* cfg, moe_ctx** out) {
     moe_ctx* c = new (std::nothrow) moe_ctx;
     if (!c) return fail(nullptr, MOE_ENOMEM, "host allocation failed");
     c->cfg = *cfg;
+    if (cfg->store_path) {
+        c->store_path = cfg->store_path;
+        c->cfg.store_path = c->store_path.c_str();
+    }
     const moe_config& g = c->cfg;
     c->resident = g.pool_slots == g.n_experts;
     c->stride = moe_blob_stride(g.hidden, g.inter, g.bits);
@@ -718,14 +759,47 @@ extern "C" int moe_create(const moe_config* cfg, moe_ctx** out) {
             c->err = "pinned store allocation failed (injected)";
             return bail(MOE_ENOMEM);
         }
-        const size_t store_bytes = (size_t)L * E * c->stride;
-        if (cudaHostAlloc(reinterpret_cast<void**>(&c->store), store_bytes, cudaHostAllocDefault) != cudaSuccess) {
-            cudaGetLastError();
-            c->store = nullptr;
-            char buf[160];
-            snprintf(buf, sizeof buf, "cudaHostAlloc of the %zu-byte pinned store failed", store_bytes);
-            c->err = buf;
-            return bail(MOE_ENOMEM);
+        if (g.store_path) {
+            if (moe::store_open(g.store_path, (g.store_flags & MOE_STORE_DIRECT) != 0, c->file) != MOE_OK) {
+                c->err = "cannot open the expert container " + c->store_path;
+                return bail(MOE_EIO);
+            }
+            const moe::StoreShape& f = c->file.shape;
+            if (f.n_layers != L || f.n_experts != E || f.hidden != H || f.inter != g.inter || f.bits != g.bits ||
+                f.stride != c->stride) {
+                c->err = "the expert container " + c->store_path + " does not match the config";
+                return bail(MOE_EIO);
+            }
+            if (cudaHostAlloc(reinterpret_cast<void**>(&c->stage), (size_t)moe_ctx::kStage * c->stride,
+                              cudaHostAllocDefault) != cudaSuccess) {
+                cudaGetLastError();
+                c->stage = nullptr;
+                c->err = "cudaHostAlloc of the staging ring failed";
+                return bail(MOE_ENOMEM);
+            }
+            if (c->file.direct && reinterpret_cast<uintptr_t>(c->stage) % 4096 != 0) {
+                moe::store_close(c->file);  // direct reads want page-aligned buffers: read through the page cache
+                if (moe::store_open(g.store_path, false, c->file) != MOE_OK) {
+                    c->err = "cannot open the expert container " + c->store_path;
+                    return bail(MOE_EIO);
+                }
+            }
+            for (auto& e : c->stage_ev)
+                if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+                    c->err = "cudaEventCreate failed";
+                    return bail(MOE_ECUDA);
+                }
+        } else {
+            const size_t store_bytes = (size_t)L * E * c->stride;
+            if (cudaHostAlloc(reinterpret_cast<void**>(&c->store), store_bytes, cudaHostAllocDefault) !=
+                cudaSuccess) {
+                cudaGetLastError();
+                c->store = nullptr;
+                char buf[160];
+                snprintf(buf, sizeof buf, "cudaHostAlloc of the %zu-byte pinned store failed", store_bytes);
+                c->err = buf;
+                return bail(MOE_ENOMEM);
+            }
         }
         const size_t gate_bytes = sizeof(uint32_t) * (2 * (size_t)L + 1) + sizeof(int32_t) * (size_t)L * Bm * k;
         if (cudaHostAlloc(reinterpret_cast<void**>(&c->dir_host), sizeof(void*) * (size_t)L * E,
@@ -784,8 +858,12 @@ extern "C" int moe_load_experts(moe_ctx* c, int32_t layer, const void* blobs, si
     if (c->poisoned) return fail(c, MOE_ESTATE, "context poisoned by an earlier CUDA error");
     const moe_config& g = c->cfg;
     if (layer < 0 || layer >= g.n_layers) return fail(c, MOE_EINVAL, "layer %d out of range", layer);
-    if (!blobs || !router_w_host) return fail(c, MOE_EINVAL, "blobs and router weights are required");
-    if (stride != c->stride) return fail(c, MOE_EINVAL, "stride %zu != expected %zu", stride, c->stride);
+    const bool from_file = c->file.fd >= 0;
+    if (!router_w_host) return fail(c, MOE_EINVAL, "router weights are required");
+    if (from_file != (blobs == nullptr))
+        return fail(c, MOE_EINVAL, from_file ? "blobs must be NULL: the expert container holds them"
+                                             : "blobs are required");
+    if (!from_file && stride != c->stride) return fail(c, MOE_EINVAL, "stride %zu != expected %zu", stride, c->stride);
     if ((g.shared_inter > 0) != (shared_blob_host != nullptr) || (g.shared_inter > 0) != (shared_gate_host != nullptr))
         return fail(c, MOE_EINVAL, "shared blob and shared gate are required iff shared_inter > 0");
     CUDA_TRY(c, cudaSetDevice(g.device));
@@ -796,7 +874,7 @@ extern "C" int moe_load_experts(moe_ctx* c, int32_t layer, const void* blobs, si
         std::vector<const uint8_t*> d(E);
         for (int e = 0; e < E; ++e) d[e] = c->pool + ((size_t)layer * E + e) * c->stride;
         CUDA_TRY(c, cudaMemcpy(c->dir + (size_t)layer * E, d.data(), sizeof(void*) * E, cudaMemcpyHostToDevice));
-    } else {
+    } else if (!from_file) {
         std::memcpy(c->store + (size_t)layer * layer_bytes, blobs, layer_bytes);
     }
     if (g.shared_inter > 0) {

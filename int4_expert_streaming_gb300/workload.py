@@ -10,7 +10,8 @@ import numpy as np
 
 import synth
 
-from . import make_config, moe_blob_stride, moe_create, moe_load_experts, moe_pack_expert
+from . import (make_config, moe_blob_stride, moe_create, moe_load_experts, moe_pack_expert, moe_store_create,
+               moe_store_write_layer)
 
 
 def _threads(n=None):
@@ -18,27 +19,31 @@ def _threads(n=None):
 
 
 def layer_blobs(w: "synth.Workload", layer: int, bits: int | None = None, threads: int | None = None,
-                out: np.ndarray | None = None):
-    """Packed routed blobs [E*stride] (uint8), the shared blob, router weights
-    (bf16 bits), shared-gate weights (bf16 bits) and router bias (fp32 or None)."""
+                out: np.ndarray | None = None, routed: bool = True):
+    """Packed routed blobs [E*stride] (uint8; None when routed is False), the
+    shared blob, router weights (bf16 bits), shared-gate weights (bf16 bits)
+    and router bias (fp32 or None)."""
     bits = bits or w.bits
     stride = moe_blob_stride(w.hidden, w.inter, bits)
     E = w.n_experts
-    blobs = out if out is not None else np.empty(E * stride, np.uint8)
-    assert blobs.nbytes >= E * stride
+    blobs = None
+    if routed:
+        blobs = out if out is not None else np.empty(E * stride, np.uint8)
+        assert blobs.nbytes >= E * stride
 
-    def one(e):
-        d = synth.expert(w.seed, layer, e, w.hidden, w.inter, bits, w.sigma)
-        moe_pack_expert(w.hidden, w.inter, bits, d, out=blobs[e * stride:(e + 1) * stride])
+        def one(e):
+            d = synth.expert(w.seed, layer, e, w.hidden, w.inter, bits, w.sigma)
+            moe_pack_expert(w.hidden, w.inter, bits, d, out=blobs[e * stride:(e + 1) * stride])
 
-    with cf.ThreadPoolExecutor(_threads(threads)) as ex:
-        list(ex.map(one, range(E)))
+        with cf.ThreadPoolExecutor(_threads(threads)) as ex:
+            list(ex.map(one, range(E)))
+        blobs = blobs[:E * stride]
     shared = None
     if w.shared_inter > 0:
         shared = moe_pack_expert(w.hidden, w.shared_inter, bits,
                                  synth.expert(w.seed, layer, synth.SHARED, w.hidden, w.shared_inter, bits, w.sigma))
     wr, wsg, beta = synth.layer_inputs(w, layer)
-    return blobs[:E * stride], shared, wr, wsg, beta
+    return blobs, shared, wr, wsg, beta
 
 
 def config_for(w: "synth.Workload", bits: int | None = None, max_batch: int = 1, max_tokens: int = 0,
@@ -51,16 +56,32 @@ def config_for(w: "synth.Workload", bits: int | None = None, max_batch: int = 1,
 
 def create_loaded(w: "synth.Workload", bits: int | None = None, max_batch: int = 1, max_tokens: int = 0,
                   pool_slots: int | None = None, layers=None, threads: int | None = None, **kw):
-    """Create a context for workload w and load every layer (or `layers`)."""
+    """Create a context for workload w and load every layer (or `layers`).
+    With store_path=... (an expert container written by write_store) the
+    routed blobs stay on disk and only the dense parts are loaded."""
     bits = bits or w.bits
     cfg = config_for(w, bits, max_batch, max_tokens, pool_slots, **kw)
+    from_file = cfg.store_path is not None
     ctx = moe_create(cfg)
     stride = moe_blob_stride(w.hidden, w.inter, bits)
-    buf = np.empty(w.n_experts * stride, np.uint8)
+    buf = None if from_file else np.empty(w.n_experts * stride, np.uint8)
     for layer in (range(cfg.n_layers) if layers is None else layers):
-        blobs, shared, wr, wsg, beta = layer_blobs(w, layer, bits, threads, out=buf)
+        blobs, shared, wr, wsg, beta = layer_blobs(w, layer, bits, threads, out=buf, routed=not from_file)
         moe_load_experts(ctx, layer, blobs, stride, shared, wr, wsg if shared is not None else None, beta)
     return ctx
+
+
+def write_store(w: "synth.Workload", path, bits: int | None = None, n_layers: int | None = None,
+                threads: int | None = None) -> None:
+    """Write the routed blobs of the workload's layers into an expert container."""
+    bits = bits or w.bits
+    L = n_layers or w.n_layers
+    moe_store_create(path, L, w.n_experts, w.hidden, w.inter, bits)
+    stride = moe_blob_stride(w.hidden, w.inter, bits)
+    buf = np.empty(w.n_experts * stride, np.uint8)
+    for layer in range(L):
+        blobs, *_ = layer_blobs(w, layer, bits, threads, out=buf)
+        moe_store_write_layer(path, layer, blobs, stride)
 
 
 class Drift:

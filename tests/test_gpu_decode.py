@@ -249,6 +249,41 @@ def test_pool_reset_size_and_policy_replay_oracle(slots, policy, aging):
         moe.moe_destroy(st)
 
 
+@pytest.mark.parametrize("flags,B", [(0, 1), (moe.MOE_STORE_DIRECT, 2), (0, 5)])
+def test_streaming_from_expert_container_equals_pinned_store(tmp_path, flags, B):
+    """Misses read from the expert container (one positioned read per blob
+    into the staging ring, then the copy) give the pinned store's outputs and
+    pool trace exactly; the container's bytes are the packer's."""
+    w = dataclasses.replace(TINY, n_layers=3, zipf_s=1.1)
+    path = tmp_path / "experts.bin"
+    workload.write_store(w, path)
+    a = _ctx(w, max_batch=8, pool_slots=10)
+    b = _ctx(w, max_batch=8, pool_slots=10, store_path=path, store_flags=flags)
+    try:
+        for step in range(8):
+            x = torch.from_numpy(synth.tokens(w.seed, 400 + step, B, w.hidden)).cuda()
+            ya, yb = torch.empty_like(x), torch.empty_like(x)
+            moe.moe_forward_decode_stack(a, 0, w.n_layers, x, B, ya)
+            moe.moe_forward_decode_stack(b, 0, w.n_layers, x, B, yb)
+            torch.cuda.synchronize()
+            assert torch.equal(ya, yb), step
+        assert np.array_equal(moe.moe_pool_trace(a), moe.moe_pool_trace(b))
+        sa, sb = moe.moe_pool_stats(a), moe.moe_pool_stats(b)
+        assert sb["misses"] == sa["misses"] > 0 and sb["h2d_bytes"] == sa["h2d_bytes"]
+        with pytest.raises(moe.MoeError) as e:  # the container holds the routed blobs
+            blobs, shared, wr, wsg, beta = workload.layer_blobs(w, 0)
+            moe.moe_load_experts(b, 0, blobs, moe.moe_blob_stride(w.hidden, w.inter, w.bits), shared, wr, wsg, beta)
+        assert e.value.code == moe.MOE_EINVAL
+    finally:
+        moe.moe_destroy(a)
+        moe.moe_destroy(b)
+    bad = tmp_path / "other.bin"
+    moe.moe_store_create(bad, w.n_layers, w.n_experts, w.hidden, w.inter, 8)  # int8 container for an int4 config
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_create(workload.config_for(w, pool_slots=10, store_path=bad))
+    assert e.value.code == moe.MOE_EIO
+
+
 def test_pool_reset_errors():
     w = TINY
     st = _ctx(w, max_batch=1, pool_slots=6)
