@@ -56,6 +56,9 @@ def parse_args():
     ap.add_argument("--slots", type=int, default=0, help="stress: slots per layer (default: the workload's 128)")
     ap.add_argument("--policy", default="lfu", choices=list(POLICIES), help="stress: eviction policy")
     ap.add_argument("--aging", type=int, default=64, help="stress: calls between halvings of the aged LFU")
+    ap.add_argument("--store-file", default="",
+                    help="stress: read misses from this expert container (written first unless it matches)")
+    ap.add_argument("--store-direct", action="store_true", help="stress: O_DIRECT reads of the container")
     ap.add_argument("--pool-sweep", action="store_true",
                     help="stress: one JSON line per (slots, policy) point on one loaded store instead of the bench line")
     ap.add_argument("--sweep-slots", default="16,32,64,128,256")
@@ -512,8 +515,12 @@ def run_stress(args):
             raise SystemExit("--pool-sweep runs on one GPU")
         return run_pool_sweep(args, w, bits, link_peak)
     slots = args.slots or w.pool_slots
+    store_kw = {}
+    if args.store_file:
+        ensure_store(w, bits, args.store_file)
+        store_kw = dict(store_path=args.store_file, store_flags=moe.MOE_STORE_DIRECT if args.store_direct else 0)
     ctx = workload.create_loaded(w, bits, max_batch=1, pool_slots=slots, policy=POLICIES[args.policy],
-                                 aging_period=args.aging)
+                                 aging_period=args.aging, **store_kw)
     try:
         drift = workload.Drift(w)
         n_ring = 256
@@ -596,8 +603,10 @@ def run_stress(args):
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": (f"stress: {L}-layer 80B-shaped decode stack, int{bits} group-64, batch 1, "
                                     f"{slots} of {w.n_experts} slots per layer in HBM ({args.policy} eviction), "
-                                    "full store in pinned "
-                                    f"host memory, Zipf(1.1) routing with {w.drift_swaps} adjacent-rank swaps per "
+                                    + (f"routed blobs in the expert container {args.store_file} (one "
+                                       f"{'O_DIRECT ' if args.store_direct else ''}pread per miss into pinned "
+                                       "staging), " if args.store_file else "full store in pinned host memory, ")
+                                    + f"Zipf(1.1) routing with {w.drift_swaps} adjacent-rank swaps per "
                                     "layer per step (biases of the timed steps computed before timing and sent with "
                                     "one moe_set_router_bias_all per step), misses by cudaMemcpyAsync on a side "
                                     "stream, pool starts cold"),
@@ -625,6 +634,20 @@ def run_stress(args):
         moe.moe_destroy(ctx)
         if pg:
             pg.destroy_process_group()
+
+
+def ensure_store(w, bits, path):
+    """Write the workload's expert container at `path` unless one with its shape is there."""
+    import int4_expert_streaming_gb300 as moe
+    from int4_expert_streaming_gb300 import workload
+    want = dict(n_layers=w.n_layers, n_experts=w.n_experts, hidden=w.hidden, inter=w.inter, bits=bits,
+                stride=moe.moe_blob_stride(w.hidden, w.inter, bits))
+    try:
+        if moe.moe_store_info(path) == want:
+            return
+    except moe.MoeError:
+        pass
+    workload.write_store(w, path, bits=bits)
 
 
 def run_pool_sweep(args, w, bits, link_peak):
