@@ -48,8 +48,10 @@
  *     its side stream and all scratch.  One host thread per context.
  *   - A CUDA error poisons the context: later calls return MOE_ESTATE.
  *   - All-resident contexts (pool_slots == n_experts) never synchronise the
- *     host in forward calls; streaming contexts synchronise once per layer
- *     call to read the routing result.
+ *     host in forward calls.  Streaming contexts wait (bounded by timeout_ms)
+ *     for each layer's routing, published by the GPU to mapped host memory,
+ *     and run the slot pool on it; the call returns once the last layer has
+ *     been served, with that layer's work still queued on the stream.
  */
 #ifndef MOE_H
 #define MOE_H
@@ -214,6 +216,12 @@ int moe_forward_decode(moe_ctx* ctx, int32_t layer, const float* x_dev, int32_t 
  *   idx_trace_dev int32 [n_layers x B x top_k] chosen experts
  *   y_trace_dev fp32 [n_layers x B x hidden]   layer outputs y_l
  * All-resident contexts run the whole stack as one persistent kernel.
+ * Streaming contexts run up to 3 tokens on the same kernel, which goes on
+ * through layers whose experts are all resident and stops at a layer with an
+ * absent expert; the host fetches the missing experts and launches again
+ * from there (calls with traces use the per-layer kernels).  From 4 tokens
+ * on: per-layer kernels with the host's pool decision between routing and
+ * dispatch of every layer.  All paths give the same bits.
  */
 int moe_forward_decode_stack(moe_ctx* ctx, int32_t layer0, int32_t n_layers, const float* x_dev, int32_t B,
                              float* y_dev, float renorm_eps, float* x_trace_dev, int32_t* idx_trace_dev,
