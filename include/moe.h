@@ -109,6 +109,10 @@ typedef struct {
     uint32_t store_flags; /* MOE_STORE_* */
     const char* store_path; /* streaming only: expert container (moe_store_create) that holds the routed
                                blobs; NULL = a pinned host store filled by moe_load_experts */
+    const int32_t* layer_bits; /* [n_layers] 4 or 8 per layer, a mixed store (NULL = every layer `bits`).
+                                  Blobs of layer l are packed for layer_bits[l]; every slot is sized for the
+                                  widest layer.  Mixed stacks run on the per-layer kernels; no expert
+                                  container (it holds one width).  Copied by moe_create. */
 } moe_config;
 
 typedef struct {
@@ -161,8 +165,9 @@ void moe_destroy(moe_ctx* ctx);
 /*
  * Load one layer (call once per layer before its first forward).  Copies:
  *   blobs_host      [n_experts x stride] routed expert blobs (stride as returned
- *                   by moe_blob_stride for (hidden, inter, bits))
- *   shared_blob_host one blob of the shared expert (stride for shared_inter),
+ *                   by moe_blob_stride for (hidden, inter, the layer's bits))
+ *   shared_blob_host one blob of the shared expert (stride for shared_inter and
+ *                   the layer's bits),
  *                   NULL iff shared_inter == 0
  *   router_w_host   bf16 bits [n_experts x hidden]
  *   shared_gate_host bf16 bits [hidden] (NULL iff shared_inter == 0)

@@ -46,7 +46,8 @@ class moe_config(ctypes.Structure):
         "n_layers", "hidden", "n_experts", "top_k", "inter", "shared_inter", "bits", "group_size", "pool_slots",
         "norm_topk", "policy", "device", "max_batch", "max_tokens")] + [
         ("fault_flags", ctypes.c_uint32), ("fault_arg", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
-        ("aging_period", ctypes.c_int32), ("store_flags", ctypes.c_uint32), ("store_path", ctypes.c_char_p)]
+        ("aging_period", ctypes.c_int32), ("store_flags", ctypes.c_uint32), ("store_path", ctypes.c_char_p),
+        ("layer_bits", ctypes.POINTER(ctypes.c_int32))]
 
 
 class moe_pool_stats_t(ctypes.Structure):
@@ -294,13 +295,20 @@ def moe_slotpool_request(pool, req) -> list:
 
 def make_config(n_layers, hidden, n_experts, top_k, inter, shared_inter, bits=4, pool_slots=None, norm_topk=True,
                 policy=MOE_EVICT_LFU_RECENCY, device=0, max_batch=1, max_tokens=0, fault_flags=0, fault_arg=0,
-                timeout_ms=0, aging_period=0, store_path=None, store_flags=0) -> moe_config:
-    """store_path: an expert container (moe_store_create) for a streaming context; the
-    library copies the path, and ctypes keeps the encoded string alive with the struct."""
-    return moe_config(n_layers, hidden, n_experts, top_k, inter, shared_inter, bits, 64,
-                      n_experts if pool_slots is None else pool_slots, int(norm_topk), policy, device, max_batch,
-                      max_tokens, fault_flags, fault_arg, timeout_ms, aging_period, store_flags,
-                      os.fsencode(store_path) if store_path is not None else None)
+                timeout_ms=0, aging_period=0, store_path=None, store_flags=0, layer_bits=None) -> moe_config:
+    """store_path: an expert container (moe_store_create) for a streaming context;
+    layer_bits: 4 or 8 per layer (a mixed store).  The library copies both at
+    moe_create; until then the struct keeps the Python-side buffers alive."""
+    lb = None
+    if layer_bits is not None:
+        lb = (ctypes.c_int32 * len(layer_bits))(*[int(b) for b in layer_bits])
+    cfg = moe_config(n_layers, hidden, n_experts, top_k, inter, shared_inter, bits, 64,
+                     n_experts if pool_slots is None else pool_slots, int(norm_topk), policy, device, max_batch,
+                     max_tokens, fault_flags, fault_arg, timeout_ms, aging_period, store_flags,
+                     os.fsencode(store_path) if store_path is not None else None,
+                     ctypes.cast(lb, ctypes.POINTER(ctypes.c_int32)) if lb is not None else None)
+    cfg._layer_bits = lb  # keeps the array alive with the struct
+    return cfg
 
 
 # --------------------------------------------------------------------------

@@ -53,7 +53,12 @@ struct LayerStats {
 struct moe_ctx {
     moe_config cfg{};
     moe::Shapes sh{};
-    size_t stride = 0, shared_stride = 0;
+    size_t stride = 0, shared_stride = 0;  // slot pitches: the widest layer's blob strides
+    // per layer: bits, shapes handed to the per-layer kernels, blob strides
+    std::vector<int32_t> lbits;
+    std::vector<moe::Shapes> lsh;
+    std::vector<size_t> lstride, lsstride;
+    bool mixed = false;  // layers of different widths
     bool resident = false, poisoned = false;
     std::string err;
 
@@ -197,6 +202,18 @@ int check_config(const moe_config* g) {
     if (g->shared_inter < 0 || g->shared_inter % 64)
         return fail(nullptr, MOE_EINVAL, "shared_inter must be a multiple of 64");
     if (g->bits != 4 && g->bits != 8) return fail(nullptr, MOE_EINVAL, "bits must be 4 or 8");
+    if (g->layer_bits) {
+        bool mixed = false;
+        for (int l = 0; l < g->n_layers; ++l) {
+            const int b = g->layer_bits[l];
+            if (b != 4 && b != 8) return fail(nullptr, MOE_EINVAL, "layer_bits[%d] = %d: must be 4 or 8", l, b);
+            if (g->inter * b > 4096 || g->shared_inter * b > 4096)
+                return fail(nullptr, MOE_EINVAL, "layer_bits[%d]: inter * bits must be <= 4096", l);
+            mixed |= b != g->layer_bits[0];
+        }
+        if (mixed && g->store_path)
+            return fail(nullptr, MOE_EINVAL, "an expert container holds one width: no store_path with mixed layer_bits");
+    }
     if (g->group_size != 64) return fail(nullptr, MOE_EINVAL, "group_size must be 64");
     if (g->pool_slots < g->top_k || g->pool_slots > g->n_experts)
         return fail(nullptr, MOE_EINVAL, "pool_slots must be in top_k..n_experts");
@@ -330,12 +347,12 @@ int serve_layer(moe_ctx* c, int layer, int B, uint32_t epoch, cudaStream_t st, b
         }
         c->miss_copies++;
         // the slot's previous expert was last read before this routing was published
-        CUDA_TRY(c, cudaMemcpyAsync(dst, src, c->stride, cudaMemcpyHostToDevice, c->side));
+        CUDA_TRY(c, cudaMemcpyAsync(dst, src, c->lstride[layer], cudaMemcpyHostToDevice, c->side));
         if (stage_i >= 0) {
             CUDA_TRY(c, cudaEventRecord(c->stage_ev[stage_i], c->side));
             c->stage_used[stage_i] = true;
         }
-        S.h2d_bytes += c->stride;
+        S.h2d_bytes += c->lstride[layer];
         dirh[e] = dst;
     }
     if (any_miss) {
@@ -355,7 +372,7 @@ int serve_layer(moe_ctx* c, int layer, int B, uint32_t epoch, cudaStream_t st, b
 // Enqueues one layer of an all-resident context.
 int decode_layer(moe_ctx* c, int layer, const float* x, int B, float* y, int32_t* uidx, float* uw,
                  cudaStream_t st) {
-    const moe::Shapes& s = c->sh;
+    const moe::Shapes& s = c->lsh[layer];
     const int E = c->cfg.n_experts;
     const uint16_t* wr = c->router_w + (size_t)layer * E * c->cfg.hidden;
     const float* bias = c->router_bias + (size_t)layer * E;
@@ -375,7 +392,7 @@ int decode_layer(moe_ctx* c, int layer, const float* x, int B, float* y, int32_t
 // Streaming, enqueue helpers.  Routing of layer l: router, top-k and the
 // publication of the routing to the host.
 int enq_route(moe_ctx* c, int l, const float* xin, int B, int32_t* uidx, float* uw, cudaStream_t st) {
-    const moe::Shapes& s = c->sh;
+    const moe::Shapes& s = c->lsh[l];
     const int H = c->cfg.hidden, k = c->cfg.top_k, E = c->cfg.n_experts;
     const uint16_t* wr = c->router_w + (size_t)l * E * H;
     const float* bias = c->router_bias + (size_t)l * E;
@@ -390,7 +407,7 @@ int enq_route(moe_ctx* c, int l, const float* xin, int B, int32_t* uidx, float* 
 // ... and the rest of layer l once the host has served it: dispatch (reading
 // the directory the host has just written), gate/up, down, combine into yl.
 int enq_post(moe_ctx* c, int l, const float* xin, int B, float* yl, cudaStream_t st) {
-    const moe::Shapes& s = c->sh;
+    const moe::Shapes& s = c->lsh[l];
     const int H = c->cfg.hidden, E = c->cfg.n_experts;
     const uint16_t* wsg = c->cfg.shared_inter > 0 ? c->shared_gate + (size_t)l * H : nullptr;
     CUDA_TRY(c, moe::launch_route_dispatch(s, 2, c->logits, xin, wsg, B, c->idx, c->w, c->sigma, nullptr, nullptr,
@@ -408,7 +425,7 @@ int enq_post(moe_ctx* c, int l, const float* xin, int B, float* yl, cudaStream_t
 // first layer, else what the stopped launch left.  Results are bitwise those
 // of the all-resident persistent kernel.
 bool stream_stack_ok(const moe_ctx* c, int B) {
-    return !c->resident && B <= moe::kStackPreferMaxB && moe::stack_supported(c->sh, c->stack, B);
+    return !c->resident && !c->mixed && B <= moe::kStackPreferMaxB && moe::stack_supported(c->sh, c->stack, B);
 }
 
 int enq_stack_from(moe_ctx* c, int l, int lend, bool first, const float* x, int B, float eps, float* y,
@@ -661,12 +678,17 @@ extern "C" int moe_create(const moe_config* cfg, moe_ctx** out) {
         c->store_path = cfg->store_path;
         c->cfg.store_path = c->store_path.c_str();
     }
+    const int L = cfg->n_layers;
+    if (cfg->layer_bits)
+        c->lbits.assign(cfg->layer_bits, cfg->layer_bits + L);
+    else
+        c->lbits.assign(L, cfg->bits);
+    c->cfg.layer_bits = c->lbits.data();
+    c->cfg.bits = c->lbits[0];  // the width of a uniform stack (mixed stacks do not use it)
     const moe_config& g = c->cfg;
     c->resident = g.pool_slots == g.n_experts;
-    c->stride = moe_blob_stride(g.hidden, g.inter, g.bits);
-    c->shared_stride = g.shared_inter > 0 ? moe_blob_stride(g.hidden, g.shared_inter, g.bits) : 0;
     c->fault_timeout_armed = (g.fault_flags & MOE_FAULT_WAIT_TIMEOUT) != 0;
-    const int L = g.n_layers, E = g.n_experts, H = g.hidden, Bm = g.max_batch, k = g.top_k;
+    const int E = g.n_experts, H = g.hidden, Bm = g.max_batch, k = g.top_k;
     moe::Shapes& s = c->sh;
     s.hidden = H, s.n_experts = E, s.top_k = k, s.inter = g.inter, s.shared_inter = g.shared_inter;
     s.bits = g.bits, s.norm_topk = g.norm_topk ? 1 : 0;
@@ -674,6 +696,17 @@ extern "C" int moe_create(const moe_config* cfg, moe_ctx** out) {
     s.max_pairs = Bm * (k + 1);
     s.h_stride = std::max(g.inter, g.shared_inter);
     s.max_work = s.max_act + s.max_pairs / 8 + 1;
+    c->lsh.assign(L, s);
+    c->lstride.assign(L, 0);
+    c->lsstride.assign(L, 0);
+    for (int l = 0; l < L; ++l) {
+        c->lsh[l].bits = c->lbits[l];
+        c->mixed |= c->lbits[l] != c->lbits[0];
+        c->lstride[l] = moe_blob_stride(H, g.inter, c->lbits[l]);
+        c->lsstride[l] = g.shared_inter > 0 ? moe_blob_stride(H, g.shared_inter, c->lbits[l]) : 0;
+        c->stride = std::max(c->stride, c->lstride[l]);
+        c->shared_stride = std::max(c->shared_stride, c->lsstride[l]);
+    }
     c->loaded.assign(L, 0);
     c->stats.assign(L, LayerStats{});
 
@@ -766,7 +799,7 @@ extern "C" int moe_create(const moe_config* cfg, moe_ctx** out) {
             }
             const moe::StoreShape& f = c->file.shape;
             if (f.n_layers != L || f.n_experts != E || f.hidden != H || f.inter != g.inter || f.bits != g.bits ||
-                f.stride != c->stride) {
+                f.stride != c->stride) {  // (a container context is uniform: g.bits is every layer's width)
                 c->err = "the expert container " + c->store_path + " does not match the config";
                 return bail(MOE_EIO);
             }
@@ -863,23 +896,33 @@ extern "C" int moe_load_experts(moe_ctx* c, int32_t layer, const void* blobs, si
     if (from_file != (blobs == nullptr))
         return fail(c, MOE_EINVAL, from_file ? "blobs must be NULL: the expert container holds them"
                                              : "blobs are required");
-    if (!from_file && stride != c->stride) return fail(c, MOE_EINVAL, "stride %zu != expected %zu", stride, c->stride);
+    const size_t ls = c->lstride[layer];  // the layer's blob stride; slots are c->stride apart
+    if (!from_file && stride != ls) return fail(c, MOE_EINVAL, "stride %zu != the layer's %zu", stride, ls);
     if ((g.shared_inter > 0) != (shared_blob_host != nullptr) || (g.shared_inter > 0) != (shared_gate_host != nullptr))
         return fail(c, MOE_EINVAL, "shared blob and shared gate are required iff shared_inter > 0");
     CUDA_TRY(c, cudaSetDevice(g.device));
     const int E = g.n_experts, H = g.hidden;
     const size_t layer_bytes = (size_t)E * c->stride;
     if (c->resident) {
-        CUDA_TRY(c, cudaMemcpy(c->pool + (size_t)layer * layer_bytes, blobs, layer_bytes, cudaMemcpyHostToDevice));
+        uint8_t* dst = c->pool + (size_t)layer * layer_bytes;
+        if (ls == c->stride)
+            CUDA_TRY(c, cudaMemcpy(dst, blobs, layer_bytes, cudaMemcpyHostToDevice));
+        else  // a narrower layer of a mixed stack: one blob per (wider) slot
+            CUDA_TRY(c, cudaMemcpy2D(dst, c->stride, blobs, ls, ls, E, cudaMemcpyHostToDevice));
         std::vector<const uint8_t*> d(E);
         for (int e = 0; e < E; ++e) d[e] = c->pool + ((size_t)layer * E + e) * c->stride;
         CUDA_TRY(c, cudaMemcpy(c->dir + (size_t)layer * E, d.data(), sizeof(void*) * E, cudaMemcpyHostToDevice));
     } else if (!from_file) {
-        std::memcpy(c->store + (size_t)layer * layer_bytes, blobs, layer_bytes);
+        uint8_t* dst = c->store + (size_t)layer * layer_bytes;
+        if (ls == c->stride)
+            std::memcpy(dst, blobs, layer_bytes);
+        else
+            for (int e = 0; e < E; ++e)
+                std::memcpy(dst + (size_t)e * c->stride, static_cast<const uint8_t*>(blobs) + (size_t)e * ls, ls);
     }
     if (g.shared_inter > 0) {
-        CUDA_TRY(c, cudaMemcpy(c->shared_pool + (size_t)layer * c->shared_stride, shared_blob_host, c->shared_stride,
-                               cudaMemcpyHostToDevice));
+        CUDA_TRY(c, cudaMemcpy(c->shared_pool + (size_t)layer * c->shared_stride, shared_blob_host,
+                               c->lsstride[layer], cudaMemcpyHostToDevice));
         CUDA_TRY(c, cudaMemcpy(c->shared_gate + (size_t)layer * H, shared_gate_host, sizeof(uint16_t) * H,
                                cudaMemcpyHostToDevice));
     }
@@ -981,7 +1024,7 @@ extern "C" int moe_forward_decode_stack(moe_ctx* c, int32_t layer0, int32_t n, c
                    : MOE_ETIMEOUT;
     // the persistent kernel wins for a few tokens; from 4 tokens on, the batched
     // per-layer kernels (each expert's rows read once for all of its tokens) are faster
-    if (c->resident && B <= moe::kStackPreferMaxB && moe::stack_supported(c->sh, c->stack, B)) {
+    if (c->resident && !c->mixed && B <= moe::kStackPreferMaxB && moe::stack_supported(c->sh, c->stack, B)) {
         moe::StackArgs a{};
         a.layer0 = layer0;
         a.n_layers = n;
@@ -1056,8 +1099,8 @@ extern "C" int moe_route_noalloc(moe_ctx* c, int32_t layer, const float* x, int3
     const uint16_t* wr = c->router_w + (size_t)layer * E * H;
     const float* bias = c->router_bias + (size_t)layer * E;
     const uint16_t* wsg = c->cfg.shared_inter > 0 ? c->shared_gate + (size_t)layer * H : nullptr;
-    CUDA_TRY(c, moe::launch_router(c->sh, wr, bias, x, B, lg, st));
-    CUDA_TRY(c, moe::launch_route_dispatch(c->sh, 1 | 4, lg, x, wsg, B, ix, wt, sg, topk_idx, topk_w, nullptr,
+    CUDA_TRY(c, moe::launch_router(c->lsh[layer], wr, bias, x, B, lg, st));
+    CUDA_TRY(c, moe::launch_route_dispatch(c->lsh[layer], 1 | 4, lg, x, wsg, B, ix, wt, sg, topk_idx, topk_w, nullptr,
                                            nullptr, c->disp, c->xd, nullptr, st));
     c->launches += 2;
     return MOE_OK;
@@ -1102,7 +1145,7 @@ extern "C" int moe_forward_prefill(moe_ctx* c, int32_t layer, const float* x, in
         c->prof_calls++;
     }
     int n = 0;
-    cudaError_t e = moe::launch_prefill(c->sh, c->pre, a, static_cast<cudaStream_t>(stream), &n, ev);
+    cudaError_t e = moe::launch_prefill(c->lsh[layer], c->pre, a, static_cast<cudaStream_t>(stream), &n, ev);
     c->launches += n;
     if (e != cudaSuccess) return fail(c, MOE_ECUDA, "prefill launch failed: %s", cudaGetErrorString(e));
     c->stats[layer].calls++;

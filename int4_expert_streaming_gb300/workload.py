@@ -62,12 +62,13 @@ def create_loaded(w: "synth.Workload", bits: int | None = None, max_batch: int =
     bits = bits or w.bits
     cfg = config_for(w, bits, max_batch, max_tokens, pool_slots, **kw)
     from_file = cfg.store_path is not None
+    lbits = kw.get("layer_bits") or [bits] * cfg.n_layers  # layer_bits=[...]: a mixed store
     ctx = moe_create(cfg)
-    stride = moe_blob_stride(w.hidden, w.inter, bits)
-    buf = None if from_file else np.empty(w.n_experts * stride, np.uint8)
+    strides = [moe_blob_stride(w.hidden, w.inter, b) for b in lbits]
+    buf = None if from_file else np.empty(w.n_experts * max(strides), np.uint8)
     for layer in (range(cfg.n_layers) if layers is None else layers):
-        blobs, shared, wr, wsg, beta = layer_blobs(w, layer, bits, threads, out=buf, routed=not from_file)
-        moe_load_experts(ctx, layer, blobs, stride, shared, wr, wsg if shared is not None else None, beta)
+        blobs, shared, wr, wsg, beta = layer_blobs(w, layer, lbits[layer], threads, out=buf, routed=not from_file)
+        moe_load_experts(ctx, layer, blobs, strides[layer], shared, wr, wsg if shared is not None else None, beta)
     return ctx
 
 

@@ -126,6 +126,20 @@ def test_create_rejects_bad_config_before_any_gpu_work(lib, field, value):
     assert moe.moe_last_error(None)
 
 
+@pytest.mark.parametrize("kw", [dict(layer_bits=[4, 3]), dict(layer_bits=[8, 4], inter=1024),
+                                dict(layer_bits=[4, 8], pool_slots=4, store_path="/nonexistent/c.bin")])
+def test_create_rejects_bad_layer_bits_before_any_gpu_work(lib, kw):
+    """Widths other than 4 or 8, a row too long for a layer's width, and a
+    mixed stack with an expert container (which holds one width)."""
+    args = dict(n_layers=2, hidden=256, n_experts=16, top_k=2, inter=128, shared_inter=128)
+    args.update(kw)
+    cfg = moe.make_config(**args)
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_create(cfg)
+    assert e.value.code == moe.MOE_EINVAL
+    assert "layer_bits" in moe.moe_last_error(None) or "width" in moe.moe_last_error(None)
+
+
 def test_binding_rejects_host_tensors_for_device_args(lib):
     import torch
     with pytest.raises(ValueError):
