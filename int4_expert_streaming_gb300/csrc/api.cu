@@ -390,7 +390,10 @@ int decode_layer(moe_ctx* c, int layer, const float* x, int B, float* y, int32_t
 }
 
 // Streaming, enqueue helpers.  Routing of layer l: router, top-k and the
-// publication of the routing to the host.
+// publication of the routing to the host (a separate publish kernel above 8
+// tokens): this many kernels.
+int route_launches(int B) { return B > 8 ? 3 : 2; }
+
 int enq_route(moe_ctx* c, int l, const float* xin, int B, int32_t* uidx, float* uw, cudaStream_t st) {
     const moe::Shapes& s = c->lsh[l];
     const int H = c->cfg.hidden, k = c->cfg.top_k, E = c->cfg.n_experts;
@@ -520,7 +523,7 @@ int stream_layers(moe_ctx* c, int layer0, int n, const float* x, int B, float* y
     if (plain && stream_stack_ok(c, B)) {
         // route the first layer, serve it, then one persistent launch that the
         // host relaunches only from layers that miss
-        c->launches += 3;
+        c->launches += route_launches(B);
         int rc = enq_route(c, layer0, x, B, nullptr, nullptr, st);
         if (!rc) rc = serve_layer(c, layer0, B, epoch, st, nullptr);
         if (!rc) rc = enq_stack_from(c, layer0, layer0 + n, true, x, B, eps, y, st);
@@ -545,12 +548,12 @@ int stream_layers(moe_ctx* c, int layer0, int n, const float* x, int B, float* y
     if (whole && !c->graphs_off) {
         CUDA_TRY(c, cudaMemcpyAsync(c->xring, x, tok * sizeof(float), cudaMemcpyDeviceToDevice, st));
         CUDA_TRY(c, cudaGraphLaunch(c->graphs[0], st));
-        c->launches += 3;
+        c->launches += route_launches(B);
         for (int l = 0; l < n; ++l) {
             int rc = serve_layer(c, l, B, epoch, st, nullptr);
             if (rc) return rc;
             CUDA_TRY(c, cudaGraphLaunch(c->graphs[1 + l], st));
-            c->launches += l == L - 1 ? 4 : 8;
+            c->launches += 4 + (l == L - 1 ? 0 : 1 + route_launches(B));  // post, renorm, next routing
         }
         CUDA_TRY(c, cudaMemcpyAsync(y, c->yout, tok * sizeof(float), cudaMemcpyDeviceToDevice, st));
         return MOE_OK;
@@ -558,7 +561,7 @@ int stream_layers(moe_ctx* c, int layer0, int n, const float* x, int B, float* y
     const float* xin = x;
     auto route = [&](int i) -> int {
         if (x_trace) CUDA_TRY(c, cudaMemcpyAsync(x_trace + i * tok, xin, tok * sizeof(float), cudaMemcpyDeviceToDevice, st));
-        c->launches += 3;
+        c->launches += route_launches(B);
         return enq_route(c, layer0 + i, xin, B, idx_trace ? idx_trace + (size_t)i * B * k : uidx, idx_trace ? nullptr : uw,
                          st);
     };
