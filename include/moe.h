@@ -120,7 +120,8 @@ typedef struct {
     uint64_t misses;    /* lookups that needed a host->HBM copy */
     uint64_t evictions; /* misses that displaced a resident expert */
     uint64_t h2d_bytes; /* bytes copied for misses */
-    double h2d_ms;      /* device time of those copies (CUDA events) */
+    double h2d_ms;      /* device time of those copies (CUDA events; with an expert container it
+                           also spans the positioned reads between the copies) */
     int32_t resident;   /* experts currently resident */
     int32_t calls;      /* forward calls that routed through this layer */
 } moe_pool_stats_t;
