@@ -94,7 +94,7 @@ typedef struct {
     int32_t top_k;        /* k, 1..min(E, 16) */
     int32_t inter;        /* I, expert intermediate size, multiple of 64 */
     int32_t shared_inter; /* shared expert intermediate, multiple of 64 (0 = no shared expert) */
-    int32_t bits;         /* 4 or 8 */
+    int32_t bits;         /* 4 or 8 (with layer_bits: the widths come from there, `bits` is not used) */
     int32_t group_size;   /* 64 only */
     int32_t pool_slots;   /* slots per layer; == n_experts => all resident, no host sync */
     int32_t norm_topk;    /* 1 = renormalise the k weights (softmax over chosen), 0 = full softmax */
@@ -151,6 +151,10 @@ int moe_pack_expert(int32_t hidden, int32_t inter, int32_t bits, const uint8_t* 
 /* ------------------------------------------------------------------ */
 
 /*
+ * [Swiftlet article (linlog.top), section 1 "Dense core resident, experts read
+ * on demand": router, shared expert and the other dense weights stay
+ * resident while routed experts are fetched when chosen; section 3 "Expert
+ * cache pool and LFU+LRU eviction": a bounded pool of experts in memory.]
  * Validate cfg, allocate the HBM slot pool (n_layers x pool_slots x stride,
  * 64-bit offsets), the device directory, scratch and, when streaming, the
  * pinned host store (n_layers x n_experts x stride) and the side stream.
@@ -164,6 +168,10 @@ int moe_create(const moe_config* cfg, moe_ctx** out);
 void moe_destroy(moe_ctx* ctx);
 
 /*
+ * [Swiftlet article, section 2 "Fixed-stride pread reads": every routed
+ * expert is one fixed-stride blob, fetched by one read; README translation
+ * (news.paixiangai.cn), "How it works": router and shared expert are part of
+ * the resident dense weights.]
  * Load one layer (call once per layer before its first forward).  Copies:
  *   blobs_host      [n_experts x stride] routed expert blobs (stride as returned
  *                   by moe_blob_stride for (hidden, inter, the layer's bits))
@@ -200,6 +208,10 @@ int moe_set_router_bias_all(moe_ctx* ctx, const float* router_bias_host, void* s
 /* ------------------------------------------------------------------ */
 
 /*
+ * [README translation, "How it works": each layer routes each token to 10 of
+ * 512 experts (80B) or 8 of 256 (35B); Swiftlet article, "Why MoE
+ * architectures can be streamed": the router picks the routed experts, one
+ * shared expert always runs.]
  * Decode: one layer for B tokens (1 <= B <= max_batch).
  *   x_dev   fp32 [B x hidden] in, y_dev fp32 [B x hidden] out (may not alias x).
  *   topk_idx_dev int32 [B x top_k] / topk_w_dev fp32 [B x top_k]: the chosen
@@ -213,6 +225,8 @@ int moe_forward_decode(moe_ctx* ctx, int32_t layer, const float* x_dev, int32_t 
                        int32_t* topk_idx_dev, float* topk_w_dev, void* stream);
 
 /*
+ * [Swiftlet article, "Capability boundaries": the decode loop is limited by
+ * dispatch, not by I/O; one launch here runs every layer of the call.]
  * Decode through consecutive layers layer0 .. layer0+n_layers-1 for B tokens:
  *   y_l = MoE_l(x_l);  x_{l+1} = y_l / sqrt(mean(y_l^2) + renorm_eps)
  * (the renormalisation stands in for the attention/norm layers that sit
@@ -234,12 +248,17 @@ int moe_forward_decode_stack(moe_ctx* ctx, int32_t layer0, int32_t n_layers, con
                              float* y_trace_dev, void* stream);
 
 /*
+ * [README translation, "Correctness": incremental decode is verified against
+ * full-sequence processing; "Four ways to use it": a conversation cache with
+ * incremental prefill.  The pages give no prefill kernel design.]
  * Prefill: one layer for T tokens (1 <= T <= max_tokens), all experts of the
  * layer resident.  Tokens are sorted per expert and the experts run as a
  * grouped GEMM on the tensor cores: weights dequantised to bf16
- * (bf16(fp32 fma(scale, q, bias))), activations rounded to bf16, fp32
- * accumulation, SwiGLU output rounded to bf16 before the down projection.
- * Routing is computed exactly as in decode (fp32 x).
+ * (bf16(fp32 fma(scale, q, bias))), token activations rounded to bf16 for the
+ * gate/up projections, fp32 accumulation.  The SwiGLU output h is NOT rounded
+ * to one bf16: it enters the down projection as the bf16 pair hi = bf16(h),
+ * lo = bf16(h - hi) (h to about 2^-17 relative), both multiplied by the bf16
+ * down weights.  Routing is computed exactly as in decode (fp32 x).
  *   x_dev fp32 [T x hidden], y_dev fp32 [T x hidden],
  *   topk_idx_dev int32 [T x top_k] / topk_w_dev fp32 [T x top_k] or NULL.
  */
@@ -259,8 +278,11 @@ int moe_forward_prefill(moe_ctx* ctx, int32_t layer, const float* x_dev, int32_t
  * Nothing in the array has to start at zero: every element the kernels read
  * is written earlier in the same call.  The first call on a device looks up
  * the array's address (cudaGetSymbolAddress) and should therefore come before
- * any stream capture.  The array is shared by all contexts of a device: calls
- * that may overlap in time (other streams, other host threads) race on it.
+ * any stream capture.  The looked-up address is kept for the life of the
+ * process and assumes the device's primary context stays alive: after a
+ * cudaDeviceReset, or under a non-primary context, it is stale.  The array is
+ * shared by all contexts of a device: calls that may overlap in time (other
+ * streams, other host threads) race on it.
  */
 int moe_route_noalloc(moe_ctx* ctx, int32_t layer, const float* x_dev, int32_t B, int32_t* topk_idx_dev,
                       float* topk_w_dev, void* stream);
@@ -269,7 +291,9 @@ int moe_route_noalloc(moe_ctx* ctx, int32_t layer, const float* x_dev, int32_t B
 /* pool introspection                                                   */
 /* ------------------------------------------------------------------ */
 
-/* Counters of one layer, or the sum over layers (layer = -1).  Synchronises. */
+/* [Swiftlet article, section 3 "Expert cache pool and LFU+LRU eviction":
+ * the pages report the pool's hit rate (43-70 %).]
+ * Counters of one layer, or the sum over layers (layer = -1).  Synchronises. */
 int moe_pool_stats(moe_ctx* ctx, int32_t layer, moe_pool_stats_t* out);
 
 /*
@@ -287,6 +311,9 @@ int moe_pool_stats(moe_ctx* ctx, int32_t layer, moe_pool_stats_t* out);
 int moe_pool_reset(moe_ctx* ctx, int32_t slots, int32_t policy, int32_t aging_period, void* stream);
 
 /*
+ * [README translation, "Correctness": streaming placement never changes the
+ * model's semantics, an expert answers the same from the cache or from disk;
+ * the trace lets a checker replay every pool decision.]
  * Streaming contexts: copy the pool event trace, oldest first, as rows of six
  * int32 (call number of that layer, layer, expert, kind 0 = HIT / 1 = MISS,
  * slot, evicted expert or -1), at most `cap` rows into buf_host; *n_out = rows

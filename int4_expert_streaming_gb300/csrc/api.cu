@@ -197,11 +197,12 @@ int check_config(const moe_config* g) {
     if (g->top_k < 1 || g->top_k > 16 || g->top_k > g->n_experts)
         return fail(nullptr, MOE_EINVAL, "top_k must be in 1..min(16, n_experts)");
     if (g->inter < 64 || g->inter % 64) return fail(nullptr, MOE_EINVAL, "inter must be a positive multiple of 64");
-    if (g->inter * g->bits > 4096 || g->shared_inter * g->bits > 4096)
-        return fail(nullptr, MOE_EINVAL, "inter * bits must be <= 4096 (inter <= 1024 for int4, <= 512 for int8)");
     if (g->shared_inter < 0 || g->shared_inter % 64)
         return fail(nullptr, MOE_EINVAL, "shared_inter must be a multiple of 64");
     if (g->bits != 4 && g->bits != 8) return fail(nullptr, MOE_EINVAL, "bits must be 4 or 8");
+    // with layer_bits every layer's own width bounds its rows; `bits` alone otherwise
+    if (!g->layer_bits && (g->inter * g->bits > 4096 || g->shared_inter * g->bits > 4096))
+        return fail(nullptr, MOE_EINVAL, "inter * bits must be <= 4096 (inter <= 1024 for int4, <= 512 for int8)");
     if (g->layer_bits) {
         bool mixed = false;
         for (int l = 0; l < g->n_layers; ++l) {
