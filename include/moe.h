@@ -77,10 +77,15 @@ extern "C" {
 #define MOE_EVICT_LFU_PERSIST 2 /* min (all-time request count of the expert, last use, slot) */
 #define MOE_EVICT_LFU_AGED 3    /* MOE_EVICT_LFU_RECENCY, counts halved every aging_period calls */
 
-/* fault_flags: host-side fault injection for tests (0 in production). */
+/* fault_flags: fault injection for tests (0 in production); no flag makes the GPU fault. */
 #define MOE_FAULT_PINNED_ALLOC 0x1u /* pretend the pinned store allocation failed */
 #define MOE_FAULT_MISS_COPY 0x2u    /* fail the fault_arg-th miss copy (0-based), without issuing it */
 #define MOE_FAULT_WAIT_TIMEOUT 0x4u /* treat the next host wait as timed out */
+#define MOE_FAULT_DEVICE_WAIT 0x8u  /* the next multi-layer persistent decode-stack launch of an all-resident
+                                       context: one CTA withholds its outputs of the launch's first layer and
+                                       every device-side wait is bounded by 1 ms, so the other CTAs' waits run
+                                       out; the kernel ends normally with its status word set, and the next
+                                       call reports MOE_ETIMEOUT and poisons the context */
 
 /* store_flags */
 #define MOE_STORE_DIRECT 0x1u /* read blobs with O_DIRECT (buffered where the file system has none) */

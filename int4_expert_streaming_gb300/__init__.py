@@ -22,7 +22,7 @@ from ._build import LIB as _LIB_PATH, build  # noqa: F401
 MOE_OK, MOE_EINVAL, MOE_ENOMEM, MOE_ECUDA, MOE_EPOOL, MOE_ETIMEOUT, MOE_ESTATE, MOE_EIO = 0, -1, -2, -3, -4, -5, -6, -7
 MOE_STORE_DIRECT = 0x1
 MOE_EVICT_LFU_RECENCY, MOE_EVICT_LRU, MOE_EVICT_LFU_PERSIST, MOE_EVICT_LFU_AGED = 0, 1, 2, 3
-MOE_FAULT_PINNED_ALLOC, MOE_FAULT_MISS_COPY, MOE_FAULT_WAIT_TIMEOUT = 0x1, 0x2, 0x4
+MOE_FAULT_PINNED_ALLOC, MOE_FAULT_MISS_COPY, MOE_FAULT_WAIT_TIMEOUT, MOE_FAULT_DEVICE_WAIT = 0x1, 0x2, 0x4, 0x8
 _ERRNAMES = {MOE_EINVAL: "MOE_EINVAL", MOE_ENOMEM: "MOE_ENOMEM", MOE_ECUDA: "MOE_ECUDA", MOE_EPOOL: "MOE_EPOOL",
              MOE_ETIMEOUT: "MOE_ETIMEOUT", MOE_ESTATE: "MOE_ESTATE", MOE_EIO: "MOE_EIO"}
 

@@ -139,6 +139,7 @@ struct moe_ctx {
     cudaEvent_t ev_copy0 = nullptr, ev_copy1 = nullptr;
     int64_t miss_copies = 0;
     bool fault_timeout_armed = false;
+    bool fault_device_armed = false;  // MOE_FAULT_DEVICE_WAIT, not yet spent
     uint64_t launches = 0;
 };
 
@@ -692,6 +693,7 @@ extern "C" int moe_create(const moe_config* cfg, moe_ctx** out) {
     const moe_config& g = c->cfg;
     c->resident = g.pool_slots == g.n_experts;
     c->fault_timeout_armed = (g.fault_flags & MOE_FAULT_WAIT_TIMEOUT) != 0;
+    c->fault_device_armed = (g.fault_flags & MOE_FAULT_DEVICE_WAIT) != 0;
     const int E = g.n_experts, H = g.hidden, Bm = g.max_batch, k = g.top_k;
     moe::Shapes& s = c->sh;
     s.hidden = H, s.n_experts = E, s.top_k = k, s.inter = g.inter, s.shared_inter = g.shared_inter;
@@ -1045,6 +1047,8 @@ extern "C" int moe_forward_decode_stack(moe_ctx* c, int32_t layer0, int32_t n, c
         a.dir = c->dir;
         a.shared_pool = c->cfg.shared_inter > 0 ? c->shared_pool : nullptr;
         a.shared_stride = c->shared_stride;
+        a.fault = c->fault_device_armed && n > 1;
+        if (a.fault) c->fault_device_armed = false;
         cudaError_t e = moe::launch_stack(c->sh, c->stack, a, st);
         if (e != cudaSuccess) return fail(c, MOE_ECUDA, "decode stack launch failed: %s", cudaGetErrorString(e));
         for (int l = layer0; l < layer0 + n; ++l) c->stats[l].calls++;

@@ -205,6 +205,7 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
 __device__ __forceinline__ float router_logit(const uint16_t* w_row, const float* x, int H, float bias, int lane) {
     const uint4* w4 = reinterpret_cast<const uint4*>(w_row);
     float a = 0.0f;
+#pragma unroll 4
     for (int c = lane; c < H / 8; c += 32) {
         const uint4 v = w4[c];
         const float4 xa = *reinterpret_cast<const float4*>(x + 8 * c);
@@ -221,30 +222,48 @@ __device__ __forceinline__ float router_logit(const uint16_t* w_row, const float
     return __fadd_rn(warp_sum(a), bias);
 }
 
-// sigmoid(w_sg . x) (lane-strided fma, butterfly)
+// sigmoid(w_sg . x), the dot product in the router's fixed order
 __device__ __forceinline__ float shared_gate(const uint16_t* w_sg, const float* x, int H, int lane) {
-    float g = 0.0f;
-    for (int h = lane; h < H; h += 32) g = __fmaf_rn(__uint_as_float((uint32_t)w_sg[h] << 16), x[h], g);
-    g = warp_sum(g);
+    const float g = router_logit(w_sg, x, H, 0.0f, lane);
     return __fdividef(1.0f, __fadd_rn(1.0f, __expf(-g)));
 }
 
-// Renormalisation statistics of one token, computed by a whole block of
-// kRenormThreads threads: thread i accumulates y_j^2 (fma) for j = i,
-// i + kRenormThreads, ... in ascending j; each warp's partials are summed by a butterfly and the
-// warp sums in warp order.  Also max |y_j|.  Returns r = 1/sqrt(mean + eps)
-// and max |y| (via *maxabs) to every thread.  red: kRenormThreads/32 * 2
-// floats of shared memory.
-constexpr int kRenormThreads = 256;
+// Renormalisation statistics of one token over kRenormThreads threads:
+// thread i accumulates y_j^2 (fma) over the column pairs j = 2i + 2 m
+// kRenormThreads and j + 1, m ascending; each warp's partials are summed by a
+// butterfly and the warp sums in warp order.  Also max |y|.  The pairing
+// matches the persistent kernel's exchange reads (one 16-byte word pair per
+// thread and step), so there each thread sums the values it fetched itself.
+constexpr int kRenormThreads = 512;
 
+// this thread's partial sum of squares and max |y| of one token (thread i of kRenormThreads)
+__device__ __forceinline__ void renorm_partial(const float* y, int H, int i, float& s, float& m) {
+    s = 0.0f;
+    m = 0.0f;
+#pragma unroll 1
+    for (int j = 2 * i; j < H; j += 2 * kRenormThreads) {
+        s = __fmaf_rn(y[j], y[j], s);
+        s = __fmaf_rn(y[j + 1], y[j + 1], s);
+        m = fmaxf(m, fmaxf(fabsf(y[j]), fabsf(y[j + 1])));
+    }
+}
+
+// r = 1/sqrt(mean + eps) from the kRenormThreads/32 warp sums, added in warp order
+__device__ __forceinline__ float renorm_scale(const float* warp_sums, int H, float eps) {
+    float tot = warp_sums[0];
+#pragma unroll 1
+    for (int w = 1; w < kRenormThreads / 32; ++w) tot = __fadd_rn(tot, warp_sums[w]);
+    return rsqrtf(__fadd_rn(__fmul_rn(tot, 1.0f / (float)H), eps));
+}
+
+// The statistics above computed by a whole block of kRenormThreads threads.
+// Returns r to every thread and max |y| via *maxabs.  red: kRenormThreads/32 * 2
+// floats of shared memory.
 __device__ __forceinline__ float renorm_block(const float* y, int H, float eps, float* red, float* maxabs) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int NW = kRenormThreads / 32;
-    float s = 0.0f, m = 0.0f;
-    for (int j = tid; j < H; j += kRenormThreads) {
-        s = __fmaf_rn(y[j], y[j], s);
-        m = fmaxf(m, fabsf(y[j]));
-    }
+    float s, m;
+    renorm_partial(y, H, tid, s, m);
     s = warp_sum(s);
     m = warp_max(m);
     if (lane == 0) {
@@ -252,14 +271,12 @@ __device__ __forceinline__ float renorm_block(const float* y, int H, float eps, 
         red[NW + warp] = m;
     }
     __syncthreads();
-    float tot = red[0], mx = red[NW];
-    for (int w = 1; w < NW; ++w) {
-        tot = __fadd_rn(tot, red[w]);
-        mx = fmaxf(mx, red[NW + w]);
-    }
+    float mx = red[NW];
+    for (int w = 1; w < NW; ++w) mx = fmaxf(mx, red[NW + w]);
+    const float r = renorm_scale(red, H, eps);
     __syncthreads();
     *maxabs = mx;
-    return rsqrtf(__fadd_rn(__fmul_rn(tot, 1.0f / (float)H), eps));
+    return r;
 }
 
 // ---------------------------------------------------------------------------
@@ -281,8 +298,10 @@ __device__ __forceinline__ void topk_weights(const float* lg, int E, int k, int 
     const float m = val[0];
     float den = 0.0f;
     if (norm_topk) {
+#pragma unroll 1
         for (int i = 0; i < k; ++i) den = __fadd_rn(den, __expf(__fsub_rn(val[i], m)));
     } else {
+#pragma unroll 1
         for (int e = lane; e < E; e += 32) den = __fadd_rn(den, __expf(__fsub_rn(lg[e], m)));
         den = warp_sum(den);
     }
@@ -530,6 +549,35 @@ __device__ __forceinline__ void row_dot_x2(const uint8_t* q0, const uint32_t* sb
             p0 = chunk_term(p0, A0, xd.S[i], sb0[c / CPG]);
             p1 = chunk_term(p1, A1, xd.S[i], sb1[c / CPG]);
         }
+    }
+    warp_sum2(p0, p1);
+    r0 = pow2_scale(p0, -e);
+    r1 = pow2_scale(p1, -e);
+}
+
+// row_dot_x2 with the token's digit words read from shared memory chunk by
+// chunk (chunk c's words at xdw[c * DW], its integer sum at xS[c]) in a rolled
+// loop: the same chunks in the same order, the same butterfly, so each result
+// equals row_dot_x2's bit for bit, with a fraction of the code.
+template <int BITS>
+__device__ __forceinline__ void row_dot_x2_sm(const uint8_t* q0, const uint32_t* sb0, const uint8_t* q1,
+                                              const uint32_t* sb1, const uint32_t* xdw, const int32_t* xS, int e,
+                                              int nchunk, int lane, float& r0, float& r1) {
+    constexpr int DW = Codes<BITS>::kDigitWords, CPG = 64 / Codes<BITS>::kCols;
+    float p0 = 0.0f, p1 = 0.0f;
+#pragma unroll 1
+    for (int c = lane; c < nchunk; c += 32) {
+        uint32_t dw[DW];
+#pragma unroll
+        for (int j = 0; j < DW; j += 4) {
+            const uint4 v = *reinterpret_cast<const uint4*>(xdw + (size_t)c * DW + j);
+            dw[j] = v.x, dw[j + 1] = v.y, dw[j + 2] = v.z, dw[j + 3] = v.w;
+        }
+        const int S = xS[c];
+        const float A0 = chunk_dot(reinterpret_cast<const uint4*>(q0)[c], dw, Codes<BITS>{});
+        const float A1 = chunk_dot(reinterpret_cast<const uint4*>(q1)[c], dw, Codes<BITS>{});
+        p0 = chunk_term(p0, A0, S, sb0[c / CPG]);
+        p1 = chunk_term(p1, A1, S, sb1[c / CPG]);
     }
     warp_sum2(p0, p1);
     r0 = pow2_scale(p0, -e);

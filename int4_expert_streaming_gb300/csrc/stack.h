@@ -47,6 +47,9 @@ struct StackArgs {
     float* rout_w;
     float* rout_sig;
     const HostGate* pub;
+    // tests: one CTA withholds its outputs of the launch's first layer and every
+    // device-side wait is bounded by 1 ms, so the others' waits run out
+    int fault;
 };
 
 // largest batch the decode stack sends to the persistent kernel (measured crossover)

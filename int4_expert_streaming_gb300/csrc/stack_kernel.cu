@@ -1,16 +1,21 @@
 // stack_kernel.cu -- the persistent decode-stack kernel for sm_103a.
 //
 // One cooperative launch runs B tokens (B <= 8) through every MoE layer of a
-// call, one CTA per SM.  Per layer and CTA:
+// call, one CTA of 16 warps per SM.  Per layer and CTA:
 //   A  x = renorm(y of the previous layer) (or the input) and its block-
-//      fixed-point digits; router logits of this CTA's experts and the shared
-//      expert's gate/up rows of this CTA, both from shared memory prefetched
-//      during the previous layer.
-//   B  top-k + routing weights + dispatch lists (computed redundantly, the
-//      same bits in every CTA); this CTA's share of the routed gate/up rows
-//      and of every active expert's down rows are fetched with cp.async.bulk
-//      into shared-memory stages (mbarrier completion); the next layer's
-//      router/shared rows are prefetched; gate/up + SwiGLU runs stage by stage.
+//      fixed-point digits; the router logits of this CTA's experts and the
+//      shared expert's gate/up rows of this CTA, both from shared memory
+//      prefetched during the previous layer; then the next layer's router and
+//      shared rows are prefetched while HBM would otherwise idle.
+//   B  top-k + routing weights + dispatch lists, computed redundantly (the
+//      same bits in every CTA).  Top-k: each warp keeps the k best logits of
+//      its 32-expert slice; every key below the largest of the warps' k-th
+//      keys is out; the survivors are ranked in parallel.  Then every warp
+//      fetches its own share of the routed gate/up rows with cp.async.bulk
+//      into its own ring of shared-memory slots (one mbarrier per slot, so a
+//      warp starts as soon as its rows land and nothing waits for the whole
+//      CTA), and the down rows of every active expert for this CTA's output
+//      rows are fetched behind them.
 //   C  this CTA's output rows: every active expert's down rows (already in
 //      shared memory) times h, weighted and summed in ascending expert order.
 // There is no grid barrier.  Values that cross CTAs (logits, h, y) travel as
@@ -20,6 +25,11 @@
 // and a load).  Each exchange buffer is double-buffered by layer parity; a
 // CTA can be at most one layer ahead of any other, because every CTA produces
 // y rows and gate/up rows that all others wait for (grid <= min(H, k*I)).
+//
+// Code size is a first-order cost here: each layer's code runs once per layer
+// and is fetched again from L2 when it does not fit the instruction caches,
+// so every outer loop stays rolled and each arithmetic helper has one call
+// site per phase.
 //
 // This removes the per-layer launch chain that the Swiftlet pages identify
 // as the limit of their decode loop ("dispatch-bound, not IO-bound": article
@@ -38,7 +48,7 @@
 // it is on the critical path only for layers that miss.
 //
 // Every wait is bounded (%globaltimer): a poll or an mbarrier wait that does
-// not complete within kWaitNs sets the status word; every CTA then stops at
+// not complete within wait_ns sets the status word; every CTA then stops at
 // its next wait, drains its outstanding copies (again bounded) and exits.  The
 // last CTA to leave publishes the status to mapped host memory and advances
 // the epoch for the next launch.
@@ -50,12 +60,18 @@
 namespace moe {
 namespace {
 
-constexpr int kST = 256, kSW = kST / 32;
-constexpr int kNSG = 4, kNSD = 2;  // gate/up stages, down stages
+constexpr int kST = 512, kSW = kST / 32;
 constexpr int kMaxB = 8;
-constexpr int kNB = kNSG + kNSD + 2;  // mbarriers: G stages, D stages, prefetch[2]
-constexpr unsigned long long kWaitNs = 1000000000ull;
+constexpr int kRing = 4;                              // gate/up slots per warp (at most)
+constexpr int kNSD = 2;                               // down stages
+constexpr int kMbD = kSW * kRing;                     // first down-stage mbarrier
+constexpr int kMbP = kMbD + kNSD;                     // the prefetch mbarriers [2], by layer parity
+constexpr int kNB = kMbP + 2;
+constexpr unsigned long long kWaitNs = 1000000000ull;  // 1 s
+constexpr unsigned long long kFaultWaitNs = 1000000ull;  // 1 ms (the test-only fault mode)
 constexpr int kStatusTimeout = 2;
+
+static_assert(kST == kRenormThreads, "the renormalisation order is defined for kRenormThreads threads");
 
 struct Params {
     int H, E, k, I, Is, norm_topk, B, bits;
@@ -79,6 +95,8 @@ struct Params {
     unsigned* sync;             // [1] CTAs finished, [2] epoch base
     int* status;
     int* status_host;
+    unsigned long long wait_ns;  // bound of every device-side wait
+    int fault_cta;               // tests: this CTA withholds its y words of the launch's first layer (-1: none)
     // streaming launch (rin_idx non-null): the first layer's routing is given
     // (idx, w [B*k], sigma [B]); every later layer's routing is published to
     // mapped host memory (pub_idx row l, then pub_ready[l] = *pub_epoch).  A
@@ -100,11 +118,11 @@ struct Params {
     const volatile uint32_t* pub_epoch;
     // shared-memory plan
     int rE, rS, jn;
-    int p_bytes;
-    int g_cap, g_unit;
+    int p_bytes, off_sg;  // prefetch buffer size; offset of w_sg in it
+    int g_unit, ring, g_bytes;
     int d_cap, d_unit, d_rows_bytes;
     int amax, pmax;
-    int off_disp, off_part, off_xs, off_xd, off_P, off_G, off_D;
+    int off_disp, off_part, off_xs, off_xd, off_P, off_dirs, off_G, off_D;
     int smem_bytes;
 };
 
@@ -142,16 +160,16 @@ __device__ __forceinline__ unsigned long long gtime() {
 }
 __device__ __forceinline__ int ld_volatile(const int* p) { return *(volatile const int*)p; }
 
-// Abort check for spin loops: the timer and the (shared, global) status word
-// are looked at only every 256 spins, so thousands of waiting threads do not
+// Abort check for spin loops: the timer and the (global) status word are
+// looked at only every 256 spins, so thousands of waiting threads do not
 // hammer one L2 line.
-__device__ __forceinline__ bool spin_abort(int* status, unsigned& spins, unsigned long long t0) {
+__device__ __forceinline__ bool spin_abort(const Params& p, unsigned& spins, unsigned long long t0) {
     if ((++spins & 255u) != 0u) return false;
-    if (gtime() - t0 > kWaitNs) {
-        atomicCAS(status, 0, kStatusTimeout);
+    if (gtime() - t0 > p.wait_ns) {
+        atomicCAS(p.status, 0, kStatusTimeout);
         return true;
     }
-    return ld_volatile(status) != 0;
+    return ld_volatile(p.status) != 0;
 }
 
 // {value, epoch} words
@@ -159,62 +177,71 @@ __device__ __forceinline__ void ll_store(unsigned long long* p, float v, uint32_
     const unsigned long long w = ((unsigned long long)ep << 32) | __float_as_uint(v);
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
 }
+__device__ __forceinline__ unsigned long long ll_load(const unsigned long long* p) {
+    unsigned long long a;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(a) : "l"(p) : "memory");
+    return a;
+}
 __device__ __forceinline__ void ll_load2(const unsigned long long* p, unsigned long long& a, unsigned long long& b) {
     asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
 }
 
-// Poll the first `cols` words of rows row0 .. row0+nrows-1 of an exchange
-// buffer (row stride `stride` words) until each carries epoch ep; the values
-// go to dst[(row - row0) * stride + col].  cols and stride are even.  All
-// threads take part; each polls batches of 8 word pairs, re-issuing the whole
-// batch until every pair carries ep (a rolled loop: this runs once per
-// exchange and its code size matters more than its arithmetic).  Returns false
-// on timeout or abort.
-__device__ bool ll_read_rows(const unsigned long long* base, int row0, int nrows, int stride, int cols, uint32_t ep,
-                             float* dst, int tid, int nthreads, int* status) {
-    const int n = nrows * cols;
-    const unsigned long long* b0 = base + (size_t)row0 * stride;
-    for (int b = 2 * tid; b < n; b += 16 * nthreads) {
-        int off[8];
+// Polls the word pairs of rows row0 .. row0+nrows-1 of an exchange buffer
+// (row stride `stride` words, the first `cols` words of each row, cols even)
+// until every word carries epoch ep; the value of (row, col) goes to
+// dst[(row - row0) * dstride + col].  Thread i takes pairs i, i + kST, ... in
+// batches of up to four, re-issuing a batch until all of it is current.
+// Returns false (in the calling thread) on timeout or abort.
+__device__ __forceinline__ bool poll_rows(const unsigned long long* base, int row0, int nrows, int stride, int cols,
+                                       int dstride, uint32_t ep, float* dst, const Params& p) {
+    const int half = cols >> 1, n = nrows * half;
+#pragma unroll 1
+    for (int q0 = threadIdx.x; q0 < n; q0 += 4 * kST) {
+        int so[4], d0[4];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int i = b + 2 * nthreads * q;
-            const int r = i / cols;
-            off[q] = i < n ? r * stride + (i - r * cols) : -1;
+        for (int m = 0; m < 4; ++m) {
+            const int q = q0 + m * kST;
+            const int r = q / half, cc = 2 * (q - r * half);
+            so[m] = q < n ? (row0 + r) * stride + cc : -1;
+            d0[m] = r * dstride + cc;
         }
-        unsigned long long a[8], c[8];
+        unsigned long long a[4], b[4];
         unsigned spins = 0;
         unsigned long long t0 = 0;
+#pragma unroll 1
         for (;;) {
             bool all = true;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                a[q] = c[q] = (unsigned long long)ep << 32;
-                if (off[q] >= 0) ll_load2(b0 + off[q], a[q], c[q]);
+            for (int m = 0; m < 4; ++m) {
+                a[m] = b[m] = (unsigned long long)ep << 32;
+                if (so[m] >= 0) ll_load2(base + so[m], a[m], b[m]);
+                all = all && (uint32_t)(a[m] >> 32) == ep && (uint32_t)(b[m] >> 32) == ep;
             }
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                all = all && (uint32_t)(a[q] >> 32) == ep && (uint32_t)(c[q] >> 32) == ep;
             if (all) break;
             if (!t0) t0 = gtime();
-            if (spin_abort(status, spins, t0)) return false;
-            __nanosleep(32);
+            if (spin_abort(p, spins, t0)) return false;
+            __nanosleep(64);  // back off: thousands of pollers share L2 with the weight stream
         }
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            if (off[q] >= 0) {
-                dst[off[q]] = __uint_as_float((uint32_t)a[q]);
-                dst[off[q] + 1] = __uint_as_float((uint32_t)c[q]);
+        for (int m = 0; m < 4; ++m)
+            if (so[m] >= 0) {
+                dst[d0[m]] = __uint_as_float((uint32_t)a[m]);
+                dst[d0[m] + 1] = __uint_as_float((uint32_t)b[m]);
             }
-        }
     }
     return true;
 }
 
-// n contiguous words (n even)
-__device__ __forceinline__ bool ll_read(const unsigned long long* src, int n, uint32_t ep, float* out, int tid,
-                                        int nthreads, int* status) {
-    return ll_read_rows(src, 0, 1, n, n, ep, out, tid, nthreads, status);
+// bounded wait of one warp on an mbarrier phase; false (in every lane) on abort
+__device__ __forceinline__ bool warp_wait(uint64_t* m, uint32_t parity, const Params& p) {
+    unsigned spins = 0;
+    unsigned long long t0 = 0;
+#pragma unroll 1
+    for (;;) {
+        if (__all_sync(kFullMask, mbar_test(m, parity))) return true;
+        if (!t0) t0 = gtime();
+        if (__any_sync(kFullMask, spin_abort(p, spins, t0))) return false;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -226,9 +253,9 @@ struct Disp {
     float w[kMaxB][16];
     float sig[kMaxB];
     float rs[kMaxB];
-    int xe[kMaxB];         // block-fixed-point exponent of each token's x
-    float xmax[kMaxB];     // max |x| of each token
-    float red[2 * kRenormThreads / 32];
+    int xe[kMaxB];      // block-fixed-point exponent of each token's x
+    float xmax[kMaxB];  // max |x| of each token
+    float red[kMaxB][2][kSW];
     int n_act, n_routed, n_pairs, pad;
 };
 
@@ -264,41 +291,72 @@ __host__ __device__ inline int disp_bytes(int amax, int pmax) {
     return r16i((int)sizeof(Disp)) + r16i(amax * 8) + r16i(amax * 4) + r16i((amax + 1) * 4) + 3 * r16i(pmax * 4);
 }
 
+// top-k scratch inside the gate/up area (free between the previous layer's
+// down phase and this layer's copies): logits [B][E] and the warps' candidate
+// lists [B][kSW][k] (key, index)
+struct TopkTemp {
+    float* lg;
+    uint32_t* ck;
+    int32_t* ci;
+};
+
+__host__ __device__ inline int topk_temp_bytes(int B, int E, int k) {
+    return r16i(B * E * 4) + 2 * r16i(B * kSW * k * 4);
+}
+
+__device__ __forceinline__ TopkTemp topk_temp(uint8_t* base, int B, int E, int k) {
+    TopkTemp T;
+    uint8_t* q = base;
+    T.lg = reinterpret_cast<float*>(q);
+    q += r16i(B * E * 4);
+    const int n = r16i(B * kSW * k * 4);
+    T.ck = reinterpret_cast<uint32_t*>(q);
+    T.ci = reinterpret_cast<int32_t*>(q + n);
+    return T;
+}
+
 struct Waits {
     uint32_t phase;  // bit i = expected parity of mbarrier i
     uint32_t armed;  // bit i = mbarrier i has an outstanding phase
 };
 
-// bounded wait on mbarrier i; every thread calls it; false (everywhere) on abort
+// bounded wait on CTA-wide mbarrier i (down stages, prefetch); every thread
+// calls it; false (everywhere) on abort
 __device__ bool stage_wait(uint64_t* mb, int i, Waits& w, const Params& p) {
-    const uint32_t par = (w.phase >> i) & 1u;
+    const uint32_t bit = 1u << (i - kMbD);
+    const uint32_t par = (w.phase & bit) ? 1u : 0u;
     const unsigned long long t0 = gtime();
     unsigned spins = 0;
     bool ok = true;
     while (!mbar_test(mb + i, par)) {
-        if (spin_abort(p.status, spins, t0)) {
+        if (spin_abort(p, spins, t0)) {
             ok = false;
             break;
         }
     }
     if (ok) {
-        w.phase ^= 1u << i;
-        w.armed &= ~(1u << i);
+        w.phase ^= bit;
+        w.armed &= ~bit;
     }
     return __syncthreads_and(ok ? 1 : 0) != 0;
 }
 
 // ---------------------------------------------------------------------------
-// copies (each stage issued by one lane)
+// copies (each issued by one lane)
 // ---------------------------------------------------------------------------
-// prefetch buffer: [router rows rE x 2H][shared gate q rS][shared up q rS][gate sb rS][up sb rS]
-__device__ void issue_prefetch(const Params& p, int layer, uint8_t* buf, uint64_t* mb) {
+// prefetch buffer: [router rows rE x 2H][shared gate q rS][shared up q rS][gate sb rS][up sb rS][w_sg 2H];
+// and the layer's directory row into dirs[layer & 1] (the directory does not change during a launch)
+__device__ __forceinline__ void issue_prefetch(const Params& p, int layer, uint8_t* buf, const uint8_t** dirs,
+                                               uint64_t* mb) {
     const int c = blockIdx.x, G = gridDim.x;
-    const int e0 = (int)((long long)p.E * c / G), e1 = (int)((long long)p.E * (c + 1) / G);
-    const int s0 = (int)((long long)p.Is * c / G), s1 = (int)((long long)p.Is * (c + 1) / G);
+    const int e0 = p.E * c / G, e1 = p.E * (c + 1) / G;  // 32-bit: E, Is <= 4096, G <= 1024
+    const int s0 = p.Is * c / G, s1 = p.Is * (c + 1) / G;
     const uint32_t rb = (uint32_t)p.H * 2, qb = (uint32_t)p.H * p.bits / 8, sbb = (uint32_t)p.H / 16;
-    mbar_expect(mb, (e1 - e0) * rb + (s1 - s0) * 2 * (qb + sbb));
+    const bool sg = p.Is > 0;
+    mbar_expect(mb, (e1 - e0) * rb + (s1 - s0) * 2 * (qb + sbb) + (sg ? rb : 0u) + (uint32_t)p.E * 8u);
+    bulk_load(dirs + (layer & 1) * p.E, p.dir + (size_t)layer * p.E, (uint32_t)p.E * 8u, mb);
     if (e1 > e0) bulk_load(buf, p.router_w + ((size_t)layer * p.E + e0) * p.H, (e1 - e0) * rb, mb);
+    if (sg) bulk_load(buf + p.off_sg, p.shared_gate + (size_t)layer * p.H, rb, mb);
     if (s1 > s0) {
         const uint8_t* blob = p.shared_pool + (size_t)layer * p.shared_stride;
         const BlobLayout L = blob_layout(p.H, p.Is, p.bits);
@@ -311,29 +369,22 @@ __device__ void issue_prefetch(const Params& p, int layer, uint8_t* buf, uint64_
     }
 }
 
-// gate/up stage: [gate q g_cap rows][up q][gate sb][up sb]; units [ua, ub) of this layer's routed rows
-__device__ void issue_gateup(const Params& p, const Lists& D, int ua, int ub, uint8_t* stage, uint64_t* mb) {
+// one gate/up unit (row r of active routed expert a): [gate q][up q][gate sb][up sb]
+__device__ __forceinline__ void issue_unit(const Params& p, const uint8_t* blob, int r, uint8_t* slot, uint64_t* mb) {
     const uint32_t qb = (uint32_t)p.H * p.bits / 8, sbb = (uint32_t)p.H / 16;
-    mbar_expect(mb, (uint32_t)(ub - ua) * 2 * (qb + sbb));
     const BlobLayout L = blob_layout(p.H, p.I, p.bits);
-    for (int u = ua; u < ub;) {
-        const int a = u / p.I, r0 = u - a * p.I;
-        const int n = min(ub - u, p.I - r0);
-        const uint8_t* blob = D.act_blob[a];
-        const int o = u - ua;
-        bulk_load(stage + (size_t)o * qb, blob + L.gate_q + (size_t)r0 * qb, n * qb, mb);
-        bulk_load(stage + (size_t)(p.g_cap + o) * qb, blob + L.up_q + (size_t)r0 * qb, n * qb, mb);
-        uint8_t* sbase = stage + (size_t)2 * p.g_cap * qb;
-        bulk_load(sbase + (size_t)o * sbb, blob + L.gate_sb + (size_t)r0 * sbb, n * sbb, mb);
-        bulk_load(sbase + (size_t)(p.g_cap + o) * sbb, blob + L.up_sb + (size_t)r0 * sbb, n * sbb, mb);
-        u += n;
-    }
+    mbar_expect(mb, 2 * (qb + sbb));
+    bulk_load(slot, blob + L.gate_q + (size_t)r * qb, qb, mb);
+    bulk_load(slot + qb, blob + L.up_q + (size_t)r * qb, qb, mb);
+    bulk_load(slot + 2 * qb, blob + L.gate_sb + (size_t)r * sbb, sbb, mb);
+    bulk_load(slot + 2 * qb + sbb, blob + L.up_sb + (size_t)r * sbb, sbb, mb);
 }
 
 // down stage: per active expert a in [aa, ab): [jn rows x row bytes][aligned scale/bias superset]
-__device__ void issue_down(const Params& p, const Lists& D, int aa, int ab, int j0, int jn, uint8_t* stage,
-                           uint64_t* mb) {
+__device__ __forceinline__ void issue_down(const Params& p, const Lists& D, int aa, int ab, int j0, int jn,
+                                        uint8_t* stage, uint64_t* mb) {
     uint32_t total = 0;
+#pragma unroll 1
     for (int a = aa; a < ab; ++a) {
         const int cols = D.act_expert[a] < 0 ? p.Is : p.I;
         const uint32_t rb = (uint32_t)cols * p.bits / 8, sbb = (uint32_t)cols / 16;
@@ -341,6 +392,7 @@ __device__ void issue_down(const Params& p, const Lists& D, int aa, int ab, int 
         total += jn * rb + (s_hi - s_lo);
     }
     mbar_expect(mb, total);
+#pragma unroll 1
     for (int a = aa; a < ab; ++a) {
         const int cols = D.act_expert[a] < 0 ? p.Is : p.I;
         const uint32_t rb = (uint32_t)cols * p.bits / 8, sbb = (uint32_t)cols / 16;
@@ -354,17 +406,270 @@ __device__ void issue_down(const Params& p, const Lists& D, int aa, int ab, int 
 }
 
 // ---------------------------------------------------------------------------
+// top-k of every token: the warps' candidate lists, the threshold, the
+// survivors' ranks.  Order: logit descending, ties to the lower expert id,
+// the order of warp_topk in the per-layer kernels.
+// ---------------------------------------------------------------------------
+// Level 1 (warp w, token t): the k best of experts w*32*M + lane + 32 m
+// (m < M), polled straight from the exchange buffer; also writes every
+// polled logit to T.lg.  Returns false on abort.
+__device__ __forceinline__ bool topk_lists(const Params& p, const unsigned long long* lgx, uint32_t ep, const TopkTemp& T,
+                                        int M, int nlist) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, E = p.E, k = p.k;
+#pragma unroll 1
+    for (int t = 0; t < p.B; ++t) {
+        uint32_t key0 = 0u, key1 = 0u;  // scalars: a runtime-indexed array would live in local memory
+#pragma unroll 1
+        for (int m = 0; m < M; ++m) {
+            const int j = warp * 32 * M + 32 * m + lane;
+            if (j >= E) continue;
+            unsigned spins = 0;
+            unsigned long long t0 = 0, wv;
+#pragma unroll 1
+            for (;;) {
+                wv = ll_load(lgx + (size_t)t * E + j);
+                if ((uint32_t)(wv >> 32) == ep) break;
+                if (!t0) t0 = gtime();
+                if (spin_abort(p, spins, t0)) return false;
+                __nanosleep(64);
+            }
+            const float v = __uint_as_float((uint32_t)wv);
+            T.lg[t * E + j] = v;
+            if (m == 0)
+                key0 = order_key(v);
+            else
+                key1 = order_key(v);
+        }
+        if (warp >= nlist) continue;
+        uint32_t* ck = T.ck + (t * kSW + warp) * k;
+        int32_t* ci = T.ci + (t * kSW + warp) * k;
+#pragma unroll 1
+        for (int r = 0; r < k; ++r) {
+            const int bm = key1 > key0 ? 1 : 0;
+            const uint32_t best = bm ? key1 : key0;
+            const uint32_t mx = __reduce_max_sync(kFullMask, best);
+            const uint32_t win = __reduce_min_sync(
+                kFullMask, (best == mx && mx != 0u) ? (uint32_t)(warp * 32 * M + 32 * bm + lane) : 0xffffffffu);
+            if (lane == 0) {
+                ck[r] = mx;
+                ci[r] = (int)win;  // 0xffffffff (-1): the slice has fewer than k keys
+            }
+            if (win == 0xffffffffu) break;
+            const int wl = (int)(win & 31u), wm = (int)(win - (uint32_t)(warp * 32 * M)) >> 5;
+            if (lane == wl) {
+                if (wm == 0)
+                    key0 = 0u;
+                else
+                    key1 = 0u;
+            }
+        }
+    }
+    return true;
+}
+
+// Level 2 for token t = warp: a merge of the warps' lists (each sorted by
+// key descending, ties by index ascending, and holding its slice's k best, so
+// together they hold the token's k best) in k rounds of a warp maximum over
+// the list heads, ties to the lower expert id.  Lane i < nlist holds the head
+// of list i and its next entry.  Then the routing weights.
+__device__ __forceinline__ void topk_merge(const Params& p, const TopkTemp& T, Disp* ds, int nlist) {
+    const int t = threadIdx.x >> 5, lane = threadIdx.x & 31, k = p.k;
+    const uint32_t* ck = T.ck + (t * kSW + (lane < nlist ? lane : 0)) * k;
+    const int32_t* ci = T.ci + (t * kSW + (lane < nlist ? lane : 0)) * k;
+    uint32_t hk = 0u, hi = 0xffffffffu, nk = 0u, ni = 0xffffffffu;
+    if (lane < nlist) {
+        if (ci[0] >= 0) hk = ck[0], hi = (uint32_t)ci[0];
+        if (k > 1 && ci[1] >= 0 && hi != 0xffffffffu) nk = ck[1], ni = (uint32_t)ci[1];
+    }
+    int pos = 1;  // index of the entry held in (nk, ni)
+#pragma unroll 1
+    for (int r = 0; r < k; ++r) {
+        const uint32_t mx = __reduce_max_sync(kFullMask, hk);
+        const uint32_t win = __reduce_min_sync(kFullMask, hk == mx ? hi : 0xffffffffu);
+        if (lane == 0) {
+            ds->idx[t][r] = (int)win;
+            ds->val[t][r] = T.lg[t * p.E + (int)win];
+        }
+        if (hi == win) {  // this list's head was taken
+            hk = nk, hi = ni;
+            ++pos;
+            nk = 0u, ni = 0xffffffffu;
+            if (hi != 0xffffffffu && pos < k && ci[pos] >= 0) nk = ck[pos], ni = (uint32_t)ci[pos];
+        }
+    }
+    __syncwarp();
+    topk_weights(T.lg + t * p.E, p.E, k, p.norm_topk, lane, ds->val[t], ds->w[t]);
+}
+
+// Dispatch (warp 0): pairs sorted by (expert, token) by rank (key expert << 3 | token),
+// then the active experts in ascending id with their blob addresses.
+__device__ __forceinline__ void dispatch(const Params& p, const Lists& D, Disp* ds, int l,
+                                         const uint8_t* const* dir_row) {
+    const int lane = threadIdx.x & 31, k = p.k, nq = p.B * k;
+#pragma unroll 1
+    for (int m = 0; m * 32 < nq; ++m) {
+        const int q = lane + 32 * m;
+        const uint32_t kq = q < nq ? ((uint32_t)ds->idx[q / k][q % k] << 3) | (uint32_t)(q / k) : 0xffffffffu;
+        int rank = 0;
+#pragma unroll 1
+        for (int mm = 0; mm * 32 < nq; ++mm) {
+            const int qb = lane + 32 * mm;
+            const uint32_t kb = qb < nq ? ((uint32_t)ds->idx[qb / k][qb % k] << 3) | (uint32_t)(qb / k) : 0xffffffffu;
+            const int lim = min(32, nq - 32 * mm);
+#pragma unroll 1
+            for (int s2 = 0; s2 < lim; ++s2) rank += __shfl_sync(kFullMask, kb, s2) < kq ? 1 : 0;
+        }
+        if (q < nq) {
+            D.pair_act[rank] = (int)kq;  // the sorted keys, replaced by active indices below
+            D.pair_w[rank] = ds->w[q / k][q % k];
+        }
+    }
+    __syncwarp();
+    int base = 0;
+    uint32_t prev = 0xffffffffu;
+#pragma unroll 1
+    for (int m = 0; m * 32 < nq; ++m) {
+        const int pr = lane + 32 * m;
+        const uint32_t kq = pr < nq ? (uint32_t)D.pair_act[pr] : 0xffffffffu;
+        uint32_t kp = __shfl_up_sync(kFullMask, kq, 1);
+        if (lane == 0) kp = prev;
+        const bool first = pr < nq && (kp == 0xffffffffu || (kp >> 3) != (kq >> 3));
+        const unsigned bal = __ballot_sync(kFullMask, first);
+        const int a = base + __popc(bal & (0xffffffffu >> (31 - lane))) - 1;
+        prev = __shfl_sync(kFullMask, kq, 31);
+        __syncwarp();
+        if (pr < nq) {
+            const int e = (int)(kq >> 3);
+            D.pair_token[pr] = (int)(kq & 7u);
+            D.pair_act[pr] = a;
+            if (first) {
+                D.act_expert[a] = e;
+                D.act_blob[a] = dir_row[e];
+                D.act_off[a] = pr;
+            }
+        }
+        base += __popc(bal);
+    }
+    __syncwarp();
+    if (lane == 0) {
+        const int nr = base, B = p.B;
+        ds->n_routed = nr;
+        ds->n_pairs = B * k + (p.Is > 0 ? B : 0);
+        ds->n_act = nr + (p.Is > 0 ? 1 : 0);
+        if (p.Is > 0) {
+            D.act_expert[nr] = -1;
+            D.act_blob[nr] = p.shared_pool + (size_t)l * p.shared_stride;
+            D.act_off[nr] = B * k;
+            D.act_off[nr + 1] = B * k + B;
+        } else {
+            D.act_off[nr] = B * k;
+        }
+    }
+    if (p.Is > 0 && lane < p.B) {
+        D.pair_token[p.B * k + lane] = lane;
+        D.pair_w[p.B * k + lane] = ds->sig[lane];
+        D.pair_act[p.B * k + lane] = base;
+    }
+}
+
+// Block-fixed-point digits of x (already renormalised), by warps w0 .. w0+nw-1:
+// a warp covers 32 consecutive columns of one token (one int4 chunk, two int8
+// chunks); the digit words are assembled with shuffles in the layout of
+// bfp_chunk and stored whole.
+template <int BITS>
+__device__ __forceinline__ void make_digits(int B, int H, const float* xs, uint32_t* xdw, int32_t* xS, const Disp* ds,
+                                            int w0, int nw) {
+    constexpr int CC = Codes<BITS>::kCols, DW = Codes<BITS>::kDigitWords;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nc = H / CC, ng = H / 32;
+#pragma unroll 1
+    for (int g = warp - w0; g < B * ng; g += nw) {
+        const int t = g / ng, col = (g - t * ng) * 32 + lane;
+        const int V = bfp_int(xs[t * H + col], ds->xe[t]);
+        uint32_t d0, d1, d2;
+        bfp_digits(V, d0, d1, d2);
+        const uint32_t dig = d0 | (d1 << 8) | (d2 << 16);
+        if (BITS == 4) {
+            // word L = 6 cw + 2 j + odd: digit j of columns 8 cw + 2 b + odd, b = 0..3
+            const int Lw = lane < 24 ? lane : 0;
+            const int cw = Lw / 6, r = Lw - 6 * cw, j = r >> 1, odd = r & 1;
+            const uint32_t g0 = __shfl_sync(kFullMask, dig, 8 * cw + 0 + odd);
+            const uint32_t g1 = __shfl_sync(kFullMask, dig, 8 * cw + 2 + odd);
+            const uint32_t g2 = __shfl_sync(kFullMask, dig, 8 * cw + 4 + odd);
+            const uint32_t g3 = __shfl_sync(kFullMask, dig, 8 * cw + 6 + odd);
+            const uint32_t sel = (uint32_t)j | ((uint32_t)(j + 4) << 4);
+            const uint32_t word = __byte_perm(__byte_perm(g0, g1, sel), __byte_perm(g2, g3, sel), 0x5410);
+            const int ch = col / CC;
+            if (lane < 24) xdw[(size_t)(t * nc + ch) * DW + lane] = word;
+            const int S = __reduce_add_sync(kFullMask, V);
+            if (lane == 0) xS[t * nc + ch] = S;
+        } else {
+            // per half-warp chunk: word 3 cw + j = digit j of columns 4 cw + b, b = 0..3
+            const int hb = lane & 16, L = lane & 15;
+            const int Lw = L < 12 ? L : 0;
+            const int cw = Lw / 3, j = Lw - 3 * cw;
+            const uint32_t g0 = __shfl_sync(kFullMask, dig, hb + 4 * cw + 0);
+            const uint32_t g1 = __shfl_sync(kFullMask, dig, hb + 4 * cw + 1);
+            const uint32_t g2 = __shfl_sync(kFullMask, dig, hb + 4 * cw + 2);
+            const uint32_t g3 = __shfl_sync(kFullMask, dig, hb + 4 * cw + 3);
+            const uint32_t sel = (uint32_t)j | ((uint32_t)(j + 4) << 4);
+            const uint32_t word = __byte_perm(__byte_perm(g0, g1, sel), __byte_perm(g2, g3, sel), 0x5410);
+            const int ch = col / CC;
+            if (L < 12) xdw[(size_t)(t * nc + ch) * DW + L] = word;
+            const int S = lane < 16 ? __reduce_add_sync(0x0000ffffu, V) : __reduce_add_sync(0xffff0000u, V);
+            if (L == 0) xS[t * nc + ch] = S;
+        }
+    }
+}
+
+// gate and up rows (codes + scale/bias words in shared memory) against token
+// t's digits; silu(g) * u
+template <int BITS>
+__device__ __forceinline__ float swiglu_row(const uint8_t* gq, const uint8_t* uq, const uint32_t* gsb,
+                                            const uint32_t* usb, const uint32_t* xdw, const int32_t* xS, int xe, int nc) {
+    float g, u;
+    row_dot_x2_sm<BITS>(gq, gsb, uq, usb, xdw, xS, xe, nc, threadIdx.x & 31, g, u);
+    return silu_mul(g, u);
+}
+
+// One pair's SwiGLU vector for this lane's down-row chunk, polled straight
+// from the exchange into registers (words ch*CC .. ch*CC+CC-1 of the pair's
+// row); false on timeout or abort (in every lane).
+template <int BITS>
+__device__ __forceinline__ bool poll_h_chunk(const unsigned long long* row, bool act, int ch, uint32_t ep, HF<BITS>& hd,
+                                             const Params& p) {
+    constexpr int CC = Codes<BITS>::kCols;
+    unsigned spins = 0;
+    unsigned long long t0 = 0;
+    for (;;) {
+        bool ready = true;
+        if (act) {
+#pragma unroll
+            for (int i = 0; i < CC; i += 2) {
+                unsigned long long a, b;
+                ll_load2(row + ch * CC + i, a, b);
+                ready = ready && (uint32_t)(a >> 32) == ep && (uint32_t)(b >> 32) == ep;
+                hd.v[i] = __uint_as_float((uint32_t)a);
+                hd.v[i + 1] = __uint_as_float((uint32_t)b);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < CC; ++i) hd.v[i] = 0.0f;
+        }
+        if (__all_sync(kFullMask, ready)) return true;
+        if (!t0) t0 = gtime();
+        if (__any_sync(kFullMask, spin_abort(p, spins, t0))) return false;
+        __nanosleep(64);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <int BITS, int NPER>
-__global__ void __launch_bounds__(kST, 1) stack_kernel(const Params p) {
+template <int BITS>
+__global__ void __launch_bounds__(kST, 1) stack_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ uint64_t mbar[kNB];
-    uint64_t* mbG = mbar;
-    uint64_t* mbD = mbar + kNSG;
-    uint64_t* mbP = mbar + kNSG + kNSD;
 
-    static_assert(kST == kRenormThreads, "the renormalisation order is defined for kRenormThreads threads");
     constexpr int CC = Codes<BITS>::kCols, DW = Codes<BITS>::kDigitWords;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x, G = gridDim.x;
@@ -377,270 +682,158 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const Params p) {
     float* xs = reinterpret_cast<float*>(smem + p.off_xs);
     uint32_t* xdw = reinterpret_cast<uint32_t*>(smem + p.off_xd);           // [B][nc][DW]
     int32_t* xS = reinterpret_cast<int32_t*>(xdw + (size_t)B * nc * DW);  // [B][nc]
-    uint8_t* Pbuf = smem + p.off_P;
+    uint8_t* Pb = smem + p.off_P;                                           // [2][p_bytes], by layer parity
+    const uint8_t** dirs = reinterpret_cast<const uint8_t**>(smem + p.off_dirs);
     uint8_t* Gbuf = smem + p.off_G;
     uint8_t* Dbuf = smem + p.off_D;
-    const int gstage = p.g_cap * p.g_unit;
+    const TopkTemp TT = topk_temp(Gbuf, B, E, k);
     const int dstage = p.d_cap * p.d_unit;
     const size_t h_par = (size_t)p.hp * p.h_stride;
+    const int M = (E + kST - 1) / kST;              // keys per lane in the first top-k level
+    const int nlist = (E + 32 * M - 1) / (32 * M);  // warps holding keys
+    const int R = p.ring;
+    uint8_t* wslots = Gbuf + (size_t)warp * R * p.g_unit;
 
     const uint32_t ep0 = *(volatile const unsigned*)&p.sync[2];
     Waits wt{0u, 0u};
+    uint32_t wph = 0u, warm = 0u;  // this warp's slots: expected parity, outstanding
     if (tid == 0) {
         for (int i = 0; i < kNB; ++i) mbar_init(&mbar[i]);
         fence_mbar_init();
     }
     __syncthreads();
-    if (tid == 0) issue_prefetch(p, p.layer0, Pbuf + (p.layer0 & 1) * p.p_bytes, &mbP[p.layer0 & 1]);
-    wt.armed |= 1u << (kNSG + kNSD + (p.layer0 & 1));
+    if (tid == 0) issue_prefetch(p, p.layer0, Pb + (p.layer0 & 1) * p.p_bytes, dirs, &mbar[kMbP + (p.layer0 & 1)]);
+    wt.armed |= 1u << (kMbP + (p.layer0 & 1) - kMbD);
 
-    const int j0 = (int)((long long)H * c / G), jn = (int)((long long)H * (c + 1) / G) - j0;
-    const int e0 = (int)((long long)E * c / G), ne = (int)((long long)E * (c + 1) / G) - e0;
-    const int s0 = (int)((long long)p.Is * c / G), ns = (int)((long long)p.Is * (c + 1) / G) - s0;
+    // work splits in 32-bit arithmetic (every product stays below 2^31)
+    const int j0 = H * c / G, jn = H * (c + 1) / G - j0;
+    const int e0 = E * c / G, ne = E * (c + 1) / G - e0;
+    const int s0 = p.Is * c / G, ns = p.Is * (c + 1) / G - s0;
     bool ok = true;
     const int lend = p.layer0 + p.n_layers;
 
+#pragma unroll 1
     for (int l = p.layer0; l < lend && ok; ++l) {
         const int li = l - p.layer0, par = l & 1;
         const uint32_t ep = ep0 + (uint32_t)li;
-        const bool given = l == p.layer0 && p.rin_idx != nullptr;  // routing from rin_*
+        const bool given = l == p.layer0 && p.rin_idx != nullptr;    // routing from rin_*
         const bool streamed = l > p.layer0 && p.rin_idx != nullptr;  // routing published, residency checked
-        // the next layer's router and shared rows do not depend on this layer:
-        // fetch them now (their buffer was last read in the previous layer)
+        uint8_t* Pbuf = Pb + par * p.p_bytes;
+        unsigned long long* hll = p.h_ll + par * h_par;
+        // the next layer's router rows, shared rows and directory row do not
+        // depend on this layer: fetch them now (their buffer was last read in
+        // the previous layer)
         if (l + 1 < lend) {
-            fence_proxy_async();
-            __syncthreads();
-            if (tid == 0) issue_prefetch(p, l + 1, Pbuf + (par ^ 1) * p.p_bytes, &mbP[par ^ 1]);
-            wt.armed |= 1u << (kNSG + kNSD + (par ^ 1));
+            if (tid == 0) issue_prefetch(p, l + 1, Pb + (par ^ 1) * p.p_bytes, dirs, &mbar[kMbP + (par ^ 1)]);
+            wt.armed |= 1u << (kMbP + (par ^ 1) - kMbD);
         }
         // ------------------------------------------------------------ phase A
+        // x: the call's input, or the previous layer's y from the exchange
+        bool got = true;
         if (l == p.layer0) {
+#pragma unroll 1
             for (int i = tid; i < B * H / 4; i += kST)
                 reinterpret_cast<float4*>(xs)[i] = __ldg(reinterpret_cast<const float4*>(p.x_in) + i);
-            __syncthreads();
         } else {
-            const bool got = ll_read(p.y_ll + (size_t)(par ^ 1) * kMaxB * H, B * H, ep - 1, xs, tid, kST, p.status);
-            if (!__syncthreads_and(got ? 1 : 0)) {
-                ok = false;
-                break;
-            }
+            got = poll_rows(p.y_ll + (size_t)(par ^ 1) * kMaxB * H, 0, B, H, H, H, ep - 1, xs, p);
         }
-        // renormalisation (from the second layer on) and max |x| of each token
-        for (int t = 0; t < B; ++t) {
-            float my;
-            const float r = renorm_block(xs + t * H, H, p.eps, ds->red, &my);
-            if (tid == 0) {
-                ds->rs[t] = r;
-                ds->xmax[t] = l == p.layer0 ? my : __fmul_rn(my, r);  // max|x| = max|y| * r exactly (r > 0)
-            }
-        }
-        __syncthreads();
-        // x = y * r (from the second layer on) and its block-fixed-point digits,
-        // one pass: a warp covers 32 consecutive columns of one token (one int4
-        // chunk, two int8 chunks); the digit words are assembled with shuffles
-        // in the layout of bfp_chunk and stored whole.
-        {
-            if (tid < B) ds->xe[tid] = bfp_exponent(ds->xmax[tid]);
-            __syncthreads();
-            const bool scale = l != p.layer0;
-            for (int i = tid; i < B * H; i += kST) {
-                const int t = i / H, col = i - t * H;
-                float xv = xs[i];
-                if (scale) {
-                    xv = __fmul_rn(xv, ds->rs[t]);
-                    xs[i] = xv;
-                }
-                const int V = bfp_int(xv, ds->xe[t]);
-                uint32_t d0, d1, d2;
-                bfp_digits(V, d0, d1, d2);
-                const uint32_t dig = d0 | (d1 << 8) | (d2 << 16);
-                if (BITS == 4) {
-                    // word L = 6 cw + 2 j + odd: digit j of columns 8 cw + 2 b + odd, b = 0..3
-                    const int Lw = lane < 24 ? lane : 0;
-                    const int cw = Lw / 6, r = Lw - 6 * cw, j = r >> 1, odd = r & 1;
-                    const uint32_t g0 = __shfl_sync(kFullMask, dig, 8 * cw + 0 + odd);
-                    const uint32_t g1 = __shfl_sync(kFullMask, dig, 8 * cw + 2 + odd);
-                    const uint32_t g2 = __shfl_sync(kFullMask, dig, 8 * cw + 4 + odd);
-                    const uint32_t g3 = __shfl_sync(kFullMask, dig, 8 * cw + 6 + odd);
-                    const uint32_t sel = (uint32_t)j | ((uint32_t)(j + 4) << 4);
-                    const uint32_t word = __byte_perm(__byte_perm(g0, g1, sel), __byte_perm(g2, g3, sel), 0x5410);
-                    const int ch = col / CC;
-                    if (lane < 24) xdw[(size_t)(t * nc + ch) * DW + lane] = word;
-                    const int S = __reduce_add_sync(kFullMask, V);
-                    if (lane == 0) xS[t * nc + ch] = S;
-                } else {
-                    // per half-warp chunk: word 3 cw + j = digit j of columns 4 cw + b, b = 0..3
-                    const int hb = lane & 16, L = lane & 15;
-                    const int Lw = L < 12 ? L : 0;
-                    const int cw = Lw / 3, j = Lw - 3 * cw;
-                    const uint32_t g0 = __shfl_sync(kFullMask, dig, hb + 4 * cw + 0);
-                    const uint32_t g1 = __shfl_sync(kFullMask, dig, hb + 4 * cw + 1);
-                    const uint32_t g2 = __shfl_sync(kFullMask, dig, hb + 4 * cw + 2);
-                    const uint32_t g3 = __shfl_sync(kFullMask, dig, hb + 4 * cw + 3);
-                    const uint32_t sel = (uint32_t)j | ((uint32_t)(j + 4) << 4);
-                    const uint32_t word = __byte_perm(__byte_perm(g0, g1, sel), __byte_perm(g2, g3, sel), 0x5410);
-                    const int ch = col / CC;
-                    if (L < 12) xdw[(size_t)(t * nc + ch) * DW + L] = word;
-                    const int S = lane < 16 ? __reduce_add_sync(0x0000ffffu, V) : __reduce_add_sync(0xffff0000u, V);
-                    if (L == 0) xS[t * nc + ch] = S;
-                }
-            }
-        }
-        __syncthreads();
-        if (p.x_trace && c == 0)
-            for (int i = tid; i < B * H; i += kST) p.x_trace[(size_t)li * B * H + i] = xs[i];
-        if (!stage_wait(mbar, kNSG + kNSD + par, wt, p)) {
+        if (!__syncthreads_and(got ? 1 : 0)) {
             ok = false;
             break;
         }
-        // router rows and shared rows (prefetched), the shared gate
-        {
-            const uint8_t* pb = Pbuf + par * p.p_bytes;
-            // given routing: no router rows and no shared gate
-            const int na = given ? 0 : ne, nb = ns;
-            const int n_tasks = na + nb + (given ? 0 : B);
-            for (int task = warp; task < n_tasks; task += kSW) {
-                if (task < na) {
-                    const int e = e0 + task;
-                    const float bias = p.router_bias[(size_t)l * E + e];
-                    const uint16_t* row = reinterpret_cast<const uint16_t*>(pb + (size_t)task * 2 * H);
-                    for (int t = 0; t < B; ++t) {
-                        const float v = router_logit(row, xs + t * H, H, bias, lane);
-                        if (lane == 0) ll_store(p.lg_ll + (size_t)par * kMaxB * E + (size_t)t * E + e, v, ep);
-                    }
-                } else if (task < na + nb) {
-                    const int rr = task - na;
-                    const uint8_t* sq = pb + (size_t)p.rE * 2 * H;
-                    const uint8_t* gq = sq + (size_t)rr * qb;
-                    const uint8_t* uq = sq + (size_t)(p.rS + rr) * qb;
-                    const uint32_t* gsb = reinterpret_cast<const uint32_t*>(sq + (size_t)2 * p.rS * qb + rr * sbb);
-                    const uint32_t* usb =
-                        reinterpret_cast<const uint32_t*>(sq + (size_t)2 * p.rS * qb + (p.rS + rr) * sbb);
-                    for (int t = 0; t < B; ++t) {
-                        XDigits<BITS, NPER> xr;
-                        load_xdigits(xr, xdw + (size_t)t * nc * DW, xS + t * nc, nc, lane);
-                        float g, u;
-                        row_dot_x2(gq, gsb, uq, usb, xr, ds->xe[t], nc, lane, g, u);
-                        if (lane == 0)
-                            ll_store(p.h_ll + par * h_par + (size_t)(B * k + t) * p.h_stride + s0 + rr,
-                                     silu_mul(g, u), ep);
-                    }
-                } else {
-                    const int t = task - na - nb;
-                    const float sg =
-                        p.Is > 0 ? shared_gate(p.shared_gate + (size_t)l * H, xs + t * H, H, lane) : 0.0f;
-                    if (lane == 0) ds->sig[t] = sg;
-                }
+#pragma unroll 1
+        for (int t = 0; t < B; ++t) {
+            float s, m;
+            renorm_partial(xs + t * H, H, tid, s, m);
+            s = warp_sum(s);
+            m = warp_max(m);
+            if (lane == 0) {
+                ds->red[t][0][warp] = s;
+                ds->red[t][1][warp] = m;
             }
         }
+        __syncthreads();
+        if (tid < B) {
+            const int t = tid;
+            float mx = ds->red[t][1][0];
+#pragma unroll 1
+            for (int w = 1; w < kSW; ++w) mx = fmaxf(mx, ds->red[t][1][w]);
+            const float r = renorm_scale(ds->red[t][0], H, p.eps);
+            ds->rs[t] = r;
+            const float xm = l == p.layer0 ? mx : __fmul_rn(mx, r);  // max|x| = max|y| * r exactly (r > 0)
+            ds->xmax[t] = xm;
+            ds->xe[t] = bfp_exponent(xm);
+        }
+        __syncthreads();
+        if (l != p.layer0) {  // x = y * r
+#pragma unroll 1
+            for (int i = tid; i < B * H; i += kST) xs[i] = __fmul_rn(xs[i], ds->rs[i / H]);
+            __syncthreads();
+        }
+        if (p.x_trace && c == 0)
+#pragma unroll 1
+            for (int i = tid; i < B * H; i += kST) p.x_trace[(size_t)li * B * H + i] = xs[i];
+        if (!stage_wait(mbar, kMbP + par, wt, p)) {
+            ok = false;
+            break;
+        }
+        // The router rows go first, on the top warps: their logits reach the
+        // exchange while the other warps make the digits (which only the
+        // expert rows need) and these warps the shared gate.
+        {
+            const int na = given ? 0 : ne * B, ng = given || p.Is == 0 ? 0 : B;
+            const int nr = min(kSW / 2, max(1, na + ng));  // router warps
+            if (warp >= kSW - nr) {
+                unsigned long long* lgx = p.lg_ll + (size_t)par * kMaxB * E;
+#pragma unroll 1
+                for (int task = kSW - 1 - warp; task < na + ng; task += nr) {
+                    const bool gate = task >= na;
+                    const int q = gate ? task - na : task;
+                    const int t = gate ? q : q % B, e = gate ? 0 : e0 + q / B;
+                    const uint16_t* row =
+                        reinterpret_cast<const uint16_t*>(Pbuf + (gate ? (size_t)p.off_sg : (size_t)(e - e0) * 2 * H));
+                    const float v =
+                        router_logit(row, xs + t * H, H, gate ? 0.0f : p.router_bias[(size_t)l * E + e], lane);
+                    if (gate) {
+                        if (lane == 0) ds->sig[t] = __fdividef(1.0f, __fadd_rn(1.0f, __expf(-v)));
+                    } else if (lane == 0) {
+                        ll_store(lgx + (size_t)t * E + e, v, ep);
+                    }
+                }
+            } else {
+                make_digits<BITS>(B, H, xs, xdw, xS, ds, 0, kSW - nr);
+            }
+        }
+        __syncthreads();
         // ------------------------------------------------------------ phase B
-        // Routing by ranks (no serial selection loop).  Temp area in the
-        // gate/up stages, before this layer's copies land there.
-        const int C = kSW * k;  // top-k candidates per token (k from each warp's slice)
-        uint8_t* tp = Gbuf;
-        float* s_lg = reinterpret_cast<float*>(tp);  // [B][E] logits
-        tp += r16i(B * E * 4);
-        uint32_t* c_key = reinterpret_cast<uint32_t*>(tp);  // [B][C]
-        tp += r16i(B * C * 4);
-        int32_t* c_idx = reinterpret_cast<int32_t*>(tp);  // [B][C], -1 = empty
         if (given) {
+#pragma unroll 1
             for (int i = tid; i < B * k; i += kST) {
                 ds->idx[i / k][i % k] = p.rin_idx[i];
                 ds->w[i / k][i % k] = p.rin_w[i];
             }
             if (tid < B) ds->sig[tid] = p.Is > 0 ? p.rin_sig[tid] : 0.0f;
         } else {
-        {
-            const bool got = ll_read(p.lg_ll + (size_t)par * kMaxB * E, B * E, ep, s_lg, tid, kST, p.status);
-            if (!__syncthreads_and(got ? 1 : 0)) {
+            const bool okl = topk_lists(p, p.lg_ll + (size_t)par * kMaxB * E, ep, TT, M, nlist);
+            if (!__syncthreads_and(okl ? 1 : 0)) {
                 ok = false;
                 break;
             }
+            if (warp < B) topk_merge(p, TT, ds, nlist);
         }
-        for (int i = tid; i < B * C; i += kST) c_idx[i] = -1;
-        __syncthreads();
-        // level 1: each warp selects the k best keys of its slice of every
-        // token (key desc, index asc; <= 4 keys per lane), one per round: a
-        // warp max of the lanes' best keys, then the lowest index among the
-        // lanes holding it.  The slice's picks become candidates in order.
-        {
-            const int S = ((E + kSW - 1) / kSW + 31) / 32 * 32;  // slice of whole warp-rows
-            const int sb = warp * S, se = min(E, sb + S), M1 = S / 32;
-            for (int t = 0; t < B; ++t) {
-                uint32_t key[4];
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const int j = sb + lane + 32 * m;
-                    key[m] = (m < M1 && j < se) ? order_key(s_lg[t * E + j]) : 0u;
-                }
-#pragma unroll 1
-                for (int r = 0; r < k; ++r) {
-                    uint32_t best = key[0];
-                    int bm = 0;
-#pragma unroll
-                    for (int m = 1; m < 4; ++m)
-                        if (key[m] > best) best = key[m], bm = m;
-                    const uint32_t mx = __reduce_max_sync(kFullMask, best);
-                    const uint32_t jw = __reduce_min_sync(
-                        kFullMask, (best == mx && mx != 0u) ? (uint32_t)(sb + lane + 32 * bm) : 0xffffffffu);
-                    if (jw == 0xffffffffu) break;  // the slice has fewer than k keys
-                    if (lane == 0) {
-                        c_key[t * C + warp * k + r] = mx;
-                        c_idx[t * C + warp * k + r] = (int)jw;
-                    }
-                    const int lw = (int)(jw - sb) & 31, mw = (int)(jw - sb) >> 5;
-#pragma unroll
-                    for (int m = 0; m < 4; ++m)
-                        if (lane == lw && m == mw) key[m] = 0u;
-                }
-            }
-        }
-        __syncthreads();
-        // level 2 (one warp per token): the same selection over the token's
-        // candidates (<= 4 per lane), ties to the lower expert index; then the
-        // routing weights
-        if (warp < B) {
-            const int t = warp;
-            uint32_t key[4];
-            int id[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int j = lane + 32 * m;
-                const int ij = j < C ? c_idx[t * C + j] : -1;
-                key[m] = ij >= 0 ? c_key[t * C + j] : 0u;
-                id[m] = ij >= 0 ? ij : 0x7fffffff;
-            }
-#pragma unroll 1
-            for (int r = 0; r < k; ++r) {
-                uint32_t best = key[0];
-                int bi = id[0];
-#pragma unroll
-                for (int m = 1; m < 4; ++m)
-                    if (key[m] > best || (key[m] == best && id[m] < bi)) best = key[m], bi = id[m];
-                const uint32_t mx = __reduce_max_sync(kFullMask, best);
-                const int w = (int)__reduce_min_sync(kFullMask, best == mx ? (uint32_t)bi : 0xffffffffu);
-                if (lane == 0) {
-                    ds->idx[t][r] = w;
-                    ds->val[t][r] = s_lg[t * E + w];
-                }
-#pragma unroll
-                for (int m = 0; m < 4; ++m)
-                    if (id[m] == w) key[m] = 0u, id[m] = 0x7fffffff;
-            }
-            __syncwarp();
-            topk_weights(s_lg + t * E, E, k, p.norm_topk, lane, ds->val[t], ds->w[t]);
-        }
-        }  // routing computed
         __syncthreads();
         if (streamed) {
             // residency of the layer's experts: the same answer in every CTA
-            const bool absent = tid < B * k && p.dir[(size_t)l * E + ds->idx[tid / k][tid % k]] == nullptr;
+            const bool absent = tid < B * k && dirs[(l & 1) * E + ds->idx[tid / k][tid % k]] == nullptr;
             const bool stop = __syncthreads_or(absent ? 1 : 0) != 0;
             if (c == 0) {
                 int32_t* row = p.pub_idx + (size_t)l * p.pub_stride;
+#pragma unroll 1
                 for (int i = tid; i < B * k; i += kST) row[i] = ds->idx[i / k][i % k];
                 if (stop) {
+#pragma unroll 1
                     for (int i = tid; i < B * H; i += kST) p.x_out[i] = xs[i];
+#pragma unroll 1
                     for (int i = tid; i < B * k; i += kST) {
                         p.rout_idx[i] = ds->idx[i / k][i % k];
                         p.rout_w[i] = ds->w[i / k][i % k];
@@ -659,235 +852,174 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const Params p) {
             if (stop) break;  // the host fetches the missing experts and launches again from this layer
         }
         if (p.idx_trace && c == 0 && tid < B * k) p.idx_trace[(size_t)li * B * k + tid] = ds->idx[tid / k][tid % k];
-        // dispatch (warp 0): pairs sorted by (expert, token) by rank (pair key
-        // expert << 3 | token), then active experts in ascending id
-        const int nq = B * k;
-        if (warp == 0) {
-            for (int m = 0; m * 32 < nq; ++m) {
-                const int q = lane + 32 * m;
-                const uint32_t kq = q < nq ? ((uint32_t)ds->idx[q / k][q % k] << 3) | (uint32_t)(q / k) : 0xffffffffu;
-                int rank = 0;
-                for (int mm = 0; mm * 32 < nq; ++mm) {
-                    const int qb = lane + 32 * mm;
-                    const uint32_t kb =
-                        qb < nq ? ((uint32_t)ds->idx[qb / k][qb % k] << 3) | (uint32_t)(qb / k) : 0xffffffffu;
-                    const int lim = min(32, nq - 32 * mm);
-#pragma unroll 4
-                    for (int s2 = 0; s2 < lim; ++s2) rank += __shfl_sync(kFullMask, kb, s2) < kq ? 1 : 0;
-                }
-                if (q < nq) {
-                    D.pair_act[rank] = (int)kq;  // the sorted keys, replaced by active indices below
-                    D.pair_w[rank] = ds->w[q / k][q % k];
-                }
-            }
-            __syncwarp();
-            int base = 0;
-            uint32_t prev = 0xffffffffu;
-            for (int m = 0; m * 32 < nq; ++m) {
-                const int pr = lane + 32 * m;
-                const uint32_t kq = pr < nq ? (uint32_t)D.pair_act[pr] : 0xffffffffu;
-                uint32_t kp = __shfl_up_sync(kFullMask, kq, 1);
-                if (lane == 0) kp = prev;
-                const bool first = pr < nq && (kp == 0xffffffffu || (kp >> 3) != (kq >> 3));
-                const unsigned bal = __ballot_sync(kFullMask, first);
-                const int a = base + __popc(bal & (0xffffffffu >> (31 - lane))) - 1;
-                prev = __shfl_sync(kFullMask, kq, 31);
-                __syncwarp();
-                if (pr < nq) {
-                    const int e = (int)(kq >> 3);
-                    D.pair_token[pr] = (int)(kq & 7u);
-                    D.pair_act[pr] = a;
-                    if (first) {
-                        D.act_expert[a] = e;
-                        D.act_blob[a] = p.dir[(size_t)l * E + e];
-                        D.act_off[a] = pr;
-                    }
-                }
-                base += __popc(bal);
-            }
-            if (lane == 0) ds->n_routed = base;
-        }
-        __syncthreads();
-        if (tid == 0) {
-            const int nr = ds->n_routed;
-            ds->n_pairs = B * k + (p.Is > 0 ? B : 0);
-            ds->n_act = nr + (p.Is > 0 ? 1 : 0);
-            if (p.Is > 0) {
-                D.act_expert[nr] = -1;
-                D.act_blob[nr] = p.shared_pool + (size_t)l * p.shared_stride;
-                D.act_off[nr] = B * k;
-                D.act_off[nr + 1] = B * k + B;
-            } else {
-                D.act_off[nr] = B * k;
-            }
-        }
-        if (p.Is > 0 && tid < B) {
-            D.pair_token[B * k + tid] = tid;
-            D.pair_w[B * k + tid] = ds->sig[tid];
-            D.pair_act[B * k + tid] = ds->n_routed;
-        }
-        fence_proxy_async();  // generic accesses to the stages precede the bulk writes below
+        if (warp == 0) dispatch(p, D, ds, l, dirs + (l & 1) * E);
+        fence_proxy_async();  // generic accesses to the copy targets precede the bulk writes below
         __syncthreads();
         const int n_act = ds->n_act, n_pairs = ds->n_pairs;
         const int U = ds->n_routed * p.I;
-        const int u0 = (int)((long long)U * c / G), u1 = (int)((long long)U * (c + 1) / G);
+        const int u0 = U * c / G, u1 = U * (c + 1) / G;  // U <= 129 * 4096
         const int mine = u1 - u0;
-        const int gcs = mine > 0 ? min(p.g_cap, max(2 * kSW, (mine + kNSG - 1) / kNSG)) : 1;
-        const int n_gch = (mine + gcs - 1) / gcs;
-        const int dcs = min(p.d_cap, (n_act + kNSD - 1) / kNSD);
+        const int wu0 = u0 + mine * warp / kSW, wn = u0 + mine * (warp + 1) / kSW - wu0;  // this warp's units
+        const int dcs = min(p.d_cap, n_act);
         const int n_dch = jn > 0 ? (n_act + dcs - 1) / dcs : 0;
-        // one issuing lane per stage: warps 0..3 gate/up, 4..5 down, 6 next-layer prefetch
+        // copies: each warp its first R units, then the last warps one down stage each
         if (lane == 0) {
-            if (warp < kNSG) {
-                if (warp < n_gch)
-                    issue_gateup(p, D, u0 + warp * gcs, min(u1, u0 + (warp + 1) * gcs), Gbuf + (size_t)warp * gstage,
-                                 &mbG[warp]);
-            } else if (warp < kNSG + kNSD) {
-                const int s = warp - kNSG;
-                if (s < n_dch)
-                    issue_down(p, D, s * dcs, min(n_act, (s + 1) * dcs), j0, jn, Dbuf + (size_t)s * dstage, &mbD[s]);
+#pragma unroll 1
+            for (int j = 0; j < min(R, wn); ++j) {
+                const int u = wu0 + j, a = u / p.I;
+                issue_unit(p, D.act_blob[a], u - a * p.I, wslots + (size_t)j * p.g_unit, &mbar[warp * kRing + j]);
             }
+            const int s = kSW - 1 - warp;
+            if (s < min(n_dch, kNSD))
+                issue_down(p, D, s * dcs, min(n_act, (s + 1) * dcs), j0, jn, Dbuf + (size_t)s * dstage,
+                           &mbar[kMbD + s]);
         }
-        for (int s = 0; s < min(n_gch, kNSG); ++s) wt.armed |= 1u << s;
-        for (int s = 0; s < min(n_dch, kNSD); ++s) wt.armed |= 1u << (kNSG + s);
-        // gate/up + SwiGLU, stage by stage
-        unsigned long long* hll = p.h_ll + par * h_par;
-        for (int ch = 0; ch < n_gch; ++ch) {
-            const int s = ch % kNSG;
-            if (!stage_wait(mbar, s, wt, p)) {
-                ok = false;
-                break;
-            }
-            const uint8_t* st = Gbuf + (size_t)s * gstage;
-            const int ua = u0 + ch * gcs, n = min(u1, ua + gcs) - ua;
-            const int w0 = n * warp / kSW, w1 = n * (warp + 1) / kSW;
-            int cur_t = -1;
-            XDigits<BITS, NPER> xr;
-            for (int o = w0; o < w1; ++o) {
-                const int u = ua + o, a = u / p.I, r = u - a * p.I;
-                const uint8_t* gq = st + (size_t)o * qb;
-                const uint8_t* uq = st + (size_t)(p.g_cap + o) * qb;
-                const uint32_t* gsb = reinterpret_cast<const uint32_t*>(st + (size_t)2 * p.g_cap * qb + o * sbb);
-                const uint32_t* usb =
-                    reinterpret_cast<const uint32_t*>(st + (size_t)2 * p.g_cap * qb + (p.g_cap + o) * sbb);
+#pragma unroll 1
+        for (int j = 0; j < min(R, wn); ++j) warm |= 1u << j;
+#pragma unroll 1
+        for (int s = 0; s < min(n_dch, kNSD); ++s) wt.armed |= 1u << s;
+        // the shared expert's rows of this CTA (in shared memory since the
+        // previous layer) while the routed rows are in flight
+#pragma unroll 1
+        for (int task = warp; task < ns * B; task += kSW) {
+            const int rr = task / B, t = task - rr * B;
+            const uint8_t* sq = Pbuf + (size_t)p.rE * 2 * H;
+            const uint8_t* sbase = sq + (size_t)2 * p.rS * qb;
+            const float h = swiglu_row<BITS>(sq + (size_t)rr * qb, sq + (size_t)(p.rS + rr) * qb,
+                                             reinterpret_cast<const uint32_t*>(sbase + rr * sbb),
+                                             reinterpret_cast<const uint32_t*>(sbase + (p.rS + rr) * sbb),
+                                             xdw + (size_t)t * nc * DW, xS + t * nc, ds->xe[t], nc);
+            if (lane == 0) ll_store(hll + (size_t)(B * k + t) * p.h_stride + s0 + rr, h, ep);
+        }
+        // gate/up + SwiGLU: this warp's units as they land
+        {
+            bool okw = true;
+#pragma unroll 1
+            for (int j = 0; j < wn; ++j) {
+                const int s = j % R;
+                if (!warp_wait(&mbar[warp * kRing + s], (wph >> s) & 1u, p)) {
+                    okw = false;
+                    break;
+                }
+                wph ^= 1u << s;
+                warm &= ~(1u << s);
+                const uint8_t* st = wslots + (size_t)s * p.g_unit;
+                const int u = wu0 + j, a = u / p.I, r = u - a * p.I;
+#pragma unroll 1
                 for (int pr = D.act_off[a]; pr < D.act_off[a + 1]; ++pr) {
                     const int t = D.pair_token[pr];
-                    if (t != cur_t) {
-                        load_xdigits(xr, xdw + (size_t)t * nc * DW, xS + t * nc, nc, lane);
-                        cur_t = t;
+                    const float h = swiglu_row<BITS>(st, st + qb, reinterpret_cast<const uint32_t*>(st + 2 * qb),
+                                                     reinterpret_cast<const uint32_t*>(st + 2 * qb + sbb),
+                                                     xdw + (size_t)t * nc * DW, xS + t * nc, ds->xe[t], nc);
+                    if (lane == 0) ll_store(hll + (size_t)pr * p.h_stride + r, h, ep);
+                }
+                if (j + R < wn) {
+                    fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const int un = wu0 + j + R, an = un / p.I;
+                        issue_unit(p, D.act_blob[an], un - an * p.I, wslots + (size_t)s * p.g_unit,
+                                   &mbar[warp * kRing + s]);
                     }
-                    float g, uu;
-                    row_dot_x2(gq, gsb, uq, usb, xr, ds->xe[t], nc, lane, g, uu);
-                    if (lane == 0) ll_store(hll + (size_t)pr * p.h_stride + r, silu_mul(g, uu), ep);
+                    warm |= 1u << s;
                 }
             }
-            fence_proxy_async();
-            __syncthreads();
-            if (ch + kNSG < n_gch) {
-                if (tid == 0)
-                    issue_gateup(p, D, u0 + (ch + kNSG) * gcs, min(u1, u0 + (ch + kNSG + 1) * gcs),
-                                 Gbuf + (size_t)s * gstage, &mbG[s]);
-                wt.armed |= 1u << s;
-            }
-        }
-        if (!ok) break;
-        // ------------------------------------------------------------ phase C
-        for (int ch = 0; ch < n_dch && ok; ++ch) {
-            const int s = ch % kNSD;
-            if (!stage_wait(mbar, kNSG + s, wt, p)) {
+            if (!__syncthreads_and(okw ? 1 : 0)) {
                 ok = false;
                 break;
             }
-            const uint8_t* st = Dbuf + (size_t)s * dstage;
-            const int aa = ch * dcs, ab = min(n_act, aa + dcs);
-            const int pa = D.act_off[aa], pb = D.act_off[ab];
-            // h of the pairs, into the (idle) gate/up stage area: all pairs at the
-            // first stage when they fit, else this stage's pairs
-            const bool all_h = (long long)n_pairs * p.h_stride * 4 <= (long long)kNSG * gstage;
-            const int ha = all_h ? 0 : pa, hb = all_h ? n_pairs : pb;
-            float* hs = reinterpret_cast<float*>(Gbuf) - (size_t)ha * p.h_stride;  // hs[pr * h_stride + col]
-            if (!all_h || ch == 0) {
-                const int nrt = max(0, min(hb, B * k) - ha);  // routed pairs (cols I), then shared pairs (cols Is)
-                bool okh = ll_read_rows(hll, ha, nrt, p.h_stride, p.I, ep, hs + (size_t)ha * p.h_stride, tid, kST,
-                                        p.status);
-                if (okh && hb > ha + nrt)
-                    okh = ll_read_rows(hll, ha + nrt, hb - ha - nrt, p.h_stride, p.Is, ep,
-                                       hs + (size_t)(ha + nrt) * p.h_stride, tid, kST, p.status);
-                if (!__syncthreads_and(okh ? 1 : 0)) {
+        }
+        // ------------------------------------------------------------ phase C
+        // Each warp takes whole pairs: it polls the pair's h straight from the
+        // exchange into registers and multiplies this CTA's down rows of the
+        // pair's expert, so the first pairs run while the last are in flight.
+        // The down stages are used in rounds of kNSD (one round when every
+        // active expert fits).
+        {
+            const int rounds = (n_dch + kNSD - 1) / kNSD;
+#pragma unroll 1
+            for (int rd = 0; rd < rounds && ok; ++rd) {
+                const int aa = rd * kNSD * dcs, ab = min(n_act, aa + kNSD * dcs);
+                bool okc = true;
+#pragma unroll 1
+                for (int pr = D.act_off[aa] + warp; pr < D.act_off[ab] && okc; pr += kSW) {
+                    const int a = D.pair_act[pr];
+                    const int s = (a - aa) / dcs;
+                    if (!warp_wait(&mbar[kMbD + s], (wt.phase >> s) & 1u, p)) {
+                        okc = false;
+                        break;
+                    }
+                    const int cols = D.act_expert[a] < 0 ? p.Is : p.I;
+                    const bool halves = BITS == 4 && cols == 16 * CC;
+                    const int ch = halves ? (lane & 15) : lane;
+                    HF<BITS> hd;
+                    if (!poll_h_chunk<BITS>(hll + (size_t)pr * p.h_stride, halves || ch < cols / CC, ch, ep, hd, p)) {
+                        okc = false;
+                        break;
+                    }
+                    hf_sum(hd);
+                    const uint32_t rb = (uint32_t)cols * BITS / 8, dsb = (uint32_t)cols / 16;
+                    const uint8_t* unit = Dbuf + (size_t)s * dstage + (size_t)(a - aa - s * dcs) * p.d_unit;
+                    const uint8_t* sbase = unit + p.d_rows_bytes + ((j0 * dsb) & 15u);
+                    const float wp = D.pair_w[pr];
+                    if (halves) {
+                        // 16 chunks per row: two rows per pass, one per half-warp
+#pragma unroll 1
+                        for (int jj = 0; jj < jn; jj += 2) {
+                            const int j1 = min(jj + 1, jn - 1);  // an odd tail repeats its row in the upper half
+                            const float v = row_dot_h_halves<BITS>(
+                                unit + (size_t)jj * rb, reinterpret_cast<const uint32_t*>(sbase + (size_t)jj * dsb),
+                                unit + (size_t)j1 * rb, reinterpret_cast<const uint32_t*>(sbase + (size_t)j1 * dsb), hd,
+                                lane);
+                            const int jo = jj + (lane >> 4);
+                            if ((lane & 15) == 0 && jo < jn) part[(size_t)pr * p.jn + jo] = __fmul_rn(wp, v);
+                        }
+                    } else {
+#pragma unroll 1
+                        for (int jj = 0; jj < jn; ++jj) {
+                            const float v = row_dot_h<BITS>(unit + (size_t)jj * rb,
+                                                            reinterpret_cast<const uint32_t*>(sbase + (size_t)jj * dsb),
+                                                            hd, cols, lane);
+                            if (lane == 0) part[(size_t)pr * p.jn + jj] = __fmul_rn(wp, v);
+                        }
+                    }
+                }
+                fence_proxy_async();
+                if (!__syncthreads_and(okc ? 1 : 0)) {
                     ok = false;
                     break;
                 }
-            }
-            bool okc = true;
-            // tasks: (pair, group of kRG of this CTA's rows)
-            constexpr int kRG = 8;
-            const int ngr = (jn + kRG - 1) / kRG;
-            for (int task = warp; task < (pb - pa) * ngr; task += kSW) {
-                const int pr = pa + task / ngr, g0 = (task % ngr) * kRG;
-                const int a = D.pair_act[pr];
-                const int cols = D.act_expert[a] < 0 ? p.Is : p.I;
-                const uint32_t rb = (uint32_t)cols * BITS / 8, dsb = (uint32_t)cols / 16;
-                const uint8_t* unit = st + (size_t)(a - aa) * p.d_unit;
-                const uint8_t* sbase = unit + p.d_rows_bytes + ((j0 * dsb) & 15u);
-                HF<BITS> hd;
-                const bool halves = BITS == 4 && cols == 16 * CC;
-                const float* hrow = hs + (size_t)pr * p.h_stride + (halves ? (lane & 15) : lane) * CC;
-                if (halves || lane < cols / CC) {
-#pragma unroll
-                    for (int i = 0; i < CC; i += 4) {
-                        const float4 v = *reinterpret_cast<const float4*>(hrow + i);
-                        hd.v[i] = v.x, hd.v[i + 1] = v.y, hd.v[i + 2] = v.z, hd.v[i + 3] = v.w;
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < CC; ++i) hd.v[i] = 0.0f;
+                // every stage of the round has completed (each holds an expert some warp waited for)
+                const int ns_r = (ab - aa + dcs - 1) / dcs;
+#pragma unroll 1
+                for (int s = 0; s < ns_r; ++s) {
+                    wt.phase ^= 1u << s;
+                    wt.armed &= ~(1u << s);
                 }
-                hf_sum(hd);
-                const float wp = D.pair_w[pr];
-                const int je = min(jn, g0 + kRG);
-                if (halves) {
-                    // 16 chunks per row: two rows per pass, one per half-warp
+                if (rd + 1 < rounds) {
+                    const int na0 = (rd + 1) * kNSD * dcs;
 #pragma unroll 1
-                    for (int jj = g0; jj < je; jj += 2) {
-                        const int j1 = min(jj + 1, je - 1);  // an odd tail repeats its row in the upper half
-                        const float v = row_dot_h_halves<BITS>(
-                            unit + (size_t)jj * rb, reinterpret_cast<const uint32_t*>(sbase + (size_t)jj * dsb),
-                            unit + (size_t)j1 * rb, reinterpret_cast<const uint32_t*>(sbase + (size_t)j1 * dsb), hd,
-                            lane);
-                        const int jo = jj + (lane >> 4);
-                        if ((lane & 15) == 0 && jo < je) part[(size_t)pr * p.jn + jo] = __fmul_rn(wp, v);
-                    }
-                } else {
-#pragma unroll 1
-                    for (int jj = g0; jj < je; ++jj) {
-                        const float v = row_dot_h<BITS>(unit + (size_t)jj * rb,
-                                                        reinterpret_cast<const uint32_t*>(sbase + (size_t)jj * dsb), hd,
-                                                        cols, lane);
-                        if (lane == 0) part[(size_t)pr * p.jn + jj] = __fmul_rn(wp, v);
+                    for (int s = 0; s < kNSD && na0 + s * dcs < n_act; ++s) {
+                        if (tid == 0)
+                            issue_down(p, D, na0 + s * dcs, min(n_act, na0 + (s + 1) * dcs), j0, jn,
+                                       Dbuf + (size_t)s * dstage, &mbar[kMbD + s]);
+                        wt.armed |= 1u << s;
                     }
                 }
             }
-            fence_proxy_async();
-            if (!__syncthreads_and(okc ? 1 : 0)) {
-                ok = false;
-                break;
-            }
-            if (ch + kNSD < n_dch) {
-                if (tid == 0)
-                    issue_down(p, D, (ch + kNSD) * dcs, min(n_act, (ch + kNSD + 1) * dcs), j0, jn,
-                               Dbuf + (size_t)s * dstage, &mbD[s]);
-                wt.armed |= 1u << (kNSG + s);
-            }
+            if (!ok) break;
         }
-        if (!ok) break;
         // y rows of this CTA: ascending expert order per token
+        const bool withhold = c == p.fault_cta && li == 0 && p.n_layers > 1;
+#pragma unroll 1
         for (int i = tid; i < B * jn; i += kST) {
             const int t = i / jn, jj = i - t * jn;
             float acc = 0.0f;
+#pragma unroll 1
             for (int pr = 0; pr < n_pairs; ++pr)
                 if (D.pair_token[pr] == t) acc = __fadd_rn(acc, part[(size_t)pr * p.jn + jj]);
             const size_t o = (size_t)t * H + j0 + jj;
-            ll_store(p.y_ll + (size_t)par * kMaxB * H + o, acc, ep);
+            if (!withhold) ll_store(p.y_ll + (size_t)par * kMaxB * H + o, acc, ep);
             if (l == lend - 1) p.y_out[o] = acc;
             if (p.y_trace) p.y_trace[(size_t)li * B * H + o] = acc;
         }
@@ -895,11 +1027,19 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const Params p) {
     }
     // drain outstanding copies (bounded) before the CTA's shared memory goes away
     __syncthreads();
-    for (int i = 0; i < kNB; ++i) {
-        if (wt.armed & (1u << i)) {
-            const uint32_t par = (wt.phase >> i) & 1u;
+#pragma unroll 1
+    for (int s = 0; s < kRing; ++s)
+        if (warm & (1u << s)) {
             const unsigned long long t0 = gtime();
-            while (!mbar_test(&mbar[i], par) && gtime() - t0 < kWaitNs) {
+            while (!mbar_test(&mbar[warp * kRing + s], (wph >> s) & 1u) && gtime() - t0 < p.wait_ns) {
+            }
+        }
+#pragma unroll 1
+    for (int i = kMbD; i < kNB; ++i) {
+        const uint32_t bit = 1u << (i - kMbD);
+        if (wt.armed & bit) {
+            const unsigned long long t0 = gtime();
+            while (!mbar_test(&mbar[i], (wt.phase & bit) ? 1u : 0u) && gtime() - t0 < p.wait_ns) {
             }
         }
     }
@@ -922,11 +1062,6 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const Params p) {
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-int nper_of(int hidden, int bits) {
-    const int nchunk = hidden * bits / 128;
-    return (nchunk + 31) / 32;
-}
-
 bool plan(const Shapes& sh, int B, int grid, int max_smem, Params& p) {
     const int H = sh.hidden, E = sh.n_experts, k = sh.top_k, bits = sh.bits;
     auto r128 = [](long long v) { return (int)((v + 127) / 128 * 128); };
@@ -935,8 +1070,9 @@ bool plan(const Shapes& sh, int B, int grid, int max_smem, Params& p) {
     p.rS = (sh.shared_inter + G - 1) / G;
     p.jn = (H + G - 1) / G;
     const int qb = H * bits / 8, sbb = H / 16;
-    p.p_bytes = r128((long long)p.rE * 2 * H + (long long)p.rS * 2 * (qb + sbb));
-    p.g_unit = 2 * (qb + sbb);
+    p.off_sg = p.rE * 2 * H + p.rS * 2 * (qb + sbb);  // a multiple of 16
+    p.p_bytes = r128((long long)p.off_sg + 2 * H);
+    p.g_unit = r16i(2 * (qb + sbb));
     const int cmax = std::max(sh.inter, sh.shared_inter);
     const int rbmax = cmax * bits / 8, sbmax = cmax / 16;
     p.d_rows_bytes = r16i(p.jn * rbmax);
@@ -954,46 +1090,35 @@ bool plan(const Shapes& sh, int B, int grid, int max_smem, Params& p) {
     off += r128((long long)B * H * 4);
     p.off_xd = off;
     off += r128((long long)B * nc * (DW + 1) * 4);
-    p.off_P = off;
+    p.off_P = off;  // [2][p_bytes], by layer parity
     off += 2 * p.p_bytes;
+    p.off_dirs = off;  // [2][E] blob addresses
+    off += r128(2LL * E * 8);
     const int budget = max_smem - 1024;  // static shared memory of the kernel
-    int left = budget - off;
-    p.d_cap = std::max(1, std::min((k + 2 + kNSD - 1) / kNSD, left / 3 / (kNSD * p.d_unit)));
-    const int dbytes = kNSD * p.d_cap * p.d_unit;  // sized before any reduction of d_cap below
-    left -= dbytes;
-    p.g_cap = left / (kNSG * p.g_unit);
-    if (p.g_cap < 1) return false;
-    // phase C stages the h of a down stage's pairs (<= d_cap * B + B) in the gate/up area
-    while (p.d_cap > 1 && (long long)(p.d_cap * B + B) * sh.h_stride * 4 > (long long)kNSG * p.g_cap * p.g_unit)
-        --p.d_cap;
-    if ((long long)(p.d_cap * B + B) * sh.h_stride * 4 > (long long)kNSG * p.g_cap * p.g_unit) return false;
+    const int left = budget - off;
+    // down stages: every active expert in the two stages if that leaves each
+    // warp two gate/up slots, else fewer experts per stage
+    int d_cap = (p.amax + kNSD - 1) / kNSD;
+    auto ring_for = [&](int dc) { return (left - kNSD * dc * p.d_unit) / (kSW * p.g_unit); };
+    while (d_cap > 1 && ring_for(d_cap) < 2) --d_cap;
+    p.d_cap = d_cap;
+    p.ring = std::min(kRing, ring_for(d_cap));
+    if (p.ring < 1) return false;
+    p.g_bytes = kSW * p.ring * p.g_unit;
+    // the gate/up area also holds the top-k scratch
+    if (topk_temp_bytes(B, E, k) > p.g_bytes) return false;
     p.off_G = off;
-    off += kNSG * p.g_cap * p.g_unit;
+    off += p.g_bytes;
     off = r128(off);
     p.off_D = off;
-    off += dbytes;
+    off += kNSD * p.d_cap * p.d_unit;
     p.smem_bytes = off;
-    // the top-k temp area lives in the gate/up stages
-    const long long tmp =
-        r16i(B * E * 4) + 2LL * r16i(B * kSW * k * 4);
-    if (tmp > (long long)kNSG * p.g_cap * p.g_unit) return false;
     return off <= budget;
 }
 
-template <int BITS, int NPER>
-void* kernel_ptr() {
-    return reinterpret_cast<void*>(&stack_kernel<BITS, NPER>);
-}
-
-void* select_kernel(int bits, int nper) {
-    if (bits == 4) {
-        if (nper == 1) return kernel_ptr<4, 1>();
-        if (nper == 2) return kernel_ptr<4, 2>();
-    } else {
-        if (nper == 1) return kernel_ptr<8, 1>();
-        if (nper == 2) return kernel_ptr<8, 2>();
-        if (nper == 4) return kernel_ptr<8, 4>();
-    }
+void* select_kernel(int bits) {
+    if (bits == 4) return reinterpret_cast<void*>(&stack_kernel<4>);
+    if (bits == 8) return reinterpret_cast<void*>(&stack_kernel<8>);
     return nullptr;
 }
 
@@ -1037,8 +1162,7 @@ int stack_alloc(StackScratch& s, const Shapes& sh, int n_layers, int max_batch, 
         err = "stack scratch initialisation failed";
         return MOE_ECUDA;
     }
-    const int nper = nper_of(sh.hidden, sh.bits);
-    if (void* f = select_kernel(sh.bits, nper)) {
+    if (void* f = select_kernel(sh.bits)) {
         if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, s.max_smem - 1024) != cudaSuccess) {
             cudaGetLastError();
             s.grid = 0;  // persistent kernel unavailable; per-layer kernels serve the stack
@@ -1059,8 +1183,9 @@ void stack_free(StackScratch& s) {
 
 bool stack_supported(const Shapes& sh, const StackScratch& s, int B) {
     if (s.grid <= 0 || !s.lg_ll || B < 1 || B > kMaxB || sh.hidden > 2048 || sh.top_k > 16) return false;
-    const int nper = nper_of(sh.hidden, sh.bits);
-    if (!select_kernel(sh.bits, nper)) return false;
+    if (sh.n_experts > 2 * kST) return false;  // two keys per lane in the first top-k level
+    if (sh.n_experts % 2) return false;        // directory rows are bulk-copied: 16-byte aligned rows
+    if (!select_kernel(sh.bits)) return false;
     const int cmax = std::max(sh.inter, sh.shared_inter);
     if (cmax * sh.bits / 128 > 32) return false;  // one chunk per lane on down rows
     Params p{};
@@ -1080,6 +1205,8 @@ cudaError_t launch_stack(const Shapes& sh, StackScratch& s, const StackArgs& a, 
     p.shared_pool = a.shared_pool, p.shared_stride = a.shared_stride;
     p.lg_ll = s.lg_ll, p.h_ll = s.h_ll, p.y_ll = s.y_ll, p.h_stride = sh.h_stride, p.hp = s.hp;
     p.sync = s.sync, p.status = s.status, p.status_host = s.status_host_dev;
+    p.wait_ns = a.fault ? kFaultWaitNs : kWaitNs;
+    p.fault_cta = a.fault ? s.grid - 1 : -1;
     if (a.rin_idx) {
         if (!a.rin_w || !a.rin_sig || !a.pub || !a.x_out || !a.rout_idx || !a.rout_w || !a.rout_sig)
             return cudaErrorInvalidValue;
@@ -1088,7 +1215,7 @@ cudaError_t launch_stack(const Shapes& sh, StackScratch& s, const StackArgs& a, 
         p.pub_idx = a.pub->idx, p.pub_stride = a.pub->idx_stride;
         p.pub_ready = a.pub->ready, p.pub_stop = a.pub->stop, p.pub_epoch = a.pub->epoch;
     }
-    void* f = select_kernel(sh.bits, nper_of(sh.hidden, sh.bits));
+    void* f = select_kernel(sh.bits);
     void* args[] = {&p};
     return cudaLaunchCooperativeKernel(f, dim3(s.grid), dim3(kST), args, (size_t)p.smem_bytes, st);
 }

@@ -386,6 +386,44 @@ def test_injected_faults_fail_cleanly():
         moe.moe_destroy(ctx)
 
 
+def test_device_wait_runs_out_and_reports_timeout():
+    """MOE_FAULT_DEVICE_WAIT: in the next multi-layer persistent launch one CTA
+    withholds its outputs of the first layer and every device-side wait is
+    bounded by 1 ms.  The other CTAs' waits run out, the kernel ends normally
+    (no GPU fault: the stream synchronises cleanly), the next call reports
+    MOE_ETIMEOUT and poisons the context; a fresh context then runs clean."""
+    w = dataclasses.replace(TINY, n_layers=3)
+    x = torch.from_numpy(synth.tokens(w.seed, 11, 1, w.hidden)).cuda()
+    y = torch.empty_like(x)
+    ctx = _ctx(w, max_batch=1, fault_flags=moe.MOE_FAULT_DEVICE_WAIT)
+    try:
+        moe.moe_forward_decode_stack(ctx, 0, 3, x, 1, y)  # asynchronous: the launch itself succeeds
+        torch.cuda.synchronize()
+        with pytest.raises(moe.MoeError) as e:
+            moe.moe_forward_decode_stack(ctx, 0, 3, x, 1, y)
+        assert e.value.code == moe.MOE_ETIMEOUT
+        with pytest.raises(moe.MoeError) as e:
+            moe.moe_forward_decode(ctx, 0, x, 1, y)
+        assert e.value.code == moe.MOE_ESTATE  # poisoned
+    finally:
+        moe.moe_destroy(ctx)
+    torch.cuda.synchronize()
+    fresh = _ctx(w, max_batch=1)
+    try:
+        xt = torch.empty((3, 1, w.hidden), device="cuda")
+        yt = torch.empty((3, 1, w.hidden), device="cuda")
+        it = torch.empty((3, 1, w.top_k), dtype=torch.int32, device="cuda")
+        for _ in range(2):
+            moe.moe_forward_decode_stack(fresh, 0, 3, x, 1, y, 1e-6, xt, it, yt)
+        torch.cuda.synchronize()
+        for l in range(3):
+            ref = oracle_layer(w, l).tokens(xt[l].cpu().numpy())
+            assert np.array_equal(it[l].cpu().numpy(), ref["idx"])
+            assert_close(yt[l].cpu().numpy(), ref["y"], what=f"layer {l}")
+    finally:
+        moe.moe_destroy(fresh)
+
+
 @pytest.mark.parametrize("B,bits", [(1, 4), (2, 4), (3, 4), (5, 4), (1, 8), (3, 8), (12, 4)])
 def test_stack_kernel_equals_per_layer_kernels(B, bits):
     """The persistent stack kernel (B <= 3, all resident) and the batched
