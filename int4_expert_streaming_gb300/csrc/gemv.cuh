@@ -292,20 +292,24 @@ __device__ __forceinline__ uint32_t order_key(float v) {
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-// routing weights of the k chosen logits val[] (one warp)
+// routing weights of the k chosen logits val[] (one warp): lane i < k takes
+// exp(val[i] - val[0]); the denominator is their warp butterfly sum (or, for
+// the full softmax, of every logit's exponential, lane-strided then the
+// butterfly)
 __device__ __forceinline__ void topk_weights(const float* lg, int E, int k, int norm_topk, int lane, const float* val,
                                              float* w) {
     const float m = val[0];
-    float den = 0.0f;
+    const float ei = lane < k ? __expf(__fsub_rn(val[lane], m)) : 0.0f;
+    float den;
     if (norm_topk) {
-#pragma unroll 1
-        for (int i = 0; i < k; ++i) den = __fadd_rn(den, __expf(__fsub_rn(val[i], m)));
+        den = warp_sum(ei);
     } else {
+        float d = 0.0f;
 #pragma unroll 1
-        for (int e = lane; e < E; e += 32) den = __fadd_rn(den, __expf(__fsub_rn(lg[e], m)));
-        den = warp_sum(den);
+        for (int e = lane; e < E; e += 32) d = __fadd_rn(d, __expf(__fsub_rn(lg[e], m)));
+        den = warp_sum(d);
     }
-    if (lane < k) w[lane] = __fdividef(__expf(__fsub_rn(val[lane], m)), den);
+    if (lane < k) w[lane] = __fdividef(ei, den);
     __syncwarp();
 }
 

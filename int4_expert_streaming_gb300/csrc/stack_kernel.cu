@@ -145,6 +145,17 @@ __device__ __forceinline__ bool mbar_test(uint64_t* m, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// the same test with a suspend-time hint: a thread whose phase has not
+// completed sleeps (up to `ns`) until it does, instead of spinning on issue slots
+__device__ __forceinline__ bool mbar_sleep(uint64_t* m, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(sptr(m)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* m) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                      sptr(dst)),
@@ -189,11 +200,15 @@ __device__ __forceinline__ void ll_load2(const unsigned long long* p, unsigned l
 // Polls the word pairs of rows row0 .. row0+nrows-1 of an exchange buffer
 // (row stride `stride` words, the first `cols` words of each row, cols even)
 // until every word carries epoch ep; the value of (row, col) goes to
-// dst[(row - row0) * dstride + col].  Thread i takes pairs i, i + kST, ... in
-// batches of up to four, re-issuing a batch until all of it is current.
-// Returns false (in the calling thread) on timeout or abort.
+// dst[(row - row0) * dstride + col], or with swz = CC > 0 (chunks of CC
+// columns, CC a multiple of 4) to the chunk-interleaved position
+// dst[(row - row0) * dstride + ((i / 4) * (dstride / CC) + col / CC) * 4 + i % 4],
+// i = col % CC, where the lanes that each read one chunk's float4s hit
+// consecutive addresses.  Thread i takes pairs i, i + kST, ... in batches of
+// up to four, re-issuing a batch until all of it is current.  Returns false
+// (in the calling thread) on timeout or abort.
 __device__ __forceinline__ bool poll_rows(const unsigned long long* base, int row0, int nrows, int stride, int cols,
-                                       int dstride, uint32_t ep, float* dst, const Params& p) {
+                                          int dstride, uint32_t ep, float* dst, const Params& p, int swz = 0) {
     const int half = cols >> 1, n = nrows * half;
 #pragma unroll 1
     for (int q0 = threadIdx.x; q0 < n; q0 += 4 * kST) {
@@ -203,7 +218,8 @@ __device__ __forceinline__ bool poll_rows(const unsigned long long* base, int ro
             const int q = q0 + m * kST;
             const int r = q / half, cc = 2 * (q - r * half);
             so[m] = q < n ? (row0 + r) * stride + cc : -1;
-            d0[m] = r * dstride + cc;
+            const int ci = swz ? cc % swz : 0;
+            d0[m] = r * dstride + (swz ? ((ci >> 2) * (dstride / swz) + cc / swz) * 4 + (ci & 3) : cc);
         }
         unsigned long long a[4], b[4];
         unsigned spins = 0;
@@ -238,7 +254,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* m, uint32_t parity, const Pa
     unsigned long long t0 = 0;
 #pragma unroll 1
     for (;;) {
-        if (__all_sync(kFullMask, mbar_test(m, parity))) return true;
+        if (__all_sync(kFullMask, mbar_sleep(m, parity, 20000u))) return true;
         if (!t0) t0 = gtime();
         if (__any_sync(kFullMask, spin_abort(p, spins, t0))) return false;
     }
@@ -328,7 +344,7 @@ __device__ bool stage_wait(uint64_t* mb, int i, Waits& w, const Params& p) {
     const unsigned long long t0 = gtime();
     unsigned spins = 0;
     bool ok = true;
-    while (!mbar_test(mb + i, par)) {
+    while (!mbar_sleep(mb + i, par, 20000u)) {
         if (spin_abort(p, spins, t0)) {
             ok = false;
             break;
@@ -631,41 +647,10 @@ __device__ __forceinline__ float swiglu_row(const uint8_t* gq, const uint8_t* uq
     return silu_mul(g, u);
 }
 
-// One pair's SwiGLU vector for this lane's down-row chunk, polled straight
-// from the exchange into registers (words ch*CC .. ch*CC+CC-1 of the pair's
-// row); false on timeout or abort (in every lane).
-template <int BITS>
-__device__ __forceinline__ bool poll_h_chunk(const unsigned long long* row, bool act, int ch, uint32_t ep, HF<BITS>& hd,
-                                             const Params& p) {
-    constexpr int CC = Codes<BITS>::kCols;
-    unsigned spins = 0;
-    unsigned long long t0 = 0;
-    for (;;) {
-        bool ready = true;
-        if (act) {
-#pragma unroll
-            for (int i = 0; i < CC; i += 2) {
-                unsigned long long a, b;
-                ll_load2(row + ch * CC + i, a, b);
-                ready = ready && (uint32_t)(a >> 32) == ep && (uint32_t)(b >> 32) == ep;
-                hd.v[i] = __uint_as_float((uint32_t)a);
-                hd.v[i + 1] = __uint_as_float((uint32_t)b);
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < CC; ++i) hd.v[i] = 0.0f;
-        }
-        if (__all_sync(kFullMask, ready)) return true;
-        if (!t0) t0 = gtime();
-        if (__any_sync(kFullMask, spin_abort(p, spins, t0))) return false;
-        __nanosleep(64);
-    }
-}
-
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <int BITS>
+template <int BITS, bool ONE>
 __global__ void __launch_bounds__(kST, 1) stack_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ uint64_t mbar[kNB];
@@ -673,7 +658,7 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const __grid_constant__ P
     constexpr int CC = Codes<BITS>::kCols, DW = Codes<BITS>::kDigitWords;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x, G = gridDim.x;
-    const int H = p.H, E = p.E, k = p.k, B = p.B;
+    const int H = p.H, E = p.E, k = p.k, B = ONE ? 1 : p.B;  // ONE: the batch-1 instance
     const int nc = H / CC;  // chunks of a gate/up row
     const uint32_t qb = (uint32_t)H * BITS / 8, sbb = (uint32_t)H / 16;
     Disp* ds = reinterpret_cast<Disp*>(smem + p.off_disp);
@@ -753,23 +738,34 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const __grid_constant__ P
             }
         }
         __syncthreads();
-        if (tid < B) {
-            const int t = tid;
-            float mx = ds->red[t][1][0];
+        // every thread forms r and the digit exponent of each token itself
+        // (the same bits everywhere), so no further barrier is needed before x = y * r
+        float r_t[kMaxB];
+        int xe_t[kMaxB];
+#pragma unroll
+        for (int t = 0; t < kMaxB; ++t) {
+            if (t < B) {
+                float mx = ds->red[t][1][0];
 #pragma unroll 1
-            for (int w = 1; w < kSW; ++w) mx = fmaxf(mx, ds->red[t][1][w]);
-            const float r = renorm_scale(ds->red[t][0], H, p.eps);
-            ds->rs[t] = r;
-            const float xm = l == p.layer0 ? mx : __fmul_rn(mx, r);  // max|x| = max|y| * r exactly (r > 0)
-            ds->xmax[t] = xm;
-            ds->xe[t] = bfp_exponent(xm);
+                for (int w = 1; w < kSW; ++w) mx = fmaxf(mx, ds->red[t][1][w]);
+                r_t[t] = renorm_scale(ds->red[t][0], H, p.eps);
+                const float xm = l == p.layer0 ? mx : __fmul_rn(mx, r_t[t]);  // max|x| = max|y| * r exactly (r > 0)
+                xe_t[t] = bfp_exponent(xm);
+            }
+        }
+        if (tid < B) {
+#pragma unroll
+            for (int t = 0; t < kMaxB; ++t)
+                if (t == tid) ds->rs[t] = r_t[t], ds->xe[t] = xe_t[t];
+        }
+        if (l != p.layer0) {  // x = y * r
+#pragma unroll
+            for (int t = 0; t < kMaxB; ++t)
+                if (t < B)
+#pragma unroll 1
+                    for (int i = tid; i < H; i += kST) xs[t * H + i] = __fmul_rn(xs[t * H + i], r_t[t]);
         }
         __syncthreads();
-        if (l != p.layer0) {  // x = y * r
-#pragma unroll 1
-            for (int i = tid; i < B * H; i += kST) xs[i] = __fmul_rn(xs[i], ds->rs[i / H]);
-            __syncthreads();
-        }
         if (p.x_trace && c == 0)
 #pragma unroll 1
             for (int i = tid; i < B * H; i += kST) p.x_trace[(size_t)li * B * H + i] = xs[i];
@@ -821,6 +817,7 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const __grid_constant__ P
             }
             if (warp < B) topk_merge(p, TT, ds, nlist);
         }
+        fence_proxy_async();  // the top-k scratch shares the area the copies below write
         __syncthreads();
         if (streamed) {
             // residency of the layer's experts: the same answer in every CTA
@@ -852,32 +849,80 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const __grid_constant__ P
             if (stop) break;  // the host fetches the missing experts and launches again from this layer
         }
         if (p.idx_trace && c == 0 && tid < B * k) p.idx_trace[(size_t)li * B * k + tid] = ds->idx[tid / k][tid % k];
-        if (warp == 0) dispatch(p, D, ds, l, dirs + (l & 1) * E);
-        fence_proxy_async();  // generic accesses to the copy targets precede the bulk writes below
-        __syncthreads();
-        const int n_act = ds->n_act, n_pairs = ds->n_pairs;
-        const int U = ds->n_routed * p.I;
-        const int u0 = U * c / G, u1 = U * (c + 1) / G;  // U <= 129 * 4096
+        const uint8_t* const* dir_l = dirs + (l & 1) * E;
+        int n_act, n_pairs, n_routed;
+        int el = 0x7fffffff, rk = 0;  // one token: this lane's expert (lanes < k) and its rank among the k
+        // blob of active expert a (every lane calls it; ONE: from the ranks, before the lists are visible)
+        auto blob_of = [&](int a) -> const uint8_t* {
+            if (ONE) {
+                const int src = __ffs(__ballot_sync(kFullMask, rk == a && lane < k)) - 1;
+                return dir_l[__shfl_sync(kFullMask, el, src)];
+            }
+            return D.act_blob[a];
+        };
+        if (ONE) {
+            // one token: the active experts are its k experts in ascending id
+            // and pair a is active expert a.  Every warp ranks them itself and
+            // issues its copies at once; warp 0 also writes the lists that
+            // phase C and the combine read (after later barriers).
+            n_routed = k;
+            n_act = n_pairs = k + (p.Is > 0 ? 1 : 0);
+            el = lane < k ? ds->idx[0][lane] : 0x7fffffff;
+#pragma unroll 1
+            for (int s2 = 0; s2 < k; ++s2) rk += __shfl_sync(kFullMask, el, s2) < el ? 1 : 0;
+            if (warp == 0) {
+                if (lane < k) {
+                    D.act_expert[rk] = el;
+                    D.act_blob[rk] = dir_l[el];
+                    D.act_off[rk] = rk;
+                    D.pair_token[rk] = 0;
+                    D.pair_w[rk] = ds->w[0][lane];
+                    D.pair_act[rk] = rk;
+                }
+                if (lane == 0) {
+                    if (p.Is > 0) {
+                        D.act_expert[k] = -1;
+                        D.act_blob[k] = p.shared_pool + (size_t)l * p.shared_stride;
+                        D.pair_token[k] = 0;
+                        D.pair_w[k] = ds->sig[0];
+                        D.pair_act[k] = k;
+                    }
+                    D.act_off[k] = k;
+                    D.act_off[k + 1] = k + 1;
+                }
+            }
+            const int U = k * p.I, u0 = U * c / G, u1 = U * (c + 1) / G;
+            const int mine = u1 - u0;
+            const int wu0 = u0 + mine * warp / kSW, wn = u0 + mine * (warp + 1) / kSW - wu0;
+#pragma unroll 1
+            for (int j = 0; j < min(R, wn); ++j) {
+                const int u = wu0 + j, a = u / p.I;
+                const uint8_t* blob = blob_of(a);
+                if (lane == 0) issue_unit(p, blob, u - a * p.I, wslots + (size_t)j * p.g_unit, &mbar[warp * kRing + j]);
+                warm |= 1u << j;
+            }
+        } else {
+            if (warp == 0) dispatch(p, D, ds, l, dir_l);
+            __syncthreads();
+            n_act = ds->n_act, n_pairs = ds->n_pairs, n_routed = ds->n_routed;
+            const int U = n_routed * p.I, u0 = U * c / G, u1 = U * (c + 1) / G;  // U <= 129 * 4096
+            const int mine = u1 - u0;
+            const int wu0 = u0 + mine * warp / kSW, wn = u0 + mine * (warp + 1) / kSW - wu0;
+            if (lane == 0) {
+#pragma unroll 1
+                for (int j = 0; j < min(R, wn); ++j) {
+                    const int u = wu0 + j, a = u / p.I;
+                    issue_unit(p, D.act_blob[a], u - a * p.I, wslots + (size_t)j * p.g_unit, &mbar[warp * kRing + j]);
+                }
+            }
+#pragma unroll 1
+            for (int j = 0; j < min(R, wn); ++j) warm |= 1u << j;
+        }
+        const int U = n_routed * p.I, u0 = U * c / G, u1 = U * (c + 1) / G;
         const int mine = u1 - u0;
         const int wu0 = u0 + mine * warp / kSW, wn = u0 + mine * (warp + 1) / kSW - wu0;  // this warp's units
         const int dcs = min(p.d_cap, n_act);
         const int n_dch = jn > 0 ? (n_act + dcs - 1) / dcs : 0;
-        // copies: each warp its first R units, then the last warps one down stage each
-        if (lane == 0) {
-#pragma unroll 1
-            for (int j = 0; j < min(R, wn); ++j) {
-                const int u = wu0 + j, a = u / p.I;
-                issue_unit(p, D.act_blob[a], u - a * p.I, wslots + (size_t)j * p.g_unit, &mbar[warp * kRing + j]);
-            }
-            const int s = kSW - 1 - warp;
-            if (s < min(n_dch, kNSD))
-                issue_down(p, D, s * dcs, min(n_act, (s + 1) * dcs), j0, jn, Dbuf + (size_t)s * dstage,
-                           &mbar[kMbD + s]);
-        }
-#pragma unroll 1
-        for (int j = 0; j < min(R, wn); ++j) warm |= 1u << j;
-#pragma unroll 1
-        for (int s = 0; s < min(n_dch, kNSD); ++s) wt.armed |= 1u << s;
         // the shared expert's rows of this CTA (in shared memory since the
         // previous layer) while the routed rows are in flight
 #pragma unroll 1
@@ -905,22 +950,21 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const __grid_constant__ P
                 warm &= ~(1u << s);
                 const uint8_t* st = wslots + (size_t)s * p.g_unit;
                 const int u = wu0 + j, a = u / p.I, r = u - a * p.I;
+                const int pr0 = ONE ? a : D.act_off[a], pr1 = ONE ? a + 1 : D.act_off[a + 1];
 #pragma unroll 1
-                for (int pr = D.act_off[a]; pr < D.act_off[a + 1]; ++pr) {
-                    const int t = D.pair_token[pr];
+                for (int pr = pr0; pr < pr1; ++pr) {
+                    const int t = ONE ? 0 : D.pair_token[pr];
                     const float h = swiglu_row<BITS>(st, st + qb, reinterpret_cast<const uint32_t*>(st + 2 * qb),
                                                      reinterpret_cast<const uint32_t*>(st + 2 * qb + sbb),
                                                      xdw + (size_t)t * nc * DW, xS + t * nc, ds->xe[t], nc);
                     if (lane == 0) ll_store(hll + (size_t)pr * p.h_stride + r, h, ep);
                 }
                 if (j + R < wn) {
+                    const int un = wu0 + j + R, an = un / p.I;
+                    const uint8_t* blob = blob_of(an);
                     fence_proxy_async();
                     __syncwarp();
-                    if (lane == 0) {
-                        const int un = wu0 + j + R, an = un / p.I;
-                        issue_unit(p, D.act_blob[an], un - an * p.I, wslots + (size_t)s * p.g_unit,
-                                   &mbar[warp * kRing + s]);
-                    }
+                    if (lane == 0) issue_unit(p, blob, un - an * p.I, wslots + (size_t)s * p.g_unit, &mbar[warp * kRing + s]);
                     warm |= 1u << s;
                 }
             }
@@ -930,19 +974,43 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const __grid_constant__ P
             }
         }
         // ------------------------------------------------------------ phase C
-        // Each warp takes whole pairs: it polls the pair's h straight from the
-        // exchange into registers and multiplies this CTA's down rows of the
-        // pair's expert, so the first pairs run while the last are in flight.
-        // The down stages are used in rounds of kNSD (one round when every
-        // active expert fits).
+        // The down rows are fetched now, behind the gate/up rows: they stream
+        // while the SwiGLU vectors travel between CTAs.  Then every pair's h is
+        // polled block-wide into the (idle) gate/up area, and each warp takes
+        // whole pairs: this CTA's down rows of the pair's expert.  The down
+        // stages are used in rounds of kNSD (one round when every active
+        // expert fits).
         {
+            if (lane == 0) {
+                const int s = kSW - 1 - warp;
+                if (s < min(n_dch, kNSD))
+                    issue_down(p, D, s * dcs, min(n_act, (s + 1) * dcs), j0, jn, Dbuf + (size_t)s * dstage,
+                               &mbar[kMbD + s]);
+            }
+#pragma unroll 1
+            for (int s = 0; s < min(n_dch, kNSD); ++s) wt.armed |= 1u << s;
+            const bool all_h = n_pairs * p.h_stride * 4 <= p.g_bytes;
+            float* hs = reinterpret_cast<float*>(Gbuf);  // all pairs, or the round's pairs from the first
             const int rounds = (n_dch + kNSD - 1) / kNSD;
 #pragma unroll 1
             for (int rd = 0; rd < rounds && ok; ++rd) {
                 const int aa = rd * kNSD * dcs, ab = min(n_act, aa + kNSD * dcs);
+                const int pa = D.act_off[aa], pb = D.act_off[ab];
+                const int ha = all_h ? 0 : pa, hb = all_h ? n_pairs : pb;
+                if (!all_h || rd == 0) {
+                    const int nrt = max(0, min(hb, B * k) - ha);  // routed pairs (cols I), then shared pairs (cols Is)
+                    bool okh = poll_rows(hll, ha, nrt, p.h_stride, p.I, p.h_stride, ep, hs, p, CC);
+                    if (okh && hb > ha + nrt)
+                        okh = poll_rows(hll, ha + nrt, hb - ha - nrt, p.h_stride, p.Is, p.h_stride, ep,
+                                        hs + (size_t)nrt * p.h_stride, p, CC);
+                    if (!__syncthreads_and(okh ? 1 : 0)) {
+                        ok = false;
+                        break;
+                    }
+                }
                 bool okc = true;
 #pragma unroll 1
-                for (int pr = D.act_off[aa] + warp; pr < D.act_off[ab] && okc; pr += kSW) {
+                for (int pr = pa + warp; pr < pb; pr += kSW) {
                     const int a = D.pair_act[pr];
                     const int s = (a - aa) / dcs;
                     if (!warp_wait(&mbar[kMbD + s], (wt.phase >> s) & 1u, p)) {
@@ -953,9 +1021,17 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const __grid_constant__ P
                     const bool halves = BITS == 4 && cols == 16 * CC;
                     const int ch = halves ? (lane & 15) : lane;
                     HF<BITS> hd;
-                    if (!poll_h_chunk<BITS>(hll + (size_t)pr * p.h_stride, halves || ch < cols / CC, ch, ep, hd, p)) {
-                        okc = false;
-                        break;
+                    if (halves || ch < cols / CC) {
+                        const int nch = p.h_stride / CC;  // chunk-interleaved: float4 i/4 of chunk ch
+                        const float* hrow = hs + (size_t)(pr - ha) * p.h_stride + ch * 4;
+#pragma unroll
+                        for (int i = 0; i < CC; i += 4) {
+                            const float4 v = *reinterpret_cast<const float4*>(hrow + (i >> 2) * nch * 4);
+                            hd.v[i] = v.x, hd.v[i + 1] = v.y, hd.v[i + 2] = v.z, hd.v[i + 3] = v.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < CC; ++i) hd.v[i] = 0.0f;
                     }
                     hf_sum(hd);
                     const uint32_t rb = (uint32_t)cols * BITS / 8, dsb = (uint32_t)cols / 16;
@@ -963,16 +1039,28 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const __grid_constant__ P
                     const uint8_t* sbase = unit + p.d_rows_bytes + ((j0 * dsb) & 15u);
                     const float wp = D.pair_w[pr];
                     if (halves) {
-                        // 16 chunks per row: two rows per pass, one per half-warp
+                        // 16 chunks per row: eight rows per pass as four row pairs of
+                        // half-warps, their butterflies interleaved (rows past the end
+                        // repeat the last row and are dropped)
 #pragma unroll 1
-                        for (int jj = 0; jj < jn; jj += 2) {
-                            const int j1 = min(jj + 1, jn - 1);  // an odd tail repeats its row in the upper half
-                            const float v = row_dot_h_halves<BITS>(
-                                unit + (size_t)jj * rb, reinterpret_cast<const uint32_t*>(sbase + (size_t)jj * dsb),
-                                unit + (size_t)j1 * rb, reinterpret_cast<const uint32_t*>(sbase + (size_t)j1 * dsb), hd,
-                                lane);
-                            const int jo = jj + (lane >> 4);
-                            if ((lane & 15) == 0 && jo < jn) part[(size_t)pr * p.jn + jo] = __fmul_rn(wp, v);
+                        for (int jj = 0; jj < jn; jj += 8) {
+                            const uint8_t* q8[8];
+                            const uint32_t* sb8[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const int jr = min(jj + i, jn - 1);
+                                q8[i] = unit + (size_t)jr * rb;
+                                sb8[i] = reinterpret_cast<const uint32_t*>(sbase + (size_t)jr * dsb);
+                            }
+                            float v[4];
+                            row_dot_h_halves_n<BITS, 4>(q8, sb8, hd, lane, v);
+                            if ((lane & 15) == 0) {
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const int jo = jj + 2 * i + (lane >> 4);
+                                    if (jo < jn) part[(size_t)pr * p.jn + jo] = __fmul_rn(wp, v[i]);
+                                }
+                            }
                         }
                     } else {
 #pragma unroll 1
@@ -1116,9 +1204,9 @@ bool plan(const Shapes& sh, int B, int grid, int max_smem, Params& p) {
     return off <= budget;
 }
 
-void* select_kernel(int bits) {
-    if (bits == 4) return reinterpret_cast<void*>(&stack_kernel<4>);
-    if (bits == 8) return reinterpret_cast<void*>(&stack_kernel<8>);
+void* select_kernel(int bits, bool one) {
+    if (bits == 4) return one ? reinterpret_cast<void*>(&stack_kernel<4, true>) : reinterpret_cast<void*>(&stack_kernel<4, false>);
+    if (bits == 8) return one ? reinterpret_cast<void*>(&stack_kernel<8, true>) : reinterpret_cast<void*>(&stack_kernel<8, false>);
     return nullptr;
 }
 
@@ -1162,12 +1250,13 @@ int stack_alloc(StackScratch& s, const Shapes& sh, int n_layers, int max_batch, 
         err = "stack scratch initialisation failed";
         return MOE_ECUDA;
     }
-    if (void* f = select_kernel(sh.bits)) {
-        if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, s.max_smem - 1024) != cudaSuccess) {
-            cudaGetLastError();
-            s.grid = 0;  // persistent kernel unavailable; per-layer kernels serve the stack
+    for (int one = 0; one < 2; ++one)
+        if (void* f = select_kernel(sh.bits, one != 0)) {
+            if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, s.max_smem - 1024) != cudaSuccess) {
+                cudaGetLastError();
+                s.grid = 0;  // persistent kernel unavailable; per-layer kernels serve the stack
+            }
         }
-    }
     return MOE_OK;
 }
 
@@ -1185,7 +1274,7 @@ bool stack_supported(const Shapes& sh, const StackScratch& s, int B) {
     if (s.grid <= 0 || !s.lg_ll || B < 1 || B > kMaxB || sh.hidden > 2048 || sh.top_k > 16) return false;
     if (sh.n_experts > 2 * kST) return false;  // two keys per lane in the first top-k level
     if (sh.n_experts % 2) return false;        // directory rows are bulk-copied: 16-byte aligned rows
-    if (!select_kernel(sh.bits)) return false;
+    if (!select_kernel(sh.bits, B == 1)) return false;
     const int cmax = std::max(sh.inter, sh.shared_inter);
     if (cmax * sh.bits / 128 > 32) return false;  // one chunk per lane on down rows
     Params p{};
@@ -1215,7 +1304,7 @@ cudaError_t launch_stack(const Shapes& sh, StackScratch& s, const StackArgs& a, 
         p.pub_idx = a.pub->idx, p.pub_stride = a.pub->idx_stride;
         p.pub_ready = a.pub->ready, p.pub_stop = a.pub->stop, p.pub_epoch = a.pub->epoch;
     }
-    void* f = select_kernel(sh.bits);
+    void* f = select_kernel(sh.bits, a.B == 1);
     void* args[] = {&p};
     return cudaLaunchCooperativeKernel(f, dim3(s.grid), dim3(kST), args, (size_t)p.smem_bytes, st);
 }
