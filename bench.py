@@ -32,9 +32,9 @@ import synth  # noqa: E402
 METRIC = "MoE-stack decode tok/s; expert-weight HBM GB/s as fraction of GB300 peak"
 FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) of one decode-stack launch per layer: an ncu capture
-# of the 35B-shaped int4 stack at batch 1 (4 layers, 68.064512 + 1.394432 MB),
+# of the 35B-shaped int4 stack at batch 1 (4 layers, 68.027136 + 0.643328 MB),
 # scaled by the layer count; valid for that workload and the current kernel
-STACK_35B_DRAM_BYTES_PER_LAYER = 69.458944e6 / 4
+STACK_35B_DRAM_BYTES_PER_LAYER = 68.670464e6 / 4
 FALLBACK_BF16_TFLOPS = 1700.0
 PREFILL_METRIC = "MoE prefill tok/s; grouped-GEMM bf16 TFLOP/s as fraction of GB300 dense peak"
 
@@ -53,6 +53,8 @@ def parse_args():
     ap.add_argument("--cpu-samples", type=int, default=64, help="(token, layer) samples of the oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-subrecords", action="store_true",
+                    help="default run: skip the 80B decode (B = 1, 8, 64) and 80B prefill sub-records")
     ap.add_argument("--slots", type=int, default=0, help="stress: slots per layer (default: the workload's 128)")
     ap.add_argument("--policy", default="lfu", choices=list(POLICIES), help="stress: eviction policy")
     ap.add_argument("--aging", type=int, default=64, help="stress: calls between halvings of the aged LFU")
@@ -83,14 +85,15 @@ def peaks():
 
 
 def tensor_peak():
-    """Dense bf16 TFLOP/s for a kernel timed inside a long loop (sustained figure)."""
+    """Dense bf16 TFLOP/s, burst figure: the grouped GEMMs run a few hundred
+    microseconds inside a step of about a millisecond, not a seconds-long loop."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        if "bf16_tflops_sustained" in d:
-            return float(d["bf16_tflops_sustained"]), "measured (sustained)"
         if "bf16_tflops" in d:
             return float(d["bf16_tflops"]), "measured (burst)"
+        if "bf16_tflops_sustained" in d:
+            return float(d["bf16_tflops_sustained"]), "measured (sustained)"
     return FALLBACK_BF16_TFLOPS, "fallback"
 
 
@@ -235,6 +238,107 @@ def run_reference(args):
 # --------------------------------------------------------------------------
 # our path
 # --------------------------------------------------------------------------
+def decode_record(moe, ctx, w, bits, B, steps, warmup, local, pg, world, e2e_steps=0):
+    """Time `steps` decode-stack steps of B tokens (inputs resident in HBM,
+    CUDA events on the launching stream) on a loaded context; returns the
+    measurement fields of a line: value, ms_per_step, roofline, clocks, launches."""
+    import torch
+
+    L, H, k = w.n_layers, w.hidden, w.top_k
+    n_ring = 256
+    X = torch.from_numpy(np.stack([synth.tokens(w.seed, s, B, H) for s in range(n_ring)])).cuda()
+    y = torch.empty((B, H), device="cuda")
+    st = torch.cuda.current_stream()
+    # expert bytes actually read per step: (distinct routed experts + shared) x blob bytes, per layer
+    blob = moe.moe_blob_bytes(H, w.inter, bits)
+    sblob = moe.moe_blob_bytes(H, w.shared_inter, bits) if w.shared_inter else 0
+    it = torch.empty((L, B, k), dtype=torch.int32, device="cuda")
+    uniq = []
+    for s in range(min(n_ring, 32)):
+        moe.moe_forward_decode_stack(ctx, 0, L, X[s], B, y, 1e-6, None, it, None, st)
+        idx = it.cpu().numpy()
+        uniq.append(sum(len(np.unique(idx[l])) for l in range(L)))
+    expert_bytes = float(np.mean(uniq)) * blob + L * sblob
+    router_bytes = L * w.n_experts * H * 2
+    for s in range(warmup):
+        moe.moe_forward_decode_stack(ctx, 0, L, X[s % n_ring], B, y, 1e-6, None, None, None, st)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    l0 = moe.moe_launch_count(ctx)
+    clk = ClockSampler(local)
+    clk.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(st)
+    for s in range(steps):
+        moe.moe_forward_decode_stack(ctx, 0, L, X[s % n_ring], B, y, 1e-6, None, None, None, st)
+    e1.record(st)
+    torch.cuda.synchronize()
+    clocks = clk.stop()
+    launches = moe.moe_launch_count(ctx) - l0
+    ms = max_over_ranks(e0.elapsed_time(e1), pg)
+    secs = ms / 1e3
+    gbs = expert_bytes * steps / secs / 1e9
+    peak, peak_kind = peaks()
+    traffic = (STACK_35B_DRAM_BYTES_PER_LAYER * L
+               if (w.name, B, bits, w.hidden, w.n_experts) == ("35b", 1, 4, 2048, 256) else None)
+    rec = {
+        "value": steps * B * world / secs, "unit": "tok/s", "ms_per_step": ms / steps, "steps": steps,
+        "warmup": warmup, "batch": B,
+        "expert_gbs": gbs, "hbm_frac": gbs / peak,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                     "peak_kind": peak_kind, "traffic": traffic,
+                     "traffic_unit": "DRAM bytes per launch (ncu, 4-layer capture scaled by layers)",
+                     "kernel": ("decode stack (one persistent forward_decode_stack launch per step)" if launches == steps
+                                else "decode stack (per-layer kernels, one forward_decode_stack call per step)"),
+                     "bytes_per_launch": expert_bytes, "router_bytes_per_launch": router_bytes},
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+    }
+    if e2e_steps:
+        # end to end through the public API with host buffers: pinned H2D of the
+        # step's tokens, the stack, D2H of the step's output, every step
+        xh = torch.from_numpy(np.stack([synth.tokens(w.seed, s, B, H) for s in range(n_ring)])).pin_memory()
+        yh = torch.empty((B, H)).pin_memory()
+        xd = torch.empty((B, H), device="cuda")
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for s in range(e2e_steps):
+            xd.copy_(xh[s % n_ring], non_blocking=True)
+            moe.moe_forward_decode_stack(ctx, 0, L, xd, B, y, 1e-6, None, None, None, st)
+            yh.copy_(y, non_blocking=True)
+            st.synchronize()
+        e2e_s = time.perf_counter() - t0
+        rec["e2e"] = {"value": e2e_steps * B * world / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": B * H * 4,
+                      "d2h_bytes_per_step": B * H * 4, "steps": e2e_steps}
+    return rec
+
+
+def subrecords(args, moe, workload, local, pg, world):
+    """The other single-GPU workloads as sub-records of the default line: the
+    80B decode stack at 1, 8 and 64 tokens, then the 80B prefill layer."""
+    out = []
+    w = synth.CONFIGS["80b"]
+    ctx = workload.create_loaded(w, w.bits, max_batch=max(w.batches))
+    try:
+        for B in w.batches:
+            rec = decode_record(moe, ctx, w, w.bits, B, args.steps, max(args.warmup, 3), local, pg, world)
+            rec = {"metric": METRIC, "workload": workload_desc(w, B, w.bits), **rec}
+            out.append(rec)
+    finally:
+        moe.moe_destroy(ctx)
+    wp = synth.CONFIGS["80b-prefill"]
+    ctx = workload.create_loaded(wp, wp.bits, max_tokens=wp.prefill_tokens)
+    try:
+        rec = prefill_record(moe, ctx, wp, wp.bits, wp.prefill_tokens, args.steps, max(args.warmup, 3), local, pg,
+                             world)
+        out.append({"metric": PREFILL_METRIC, "workload": prefill_desc(wp, wp.prefill_tokens, wp.bits), **rec})
+    finally:
+        moe.moe_destroy(ctx)
+    return out
+
+
 def run_ours(args):
     import torch
 
@@ -253,93 +357,37 @@ def run_ours(args):
         w = dataclasses.replace(w, n_layers=args.layers)
     bits = args.bits or w.bits
     B = args.batch
-    L, H, k = w.n_layers, w.hidden, w.top_k
+    L = w.n_layers
     moe.build()
     ctx = workload.create_loaded(w, bits, max_batch=B)
     try:
-        n_ring = 256
-        X = torch.from_numpy(np.stack([synth.tokens(w.seed, s, B, H) for s in range(n_ring)])).cuda()
-        y = torch.empty((B, H), device="cuda")
-        st = torch.cuda.current_stream()
-        # expert bytes actually read per step: (distinct routed experts + shared) x blob bytes, per layer
-        blob = moe.moe_blob_bytes(H, w.inter, bits)
-        sblob = moe.moe_blob_bytes(H, w.shared_inter, bits) if w.shared_inter else 0
-        it = torch.empty((L, B, k), dtype=torch.int32, device="cuda")
-        uniq = []
-        for s in range(min(n_ring, 32)):
-            moe.moe_forward_decode_stack(ctx, 0, L, X[s], B, y, 1e-6, None, it, None, st)
-            idx = it.cpu().numpy()
-            uniq.append(sum(len(np.unique(idx[l])) for l in range(L)))
-        expert_bytes = float(np.mean(uniq)) * blob + L * sblob
-        router_bytes = L * w.n_experts * H * 2
-        for s in range(args.warmup):
-            moe.moe_forward_decode_stack(ctx, 0, L, X[s % n_ring], B, y, 1e-6, None, None, None, st)
-        torch.cuda.synchronize()
-        if pg:
-            pg.barrier()
-        l0 = moe.moe_launch_count(ctx)
-        clk = ClockSampler(local)
-        clk.start()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        e0.record(st)
-        for s in range(args.steps):
-            moe.moe_forward_decode_stack(ctx, 0, L, X[s % n_ring], B, y, 1e-6, None, None, None, st)
-        e1.record(st)
-        torch.cuda.synchronize()
-        clocks = clk.stop()
-        launches = moe.moe_launch_count(ctx) - l0
-        ms = e0.elapsed_time(e1)
-        ms = max_over_ranks(ms, pg)
-        secs = ms / 1e3
-        value = args.steps * B * world / secs
-        gbs = expert_bytes * args.steps / secs / 1e9
-        peak, peak_kind = peaks()
-        # end to end through the public API with host buffers: pinned H2D of the
-        # step's tokens, the stack, D2H of the step's output, every step
-        e2e = None
-        if not args.no_e2e:
-            xh = torch.from_numpy(np.stack([synth.tokens(w.seed, s, B, H) for s in range(n_ring)])).pin_memory()
-            yh = torch.empty((B, H)).pin_memory()
-            xd = torch.empty((B, H), device="cuda")
-            n_e2e = min(args.steps, 512)
-            torch.cuda.synchronize()
-            t0 = time.perf_counter()
-            for s in range(n_e2e):
-                xd.copy_(xh[s % n_ring], non_blocking=True)
-                moe.moe_forward_decode_stack(ctx, 0, L, xd, B, y, 1e-6, None, None, None, st)
-                yh.copy_(y, non_blocking=True)
-                st.synchronize()
-            e2e_s = time.perf_counter() - t0
-            e2e = {"value": n_e2e * B * world / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": B * H * 4,
-                   "d2h_bytes_per_step": B * H * 4, "steps": n_e2e}
-        line = {
-            "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": workload_desc(w, B, bits), "batch": B, "layers": L, "bits": bits,
-                       "parallelism": "replicas" if world > 1 else "single-gpu",
-                       "l2": f"inputs larger than L2: {expert_bytes / 1e6:.1f} MB of expert weights per step"},
-            "expert_gbs": gbs, "hbm_frac": gbs / peak,
-            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
-                         "peak_kind": peak_kind,
-                         "traffic": (STACK_35B_DRAM_BYTES_PER_LAYER * L
-                                     if (w.name, B, bits, w.hidden, w.n_experts) == ("35b", 1, 4, 2048, 256) else None),
-                         "traffic_unit": "DRAM bytes per launch (ncu, 4-layer capture scaled by layers)",
-                         "kernel": "decode stack (one forward_decode_stack call per step)",
-                         "bytes_per_launch": expert_bytes, "router_bytes_per_launch": router_bytes},
-            "gpu_launches": int(launches),
-            "clocks": clocks,
-            "e2e": e2e,
-        }
-        if rank == 0 and world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(w, bits, args.cpu_samples)
-        if rank == 0:
-            print(json.dumps(line), flush=True)
+        rec = decode_record(moe, ctx, w, bits, B, args.steps, args.warmup, local, pg, world,
+                            e2e_steps=0 if args.no_e2e else min(args.steps, 512))
     finally:
         moe.moe_destroy(ctx)
-        if pg:
-            pg.destroy_process_group()
+    line = {
+        "metric": METRIC, "value": rec["value"], "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": rec["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": workload_desc(w, B, bits), "batch": B, "layers": L, "bits": bits,
+                   "parallelism": "replicas" if world > 1 else "single-gpu",
+                   "l2": f"inputs larger than L2: {rec['roofline']['bytes_per_launch'] / 1e6:.1f} MB of expert "
+                         "weights per step"},
+        "expert_gbs": rec["expert_gbs"], "hbm_frac": rec["hbm_frac"],
+        "roofline": rec["roofline"],
+        "gpu_launches": rec["gpu_launches"],
+        "clocks": rec["clocks"],
+        "e2e": rec.get("e2e"),
+    }
+    default_run = (args.config == "35b" and not args.layers and not args.bits and B == 1)
+    if default_run and not args.no_subrecords:
+        line["configs"] = subrecords(args, moe, workload, local, pg, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, bits, args.cpu_samples)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
 
 
 # --------------------------------------------------------------------------
@@ -371,6 +419,72 @@ def prefill_cpu_baseline(w, bits, n_tokens):
                       f"bf16 weights and x), split over {threads} host threads; {secs:.1f} s wall"}
 
 
+def prefill_record(moe, ctx, w, bits, T, steps, warmup, local, pg, world, e2e_steps=0):
+    """Time `steps` prefill calls of T tokens on a loaded context (CUDA events),
+    with per-kernel device times; returns the measurement fields of a line."""
+    import torch
+
+    H, k = w.hidden, w.top_k
+    n_ring = 5  # 5 x T x H fp32 inputs: larger than L2 at the workload's T
+    X = torch.from_numpy(np.stack([synth.tokens(w.seed, s, T, H) for s in range(n_ring)])).cuda()
+    y = torch.empty((T, H), device="cuda")
+    st = torch.cuda.current_stream()
+    flop = 2.0 * T * k * 3 * H * w.inter + 2.0 * T * 3 * H * w.shared_inter
+    for s in range(warmup):
+        moe.moe_forward_prefill(ctx, 0, X[s % n_ring], T, y, None, None, st)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    moe.moe_prefill_profile(ctx, True)
+    l0 = moe.moe_launch_count(ctx)
+    clk = ClockSampler(local)
+    clk.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(st)
+    for s in range(steps):
+        moe.moe_forward_prefill(ctx, 0, X[s % n_ring], T, y, None, None, st)
+    e1.record(st)
+    torch.cuda.synchronize()
+    clocks = clk.stop()
+    launches = moe.moe_launch_count(ctx) - l0
+    kms, calls = moe.moe_prefill_kernel_ms(ctx)
+    moe.moe_prefill_profile(ctx, False)
+    ms = max_over_ranks(e0.elapsed_time(e1), pg)
+    secs = ms / 1e3
+    per_kernel = {n: v / calls for n, v in kms.items()}
+    gemm_ms = per_kernel["gateup_gemm"] + per_kernel["down_gemm"]
+    peak, peak_kind = tensor_peak()
+    achieved = flop / (gemm_ms / 1e3) / 1e12
+    rec = {
+        "value": steps * T * world / secs, "unit": "tok/s", "ms_per_step": ms / steps, "steps": steps,
+        "warmup": warmup, "tokens": T,
+        "layer_tflops": flop / secs * steps / 1e12,
+        "kernel_ms": per_kernel,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": None,
+                     "kernel": "grouped GEMMs (gate/up + down), algorithmic FLOPs 2*T*k*3*H*I + 2*T*3*H*I_s",
+                     "flops_per_launch": flop, "ms_per_launch": gemm_ms},
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+    }
+    if e2e_steps:
+        xh = torch.from_numpy(np.stack([synth.tokens(w.seed, s, T, H) for s in range(2)])).pin_memory()
+        yh = torch.empty((T, H)).pin_memory()
+        xd = torch.empty((T, H), device="cuda")
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for s in range(e2e_steps):
+            xd.copy_(xh[s % 2], non_blocking=True)
+            moe.moe_forward_prefill(ctx, 0, xd, T, y, None, None, st)
+            yh.copy_(y, non_blocking=True)
+            st.synchronize()
+        e2e_s = time.perf_counter() - t0
+        rec["e2e"] = {"value": e2e_steps * T * world / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": T * H * 4,
+                      "d2h_bytes_per_step": T * H * 4, "steps": e2e_steps}
+    return rec
+
+
 def run_prefill(args):
     import torch
 
@@ -387,76 +501,25 @@ def run_prefill(args):
     w = synth.CONFIGS[args.config]
     bits = args.bits or w.bits
     T = args.tokens or w.prefill_tokens
-    H, k = w.hidden, w.top_k
     moe.build()
     ctx = workload.create_loaded(w, bits, max_tokens=T)
     try:
-        n_ring = 5  # 5 x T x H fp32 inputs: larger than L2 at the workload's T
-        X = torch.from_numpy(np.stack([synth.tokens(w.seed, s, T, H) for s in range(n_ring)])).cuda()
-        y = torch.empty((T, H), device="cuda")
-        st = torch.cuda.current_stream()
-        flop = 2.0 * T * k * 3 * H * w.inter + 2.0 * T * 3 * H * w.shared_inter
-        for s in range(args.warmup):
-            moe.moe_forward_prefill(ctx, 0, X[s % n_ring], T, y, None, None, st)
-        torch.cuda.synchronize()
-        if pg:
-            pg.barrier()
-        moe.moe_prefill_profile(ctx, True)
-        l0 = moe.moe_launch_count(ctx)
-        clk = ClockSampler(local)
-        clk.start()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        e0.record(st)
-        for s in range(args.steps):
-            moe.moe_forward_prefill(ctx, 0, X[s % n_ring], T, y, None, None, st)
-        e1.record(st)
-        torch.cuda.synchronize()
-        clocks = clk.stop()
-        launches = moe.moe_launch_count(ctx) - l0
-        kms, calls = moe.moe_prefill_kernel_ms(ctx)
-        moe.moe_prefill_profile(ctx, False)
-        ms = e0.elapsed_time(e1)
-        ms = max_over_ranks(ms, pg)
-        secs = ms / 1e3
-        value = args.steps * T * world / secs
-        per_kernel = {n: v / calls for n, v in kms.items()}
-        gemm_ms = per_kernel["gateup_gemm"] + per_kernel["down_gemm"]
-        peak, peak_kind = tensor_peak()
-        achieved = flop / (gemm_ms / 1e3) / 1e12
-        e2e = None
-        if not args.no_e2e:
-            xh = torch.from_numpy(np.stack([synth.tokens(w.seed, s, T, H) for s in range(2)])).pin_memory()
-            yh = torch.empty((T, H)).pin_memory()
-            xd = torch.empty((T, H), device="cuda")
-            n_e2e = min(args.steps, 32)
-            torch.cuda.synchronize()
-            t0 = time.perf_counter()
-            for s in range(n_e2e):
-                xd.copy_(xh[s % 2], non_blocking=True)
-                moe.moe_forward_prefill(ctx, 0, xd, T, y, None, None, st)
-                yh.copy_(y, non_blocking=True)
-                st.synchronize()
-            e2e_s = time.perf_counter() - t0
-            e2e = {"value": n_e2e * T * world / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": T * H * 4,
-                   "d2h_bytes_per_step": T * H * 4, "steps": n_e2e}
+        rec = prefill_record(moe, ctx, w, bits, T, args.steps, args.warmup, local, pg, world,
+                             e2e_steps=0 if args.no_e2e else min(args.steps, 32))
         line = {
-            "metric": PREFILL_METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "metric": PREFILL_METRIC, "value": rec["value"], "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": rec["ms_per_step"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": prefill_desc(w, T, bits), "tokens": T, "bits": bits,
                        "parallelism": "replicas" if world > 1 else "single-gpu",
                        "l2": "inputs larger than L2: 5 rotating token batches of "
-                             f"{T * H * 4 / 1e6:.1f} MB plus the touched experts' weights"},
-            "layer_tflops": flop / secs * args.steps / 1e12,
-            "kernel_ms": per_kernel,
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "peak_kind": peak_kind, "traffic": None,
-                         "kernel": "grouped GEMMs (gate/up + down), algorithmic FLOPs 2*T*k*3*H*I + 2*T*3*H*I_s",
-                         "flops_per_launch": flop, "ms_per_launch": gemm_ms},
-            "gpu_launches": int(launches),
-            "clocks": clocks,
-            "e2e": e2e,
+                             f"{T * w.hidden * 4 / 1e6:.1f} MB plus the touched experts' weights"},
+            "layer_tflops": rec["layer_tflops"],
+            "kernel_ms": rec["kernel_ms"],
+            "roofline": rec["roofline"],
+            "gpu_launches": rec["gpu_launches"],
+            "clocks": rec["clocks"],
+            "e2e": rec.get("e2e"),
         }
         if rank == 0 and world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = prefill_cpu_baseline(w, bits, 16)
