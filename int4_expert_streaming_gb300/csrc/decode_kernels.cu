@@ -348,17 +348,24 @@ __global__ void __launch_bounds__(kThreads, 2) gateup_batched_kernel(Shapes s, D
 }
 
 // ---------------------------------------------------------------------------
-// batched down: a CTA per (active expert, kDnRows output rows); for each of
-// the expert's pairs, weighted row dots into part[pair][row]
+// batched down: a CTA per (work item, kDnRows output rows); for each of the
+// item's pairs, weighted row dots into part[pair][row].  The item's h rows are
+// staged once per CTA in a chunk-interleaved layout (float4 i/4 of chunk c at
+// [(i/4) * nch + c], so the lanes that each read one chunk hit consecutive
+// addresses), with each chunk's sum (hf_sum's order) formed once per CTA.
+// int4 rows of 16 chunks: each warp keeps the codes of 8 rows (4 half-warp
+// row pairs) in registers for all of the item's pairs and interleaves their
+// butterflies; other shapes: one row at a time (row_dot_h).
 // ---------------------------------------------------------------------------
 constexpr int kDnRows = 64;
 
 template <int BITS>
 __global__ void __launch_bounds__(kThreads, 2) down_batched_kernel(Shapes s, Dispatch d, const float* __restrict__ h,
                                                                 float* __restrict__ part) {
-    constexpr int CC = Codes<BITS>::kCols, CPG = 64 / CC, RW = kDnRows / kNWarps;
-    static_assert(RW == 8, "eight rows per warp: four half-warp passes");
-    __shared__ __align__(16) float hs[kWorkPairs][1024];  // the item's h rows (cols <= 1024)
+    constexpr int CC = Codes<BITS>::kCols, CPG = 64 / CC, RW = kDnRows / kNWarps, NP = RW / 2;
+    static_assert(RW == 8, "eight rows per warp: four half-warp row pairs");
+    __shared__ __align__(16) float hs[kWorkPairs][1024];  // the item's h rows (cols <= 1024), chunk-interleaved
+    __shared__ float hsum[kWorkPairs][64];                // per-chunk sums of h (<= 64 chunks)
     if ((int)blockIdx.y >= *d.n_work) return;
     const int4 wi = d.work[blockIdx.y];
     const int a = wi.x, pg = wi.y, n = wi.z;
@@ -366,57 +373,77 @@ __global__ void __launch_bounds__(kThreads, 2) down_batched_kernel(Shapes s, Dis
     const int H = s.hidden;
     const bool shared = d.act_expert[a] < 0;
     const int cols = shared ? s.shared_inter : s.inter;
+    const int nch = cols / CC;
     const BlobLayout L = blob_layout(H, cols, BITS);
     const uint8_t* blob = d.act_blob[a];
     const size_t row_bytes = (size_t)cols * BITS / 8;
     const int ng = cols / 64;
     const int jb = blockIdx.x * kDnRows + warp * RW;
+    const bool pairs16 = BITS == 4 && nch == 16 && jb + RW <= H;
+    // this warp's codes first (the longest latency), then the staging
+    uint4 q[NP];
+    uint32_t sb[NP];
+    const int c16 = lane & 15, hi = lane >> 4;
+    if (pairs16) {
+#pragma unroll
+        for (int i = 0; i < NP; ++i) {
+            const int j = jb + 2 * i + hi;
+            q[i] = __ldg(reinterpret_cast<const uint4*>(blob + L.down_q + j * row_bytes) + c16);
+            sb[i] = __ldg(reinterpret_cast<const uint32_t*>(blob + L.down_sb) + (size_t)j * ng + c16 / CPG);
+        }
+    }
     for (int i = threadIdx.x; i < n * cols / 4; i += kThreads) {
-        const int j = i / (cols / 4), o = i - j * (cols / 4);
-        reinterpret_cast<float4*>(hs[j])[o] = reinterpret_cast<const float4*>(h + (size_t)(pg + j) * s.h_stride)[o];
+        const int j = i / (cols / 4), o = i - j * (cols / 4);  // float4 o of pair j: chunk o*4/CC, element (o*4)%CC
+        const float4 v = reinterpret_cast<const float4*>(h + (size_t)(pg + j) * s.h_stride)[o];
+        const int cc = (o * 4) / CC, e4 = ((o * 4) % CC) >> 2;
+        reinterpret_cast<float4*>(hs[j])[e4 * nch + cc] = v;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < n * nch; i += kThreads) {
+        const int j = i / nch, cc = i - j * nch;
+        float sum = hs[j][cc * 4];
+#pragma unroll 1
+        for (int e = 1; e < CC; ++e) sum = __fadd_rn(sum, hs[j][((e >> 2) * nch + cc) * 4 + (e & 3)]);
+        hsum[j][cc] = sum;
     }
     __syncthreads();
     if (jb >= H) return;
     const int je = min(H, jb + RW);
-    if (BITS == 4 && cols == 16 * CC && je - jb == RW) {
-        // rows jb + 2i (lanes 0-15) and jb + 2i + 1 (lanes 16-31): this lane's code chunk and
-        // scale/bias word of each, kept in registers for all of the item's pairs
-        const int c = lane & 15, hi = lane >> 4;
-        uint4 q[RW / 2];
-        uint32_t sb[RW / 2];
-#pragma unroll
-        for (int i = 0; i < RW / 2; ++i) {
-            const int j = jb + 2 * i + hi;
-            q[i] = __ldg(reinterpret_cast<const uint4*>(blob + L.down_q + j * row_bytes) + c);
-            sb[i] = __ldg(reinterpret_cast<const uint32_t*>(blob + L.down_sb) + (size_t)j * ng + c / CPG);
-        }
+    if (pairs16) {
         for (int p = 0; p < n; ++p) {
             HF<BITS> hd;
 #pragma unroll
             for (int i = 0; i < CC; i += 4) {
-                const float4 f = *reinterpret_cast<const float4*>(&hs[p][c * CC + i]);
+                const float4 f = reinterpret_cast<const float4*>(hs[p])[(i >> 2) * nch + c16];
                 hd.v[i] = f.x, hd.v[i + 1] = f.y, hd.v[i + 2] = f.z, hd.v[i + 3] = f.w;
             }
-            hf_sum(hd);
+            hd.s = hsum[p][c16];
             // row_dot_h_halves of the four row pairs, butterflies interleaved
-            float v[RW / 2];
+            float v[NP];
 #pragma unroll
-            for (int i = 0; i < RW / 2; ++i) v[i] = chunk_term_f<BITS>(chunk_dot_f(q[i], hd.v, Codes<BITS>{}), hd.s, sb[i]);
+            for (int i = 0; i < NP; ++i) v[i] = chunk_term_f<BITS>(chunk_dot_f(q[i], hd.v, Codes<BITS>{}), hd.s, sb[i]);
 #pragma unroll
             for (int off = 8; off >= 1; off >>= 1)
 #pragma unroll
-                for (int i = 0; i < RW / 2; ++i) v[i] = __fadd_rn(v[i], __shfl_xor_sync(kFullMask, v[i], off));
-            if (c == 0) {
+                for (int i = 0; i < NP; ++i) v[i] = __fadd_rn(v[i], __shfl_xor_sync(kFullMask, v[i], off));
+            if (c16 == 0) {
                 const float wp = d.pair_w[pg + p];
                 float* out = part + (size_t)(pg + p) * H + jb + hi;
 #pragma unroll
-                for (int i = 0; i < RW / 2; ++i) out[2 * i] = __fmul_rn(wp, v[i]);
+                for (int i = 0; i < NP; ++i) out[2 * i] = __fmul_rn(wp, v[i]);
             }
         }
     } else {
         for (int p = 0; p < n; ++p) {
             HF<BITS> hd;
-            load_hf<BITS>(hs[p], cols, lane, hd);
+            const bool mine = lane < nch;
+#pragma unroll
+            for (int i = 0; i < CC; i += 4) {
+                const float4 f = mine ? reinterpret_cast<const float4*>(hs[p])[(i >> 2) * nch + lane]
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+                hd.v[i] = f.x, hd.v[i + 1] = f.y, hd.v[i + 2] = f.z, hd.v[i + 3] = f.w;
+            }
+            hd.s = mine ? hsum[p][lane] : 0.0f;
             const float wp = d.pair_w[pg + p];
             float* out = part + (size_t)(pg + p) * H;
             for (int j = jb; j < je; ++j) {
