@@ -421,6 +421,12 @@ __device__ __forceinline__ uint32_t nib_pair(uint32_t w, int shift) {
     return ((w >> shift) & 0x000f000fu) | 0x43004300u;
 }
 
+// 128 + (byte b of x) as a float, for a byte below 16: byte b goes to bits 16..23
+// under the exponent byte of 128.0 (the bits of bf16_pair_lo(nib_pair(...)))
+__device__ __forceinline__ float q128(uint32_t x, int b) {
+    return __uint_as_float(__byte_perm(x, 0x43000000u, 0x7044u | ((unsigned)b << 8)));
+}
+
 // sum over the chunk of (128 + q_c) * h_c
 __device__ __forceinline__ float chunk_dot_f(uint4 v, const float* h, Codes<4>) {
     const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
@@ -428,16 +434,17 @@ __device__ __forceinline__ float chunk_dot_f(uint4 v, const float* h, Codes<4>) 
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const float* hw = h + 8 * i;
-        const uint32_t t0 = nib_pair(wd[i], 0), t1 = nib_pair(wd[i], 4), t2 = nib_pair(wd[i], 8),
-                       t3 = nib_pair(wd[i], 12);
-        float s = __fmul_rn(bf16_pair_lo(t0), hw[0]);
-        s = __fmaf_rn(bf16_pair_hi(t0), hw[4], s);
-        s = __fmaf_rn(bf16_pair_lo(t1), hw[1], s);
-        s = __fmaf_rn(bf16_pair_hi(t1), hw[5], s);
-        s = __fmaf_rn(bf16_pair_lo(t2), hw[2], s);
-        s = __fmaf_rn(bf16_pair_hi(t2), hw[6], s);
-        s = __fmaf_rn(bf16_pair_lo(t3), hw[3], s);
-        s = __fmaf_rn(bf16_pair_hi(t3), hw[7], s);
+        // even codes (columns 0, 2, 4, 6 of the word) and odd codes, one per byte;
+        // one byte permute then places a code in the mantissa of 128.0 (128 + q)
+        const uint32_t ev = wd[i] & 0x0f0f0f0fu, od = (wd[i] >> 4) & 0x0f0f0f0fu;
+        float s = __fmul_rn(q128(ev, 0), hw[0]);
+        s = __fmaf_rn(q128(ev, 2), hw[4], s);
+        s = __fmaf_rn(q128(od, 0), hw[1], s);
+        s = __fmaf_rn(q128(od, 2), hw[5], s);
+        s = __fmaf_rn(q128(ev, 1), hw[2], s);
+        s = __fmaf_rn(q128(ev, 3), hw[6], s);
+        s = __fmaf_rn(q128(od, 1), hw[3], s);
+        s = __fmaf_rn(q128(od, 3), hw[7], s);
         a[i] = s;
     }
     return __fadd_rn(__fadd_rn(a[0], a[1]), __fadd_rn(a[2], a[3]));
