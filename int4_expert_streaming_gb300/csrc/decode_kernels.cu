@@ -79,6 +79,133 @@ __device__ void token_digits(const float* x, int H, int lane, uint32_t* words, i
     if (lane == 0) *expo = e;
 }
 
+// Routing of one token per CTA of kRtThreads threads: top-k of its logits
+// (each warp the k best of its 32-expert slices, one warp merging the sorted
+// lists by k rounds over their heads: logit descending, ties to the lower
+// id, the order of warp_topk), the routing weights, the shared gate and
+// (unless mode & 4) the block-fixed-point digits of its x.  Published to the
+// host when pub.ready is set (one token only: several tokens publish with
+// publish_kernel afterwards).
+constexpr int kRtThreads = 512, kRtWarps = kRtThreads / 32;
+
+template <int BITS>
+__global__ void __launch_bounds__(kRtThreads) route_token_kernel(
+    Shapes s, int mode, const float* __restrict__ logits, const float* __restrict__ x,
+    const uint16_t* __restrict__ wsg, int32_t* idx, float* w, float* sigma, int32_t* uidx, float* uw, TokenDigits xd,
+    HostGate pub, int pub_layer) {
+    const int E = s.n_experts, k = s.top_k, H = s.hidden;
+    const int t = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    extern __shared__ __align__(16) float rt_x[];  // [H] this token's x
+    __shared__ float s_lg[kMaxE];
+    __shared__ uint32_t s_ck[kRtWarps][kMaxK];
+    __shared__ int32_t s_ci[kRtWarps][kMaxK];
+    __shared__ float s_val[kMaxK], s_w[kMaxK];
+    __shared__ float s_red[kRtWarps];
+    __shared__ int s_xe;
+    const float* lg = logits + (size_t)t * E;
+    const int M = (E + kRtThreads - 1) / kRtThreads;  // keys per lane (<= 2)
+    const int nlist = (E + 32 * M - 1) / (32 * M);
+    // level 1: the k best of this warp's experts w*32*M + 32 m + lane
+    uint32_t key0 = 0u, key1 = 0u;
+    for (int m = 0; m < M; ++m) {
+        const int j = warp * 32 * M + 32 * m + lane;
+        if (j < E) {
+            const float v = lg[j];
+            s_lg[j] = v;
+            if (m == 0)
+                key0 = order_key(v);
+            else
+                key1 = order_key(v);
+        }
+    }
+    if (warp < nlist) {
+#pragma unroll 1
+        for (int r = 0; r < k; ++r) {
+            const int bm = key1 > key0 ? 1 : 0;
+            const uint32_t best = bm ? key1 : key0;
+            const uint32_t mx = __reduce_max_sync(kFullMask, best);
+            const uint32_t win = __reduce_min_sync(
+                kFullMask, (best == mx && mx != 0u) ? (uint32_t)(warp * 32 * M + 32 * bm + lane) : 0xffffffffu);
+            if (lane == 0) {
+                s_ck[warp][r] = mx;
+                s_ci[warp][r] = (int)win;
+            }
+            if (win == 0xffffffffu) break;
+            if (lane == (int)(win & 31u)) {
+                if (((win - (uint32_t)(warp * 32 * M)) >> 5) == 0u)
+                    key0 = 0u;
+                else
+                    key1 = 0u;
+            }
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // level 2: merge the lists' heads; lane i < nlist holds list i's head and next entry
+        uint32_t hk = 0u, hi = 0xffffffffu, nk = 0u, ni = 0xffffffffu;
+        if (lane < nlist) {
+            if (s_ci[lane][0] >= 0) hk = s_ck[lane][0], hi = (uint32_t)s_ci[lane][0];
+            if (k > 1 && hi != 0xffffffffu && s_ci[lane][1] >= 0) nk = s_ck[lane][1], ni = (uint32_t)s_ci[lane][1];
+        }
+        int pos = 1;
+#pragma unroll 1
+        for (int r = 0; r < k; ++r) {
+            const uint32_t mx = __reduce_max_sync(kFullMask, hk);
+            const uint32_t win = __reduce_min_sync(kFullMask, hk == mx ? hi : 0xffffffffu);
+            if (lane == 0) {
+                idx[t * k + r] = (int)win;
+                if (uidx) uidx[t * k + r] = (int)win;
+                s_val[r] = s_lg[win];
+            }
+            if (hi == win) {
+                hk = nk, hi = ni;
+                ++pos;
+                nk = 0u, ni = 0xffffffffu;
+                if (hi != 0xffffffffu && pos < k && s_ci[lane][pos] >= 0) nk = s_ck[lane][pos], ni = (uint32_t)s_ci[lane][pos];
+            }
+        }
+        __syncwarp();
+        topk_weights(s_lg, E, k, s.norm_topk, lane, s_val, s_w);
+        if (lane < k) {
+            w[t * k + lane] = s_w[lane];
+            if (uw) uw[t * k + lane] = s_w[lane];
+        }
+    } else if (warp == 1) {
+        const float sg = wsg ? shared_gate(wsg, x + (size_t)t * H, H, lane) : 0.0f;
+        if (lane == 0) sigma[t] = sg;
+    }
+    if (!(mode & 4)) {
+        // digits of x: max |x| over the block, then a warp per 32 columns
+        float mx = 0.0f;
+        for (int j = threadIdx.x; j < H; j += kRtThreads) {
+            const float v = x[(size_t)t * H + j];
+            rt_x[j] = v;
+            mx = fmaxf(mx, fabsf(v));
+        }
+        mx = warp_max(mx);
+        if (lane == 0) s_red[warp] = mx;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float m2 = s_red[0];
+            for (int i = 1; i < kRtWarps; ++i) m2 = fmaxf(m2, s_red[i]);
+            s_xe = bfp_exponent(m2);
+            xd.exps[t] = s_xe;
+        }
+        __syncthreads();
+        const int nc = H / Codes<BITS>::kCols;
+        make_digits<BITS>(1, H, rt_x, xd.words + (size_t)t * nc * Codes<BITS>::kDigitWords, xd.sums + (size_t)t * nc,
+                          &s_xe, 0, kRtWarps);
+    }
+    if (pub.ready) {
+        // one token: publish the routing to the host
+        __syncthreads();
+        for (int i = threadIdx.x; i < k; i += kRtThreads) pub.idx[(size_t)pub_layer * pub.idx_stride + i] = idx[i];
+        __threadfence_system();
+        __syncthreads();
+        if (threadIdx.x == 0) pub.ready[pub_layer] = *pub.epoch;
+    }
+}
+
 __global__ void __launch_bounds__(1024) route_dispatch_kernel(
     Shapes s, int mode, const float* __restrict__ logits, const float* __restrict__ x,
     const uint16_t* __restrict__ wsg, int B, int32_t* idx, float* w, float* sigma, int32_t* uidx, float* uw,
@@ -503,15 +630,29 @@ cudaError_t launch_route_dispatch(const Shapes& s, int mode, const float* logits
                                   const uint8_t* shared_blob, Dispatch d, TokenDigits xd,
                                   unsigned long long* hit_counter, cudaStream_t st, const HostGate* pub,
                                   int pub_layer) {
-    // the top-k part publishes itself when it runs as one CTA, else a small kernel follows
-    const bool fused_pub = pub && (mode & 1) && (B + 7) / 8 == 1;
+    // the per-token part (top-k, weights, shared gate, digits): one CTA per token,
+    // publishing itself for one token, else a small kernel follows; the dispatch
+    // lists in one CTA of 1024 threads
+    const bool fused_pub = pub && (mode & 1) && B == 1;
     const HostGate none{};
-    // the per-token part (top-k, weights, shared gate, digits: one warp per token) spread
-    // over B/8 CTAs; the dispatch lists in one CTA of 1024 threads
     if (mode & 1) {
-        route_dispatch_kernel<<<(B + 7) / 8, 256, 0, st>>>(s, mode & ~2, logits, x, shared_gate_w, B, idx, w, sigma,
-                                                            user_idx, user_w, dir_layer, shared_blob, d, xd,
-                                                            hit_counter, fused_pub ? *pub : none, pub_layer);
+        const size_t xs_bytes = (mode & 4) ? 0 : (size_t)s.hidden * sizeof(float);
+        if (s.n_experts > kMaxE || s.top_k > kMaxK) return cudaErrorInvalidValue;
+        cudaError_t e = cudaSuccess;
+        if (s.bits == 4) {
+            e = smem_limit(reinterpret_cast<const void*>(route_token_kernel<4>), (int)xs_bytes);
+            if (e == cudaSuccess)
+                route_token_kernel<4><<<B, kRtThreads, xs_bytes, st>>>(s, mode, logits, x, shared_gate_w, idx, w,
+                                                                        sigma, user_idx, user_w, xd,
+                                                                        fused_pub ? *pub : none, pub_layer);
+        } else {
+            e = smem_limit(reinterpret_cast<const void*>(route_token_kernel<8>), (int)xs_bytes);
+            if (e == cudaSuccess)
+                route_token_kernel<8><<<B, kRtThreads, xs_bytes, st>>>(s, mode, logits, x, shared_gate_w, idx, w,
+                                                                        sigma, user_idx, user_w, xd,
+                                                                        fused_pub ? *pub : none, pub_layer);
+        }
+        if (e != cudaSuccess) return e;
         if (pub && !fused_pub) {
             cudaError_t e = cudaGetLastError();
             if (e != cudaSuccess) return e;

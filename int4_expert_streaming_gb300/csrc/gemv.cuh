@@ -132,6 +132,56 @@ __device__ __forceinline__ void bfp_chunk(const int* V, uint32_t* dw, int& S) {
     }
 }
 
+// Block-fixed-point digits of B tokens' x (xs [B][H], exponents xe[B]) by the
+// warps w0 .. w0+nw-1 of the block:
+// a warp covers 32 consecutive columns of one token (one int4 chunk, two int8
+// chunks); the digit words are assembled with shuffles in the layout of
+// bfp_chunk and stored whole.
+template <int BITS>
+__device__ __forceinline__ void make_digits(int B, int H, const float* xs, uint32_t* xdw, int32_t* xS, const int* xe,
+                                            int w0, int nw) {
+    constexpr int CC = Codes<BITS>::kCols, DW = Codes<BITS>::kDigitWords;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nc = H / CC, ng = H / 32;
+#pragma unroll 1
+    for (int g = warp - w0; g < B * ng; g += nw) {
+        const int t = g / ng, col = (g - t * ng) * 32 + lane;
+        const int V = bfp_int(xs[t * H + col], xe[t]);
+        uint32_t d0, d1, d2;
+        bfp_digits(V, d0, d1, d2);
+        const uint32_t dig = d0 | (d1 << 8) | (d2 << 16);
+        if (BITS == 4) {
+            // word L = 6 cw + 2 j + odd: digit j of columns 8 cw + 2 b + odd, b = 0..3
+            const int Lw = lane < 24 ? lane : 0;
+            const int cw = Lw / 6, r = Lw - 6 * cw, j = r >> 1, odd = r & 1;
+            const uint32_t g0 = __shfl_sync(kFullMask, dig, 8 * cw + 0 + odd);
+            const uint32_t g1 = __shfl_sync(kFullMask, dig, 8 * cw + 2 + odd);
+            const uint32_t g2 = __shfl_sync(kFullMask, dig, 8 * cw + 4 + odd);
+            const uint32_t g3 = __shfl_sync(kFullMask, dig, 8 * cw + 6 + odd);
+            const uint32_t sel = (uint32_t)j | ((uint32_t)(j + 4) << 4);
+            const uint32_t word = __byte_perm(__byte_perm(g0, g1, sel), __byte_perm(g2, g3, sel), 0x5410);
+            const int ch = col / CC;
+            if (lane < 24) xdw[(size_t)(t * nc + ch) * DW + lane] = word;
+            const int S = __reduce_add_sync(kFullMask, V);
+            if (lane == 0) xS[t * nc + ch] = S;
+        } else {
+            // per half-warp chunk: word 3 cw + j = digit j of columns 4 cw + b, b = 0..3
+            const int hb = lane & 16, L = lane & 15;
+            const int Lw = L < 12 ? L : 0;
+            const int cw = Lw / 3, j = Lw - 3 * cw;
+            const uint32_t g0 = __shfl_sync(kFullMask, dig, hb + 4 * cw + 0);
+            const uint32_t g1 = __shfl_sync(kFullMask, dig, hb + 4 * cw + 1);
+            const uint32_t g2 = __shfl_sync(kFullMask, dig, hb + 4 * cw + 2);
+            const uint32_t g3 = __shfl_sync(kFullMask, dig, hb + 4 * cw + 3);
+            const uint32_t sel = (uint32_t)j | ((uint32_t)(j + 4) << 4);
+            const uint32_t word = __byte_perm(__byte_perm(g0, g1, sel), __byte_perm(g2, g3, sel), 0x5410);
+            const int ch = col / CC;
+            if (L < 12) xdw[(size_t)(t * nc + ch) * DW + L] = word;
+            const int S = lane < 16 ? __reduce_add_sync(0x0000ffffu, V) : __reduce_add_sync(0xffff0000u, V);
+            if (L == 0) xS[t * nc + ch] = S;
+        }
+    }
+}
+
 // sum over the chunk of q_c * V_c, as a float (digits recombined in a fixed order)
 __device__ __forceinline__ float chunk_dot(uint4 v, const uint32_t* dw, Codes<4>) {
     const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
