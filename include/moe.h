@@ -241,12 +241,18 @@ int moe_forward_decode(moe_ctx* ctx, int32_t layer, const float* x_dev, int32_t 
  *   idx_trace_dev int32 [n_layers x B x top_k] chosen experts
  *   y_trace_dev fp32 [n_layers x B x hidden]   layer outputs y_l
  * All-resident contexts run the whole stack as one persistent kernel.
- * Streaming contexts run up to 3 tokens on the same kernel, which goes on
- * through layers whose experts are all resident and stops at a layer with an
- * absent expert; the host fetches the missing experts and launches again
- * from there (calls with traces use the per-layer kernels).  From 4 tokens
- * on: per-layer kernels with the host's pool decision between routing and
- * dispatch of every layer.  All paths give the same bits.
+ * Streaming contexts run up to 3 tokens on the same kernel (when the pool has
+ * at least B x top_k slots), one launch per call: it publishes each layer's
+ * routing to the host and goes on through layers whose experts are all
+ * resident; at a layer with an absent expert it waits for the host's slot
+ * assignment, uses the resident experts at once and each missing expert as
+ * soon as its own copy has landed [Swiftlet article, section 3: misses hidden
+ * behind compute].  The call returns once the host has served every layer;
+ * if the host has to give up mid-call (an I/O error, a failed copy) the
+ * kernel ends early and the context is poisoned.  Calls with traces use the
+ * per-layer kernels.  From 4 tokens on: per-layer kernels with the host's pool
+ * decision between routing and dispatch of every layer.  All paths give the
+ * same bits.
  */
 int moe_forward_decode_stack(moe_ctx* ctx, int32_t layer0, int32_t n_layers, const float* x_dev, int32_t B,
                              float* y_dev, float renorm_eps, float* x_trace_dev, int32_t* idx_trace_dev,

@@ -13,9 +13,12 @@
 // and fetch a missed expert with one cudaMemcpyAsync of one stride on a side
 // stream -- the CUDA counterpart of Swiftlet's one pread per expert from the
 // fixed-stride container (article section 2; explainer "Flujo de Inferencia"
-// steps 3-6).  The compute stream waits on an event recorded after the copies,
-// which is this library's explicit hazard management between slot refills and
-// the kernels that read them.  A streaming context can instead take its
+// steps 3-6).  Behind the per-layer kernels the compute stream waits on an
+// event recorded after the copies; behind the persistent decode kernel each
+// copy is followed on the side stream by a stream memory write of the
+// expert's arrival word, which the running kernel waits for before it reads
+// that expert's rows (and only those).  That is this library's explicit
+// hazard management between slot refills and the kernels that read them.  A streaming context can instead take its
 // routed blobs from an expert container on disk (store.cpp): a miss is then
 // one positioned read of the blob into a pinned staging buffer followed by the
 // same copy, which is Swiftlet's own fetch path.
@@ -30,6 +33,8 @@
 #include <string>
 #include <thread>
 #include <vector>
+
+#include <cuda.h>
 
 #include "moe_internal.h"
 #include "store.h"
@@ -78,11 +83,9 @@ struct moe_ctx {
     float* part = nullptr;  // [max_pairs][H] weighted down rows of each pair
     float* xbuf = nullptr;  // [2][max_batch][H]
     float* ybuf = nullptr;  // [max_batch][H]
-    // streaming through the persistent kernel: routing of the layer in flight,
-    // double-buffered by layer parity (idx, w [2][max_batch*top_k], sigma [2][max_batch])
-    int32_t* sr_idx = nullptr;
-    float* sr_w = nullptr;
-    float* sr_sig = nullptr;
+    // streaming through the persistent kernel: the sequence number of the last
+    // copy into each expert's slot [n_layers][E], set by the side stream
+    uint32_t* arrive = nullptr;
     // streaming, whole-stack calls: each layer's input [n_layers][max_batch][H],
     // the last layer's output, and one CUDA graph per layer (and one for the
     // first routing) for the call's batch size
@@ -129,15 +132,21 @@ struct moe_ctx {
     cudaEvent_t bias_ev[kBiasSlots] = {};
     bool bias_used[kBiasSlots] = {};
     int bias_next = 0;
-    int pending_timing_layer = -1;  // layer whose miss-copy events are not yet harvested
+    // miss-copy timing: one event pair per served layer with misses, harvested once complete
+    static constexpr int kTimeRing = 64;
+    cudaEvent_t tev[kTimeRing][2] = {};
+    int tlayer[kTimeRing] = {};
+    int64_t t_rec = 0, t_harv = 0;
     std::vector<uint8_t> loaded;
     std::vector<moe_slotpool*> pools;
     int32_t active_slots = 0;  // slots in use per layer (<= cfg.pool_slots, the reserved stride)
     std::vector<LayerStats> stats;
     std::vector<int32_t> trace;
     cudaStream_t side = nullptr;
-    cudaEvent_t ev_copy0 = nullptr, ev_copy1 = nullptr;
     int64_t miss_copies = 0;
+    uint32_t copy_seq = 0;  // sequence number of the last miss copy (never 0)
+    // cuStreamWriteValue32 (driver entry point); null: the persistent kernel does not stream
+    CUresult (*write_value)(CUstream, CUdeviceptr, cuuint32_t, unsigned int) = nullptr;
     bool fault_timeout_armed = false;
     bool fault_device_armed = false;  // MOE_FAULT_DEVICE_WAIT, not yet spent
     uint64_t launches = 0;
@@ -252,24 +261,64 @@ const uint8_t* shared_blob(moe_ctx* c, int layer) {
     return c->cfg.shared_inter > 0 ? c->shared_pool + (size_t)layer * c->shared_stride : nullptr;
 }
 
-// Account the device time of the previous layer's miss copies (complete once
-// a later routing has been published: the compute stream waited for them).
-void harvest_copy_timing(moe_ctx* c) {
-    if (c->pending_timing_layer < 0) return;
-    float ms = 0.0f;
-    if (cudaEventElapsedTime(&ms, c->ev_copy0, c->ev_copy1) == cudaSuccess)
-        c->stats[c->pending_timing_layer].h2d_ms += ms;
-    else
+// Account the device time of served layers' miss copies, oldest first: those
+// already complete, or (wait) all of them.
+void harvest_copy_timing(moe_ctx* c, bool wait) {
+    for (; c->t_harv < c->t_rec; ++c->t_harv) {
+        const int i = (int)(c->t_harv % moe_ctx::kTimeRing);
+        if (wait)
+            cudaEventSynchronize(c->tev[i][1]);
+        else if (cudaEventQuery(c->tev[i][1]) != cudaSuccess)
+            break;
+        float ms = 0.0f;
+        if (cudaEventElapsedTime(&ms, c->tev[i][0], c->tev[i][1]) == cudaSuccess) c->stats[c->tlayer[i]].h2d_ms += ms;
         cudaGetLastError();
-    c->pending_timing_layer = -1;
+    }
+}
+
+// the next miss copy's sequence number (never 0: arrival words start at 0)
+uint32_t next_seq(moe_ctx* c) {
+    if (++c->copy_seq == 0u) ++c->copy_seq;
+    return c->copy_seq;
+}
+
+// Streaming through the persistent kernel: the host gives up the call from
+// layer l on.  A layer the kernel waits at (now or later) reads serve_n < 0
+// and the kernel ends within microseconds; the host waits for that (bounded).
+// A launch that merely ended this way leaves the context usable (its status
+// word is cleared); failures that left the pool ahead of the slots (a copy or
+// a read that never ran) have poisoned the context already, and so does a
+// stream that does not drain.
+void abandon_layers(moe_ctx* c, int l, int lend, uint32_t epoch, cudaStream_t st) {
+    for (int i = l; i < lend; ++i) c->gate_host.serve_n[i] = -1;
+    std::atomic_thread_fence(std::memory_order_seq_cst);
+    for (int i = l; i < lend; ++i) c->gate_host.served[i] = epoch;
+    std::atomic_thread_fence(std::memory_order_seq_cst);
+    const auto deadline = std::chrono::steady_clock::now() + std::chrono::milliseconds(timeout_ms(c));
+    for (;;) {
+        const cudaError_t e = cudaStreamQuery(st);
+        if (e == cudaSuccess) break;
+        if (e != cudaErrorNotReady || std::chrono::steady_clock::now() > deadline) {
+            cudaGetLastError();
+            c->poisoned = true;
+            return;
+        }
+        std::this_thread::yield();
+    }
+    if (moe::stack_clear_abandoned(c->stack) != cudaSuccess) c->poisoned = true;
 }
 
 // Streaming, host side of one layer: wait until the layer's routing has been
-// published (mapped memory, polled), run the slot pool policy on it, copy each
-// missed expert's blob into its slot with cudaMemcpyAsync on the side stream
-// (the compute stream waits on an event after the copies) and write the
-// layer's directory, which the dispatch kernel launched next reads.
-int serve_layer(moe_ctx* c, int layer, int B, uint32_t epoch, cudaStream_t st, bool* stopped) {
+// published (mapped memory, polled), run the slot pool policy on it and copy
+// each missed expert's blob into its slot with cudaMemcpyAsync on the side
+// stream.  Behind the per-layer kernels (gated_launch false) the compute stream
+// then waits on an event after the copies and the layer's device directory is
+// rewritten before the dispatch enqueued next.  Behind the persistent kernel
+// (gated_launch true) the kernel is waiting at the layer when it found an
+// absent expert: it gets the slots and sequence numbers of the misses at once
+// (before any copy is issued), and each copy is followed by the stream write
+// of the expert's arrival word; the kernel patches the device directory.
+int serve_layer(moe_ctx* c, int layer, int B, uint32_t epoch, cudaStream_t st, bool gated_launch) {
     const int k = c->cfg.top_k, E = c->cfg.n_experts;
     if (c->fault_timeout_armed) {
         c->fault_timeout_armed = false;
@@ -287,10 +336,8 @@ int serve_layer(moe_ctx* c, int layer, int B, uint32_t epoch, cudaStream_t st, b
         }
     }
     std::atomic_thread_fence(std::memory_order_acquire);
-    // behind a persistent launch: did it stop at this layer (else it ran on,
-    // having found every expert of the layer in the directory)?
-    if (stopped) *stopped = c->gate_host.stop[layer] == epoch;
-    harvest_copy_timing(c);
+    const bool gated = gated_launch && c->gate_host.gated[layer] == epoch;  // the kernel waits for the answer
+    harvest_copy_timing(c, false);
     const int32_t* pub = c->gate_host.idx + (size_t)layer * c->gate_host.idx_stride;
     std::vector<int32_t> req(pub, pub + B * k);
     std::sort(req.begin(), req.end());
@@ -300,48 +347,73 @@ int serve_layer(moe_ctx* c, int layer, int B, uint32_t epoch, cudaStream_t st, b
     if (rc < 0)
         return fail(c, rc, "slot pool request of %zu experts failed (pool has %d slots)", req.size(),
                     c->active_slots);
-    if (stopped && !*stopped)
-        for (size_t i = 0; i < req.size(); ++i)
-            if (ev[4 * i + 1] != 0) {  // pool and device directory disagree: nothing later can be trusted
-                fail(c, MOE_ESTATE, "layer %d ran on the device without expert %d, which the pool lacks", layer,
-                     ev[4 * i]);
-                c->poisoned = true;
-                return MOE_ESTATE;
-            }
     LayerStats& S = c->stats[layer];
     const int64_t call_no = S.calls;
     const uint8_t** dirh = c->dir_host + (size_t)layer * E;
-    bool any_miss = false;
+    size_t n_miss = 0;
+    for (size_t i = 0; i < req.size(); ++i) n_miss += ev[4 * i + 1] != 0 ? 1 : 0;
+    if (gated_launch && (n_miss > 0) != gated) {  // pool and device directory disagree: nothing later can be trusted
+        fail(c, MOE_ESTATE, "layer %d: the pool %s while the device found every expert %s", layer,
+             n_miss ? "misses" : "hits", n_miss ? "resident" : "but one");
+        c->poisoned = true;
+        return MOE_ESTATE;
+    }
+    // slots, sequence numbers and the directory first (the pool has decided them)
+    struct Miss {
+        int32_t e;
+        uint8_t* dst;
+        uint32_t seq;
+    };
+    std::vector<Miss> miss;
+    std::vector<int32_t> evicted;
     for (size_t i = 0; i < req.size(); ++i) {
-        const int32_t e = ev[4 * i], kind = ev[4 * i + 1], slot = ev[4 * i + 2], evicted = ev[4 * i + 3];
-        c->trace.insert(c->trace.end(), {(int32_t)call_no, layer, e, kind, slot, evicted});
+        const int32_t e = ev[4 * i], kind = ev[4 * i + 1], slot = ev[4 * i + 2], out = ev[4 * i + 3];
+        c->trace.insert(c->trace.end(), {(int32_t)call_no, layer, e, kind, slot, out});
         if (kind == 0) {
             S.hits++;
             continue;
         }
         S.misses++;
-        if (evicted >= 0) {
+        if (out >= 0) {
             S.evictions++;
-            dirh[evicted] = nullptr;
+            dirh[out] = nullptr;
+            evicted.push_back(out);
         }
         uint8_t* dst = c->pool + ((size_t)layer * c->cfg.pool_slots + slot) * c->stride;
-        const uint8_t* src = c->store ? c->store + ((size_t)layer * E + e) * c->stride : nullptr;
+        miss.push_back({e, dst, gated ? next_seq(c) : 0u});
+        dirh[e] = dst;
+    }
+    if (gated) {
+        moe::ServeEntry* tab = c->gate_host.serve_tab + (size_t)layer * c->gate_host.serve_stride;
+        size_t n = 0;
+        for (const Miss& m : miss) tab[n++] = moe::ServeEntry{m.e, m.seq, m.dst};
+        for (int32_t o : evicted) tab[n++] = moe::ServeEntry{-1 - o, 0u, nullptr};
+        c->gate_host.serve_n[layer] = (int32_t)(miss.size() | evicted.size() << 16);
+        std::atomic_thread_fence(std::memory_order_seq_cst);
+        c->gate_host.served[layer] = epoch;
+        std::atomic_thread_fence(std::memory_order_seq_cst);
+    }
+    if (miss.empty()) {
+        S.calls++;
+        return MOE_OK;
+    }
+    const int64_t ti = c->t_rec % moe_ctx::kTimeRing;
+    if (c->t_rec - c->t_harv == moe_ctx::kTimeRing) harvest_copy_timing(c, true);
+    CUDA_TRY(c, cudaEventRecord(c->tev[ti][0], c->side));
+    for (const Miss& m : miss) {
+        const uint8_t* src = c->store ? c->store + ((size_t)layer * E + m.e) * c->stride : nullptr;
         int stage_i = -1;
         if (!src) {  // expert container: one positioned read into the next staging buffer
             stage_i = c->stage_next;
             c->stage_next = (stage_i + 1) % moe_ctx::kStage;
             if (c->stage_used[stage_i]) CUDA_TRY(c, cudaEventSynchronize(c->stage_ev[stage_i]));
             uint8_t* buf = c->stage + (size_t)stage_i * c->stride;
-            if (moe::store_read_blob(c->file, layer, e, buf) != MOE_OK) {
-                fail(c, MOE_EIO, "reading expert %d of layer %d from %s failed", e, layer, c->store_path.c_str());
+            if (moe::store_read_blob(c->file, layer, m.e, buf) != MOE_OK) {
+                fail(c, MOE_EIO, "reading expert %d of layer %d from %s failed", m.e, layer, c->store_path.c_str());
                 c->poisoned = true;  // the pool already counts the expert as resident
                 return MOE_EIO;
             }
             src = buf;
-        }
-        if (!any_miss) {
-            CUDA_TRY(c, cudaEventRecord(c->ev_copy0, c->side));
-            any_miss = true;
         }
         if ((c->cfg.fault_flags & MOE_FAULT_MISS_COPY) && c->miss_copies == c->cfg.fault_arg) {
             c->miss_copies++;
@@ -349,18 +421,22 @@ int serve_layer(moe_ctx* c, int layer, int B, uint32_t epoch, cudaStream_t st, b
         }
         c->miss_copies++;
         // the slot's previous expert was last read before this routing was published
-        CUDA_TRY(c, cudaMemcpyAsync(dst, src, c->lstride[layer], cudaMemcpyHostToDevice, c->side));
+        CUDA_TRY(c, cudaMemcpyAsync(m.dst, src, c->lstride[layer], cudaMemcpyHostToDevice, c->side));
+        if (gated) {
+            const CUresult r = c->write_value(c->side, (CUdeviceptr)(c->arrive + (size_t)layer * E + m.e), m.seq, 0);
+            if (r != CUDA_SUCCESS) return fail(c, MOE_ECUDA, "cuStreamWriteValue32 failed (%d)", (int)r);
+        }
         if (stage_i >= 0) {
             CUDA_TRY(c, cudaEventRecord(c->stage_ev[stage_i], c->side));
             c->stage_used[stage_i] = true;
         }
         S.h2d_bytes += c->lstride[layer];
-        dirh[e] = dst;
     }
-    if (any_miss) {
-        CUDA_TRY(c, cudaEventRecord(c->ev_copy1, c->side));
-        CUDA_TRY(c, cudaStreamWaitEvent(st, c->ev_copy1, 0));
-        c->pending_timing_layer = layer;
+    CUDA_TRY(c, cudaEventRecord(c->tev[ti][1], c->side));
+    c->tlayer[ti] = layer;
+    c->t_rec++;
+    if (!gated_launch) {
+        CUDA_TRY(c, cudaStreamWaitEvent(st, c->tev[ti][1], 0));
         // the layer's device directory, read by the dispatch enqueued next (the
         // source is pinned; the host rewrites it only after a later routing of
         // this layer has been published, i.e. after this copy has run)
@@ -423,24 +499,24 @@ int enq_post(moe_ctx* c, int l, const float* xin, int B, float* yl, cudaStream_t
     return MOE_OK;
 }
 
-// Streaming stacks of a few tokens run on the persistent kernel from layer l
-// to the end of the call, stopping only at a layer with an absent expert
-// (the kernel checks the device directory after publishing the routing).
-// Layer l's routing is given: the route kernels' output when l is the call's
-// first layer, else what the stopped launch left.  Results are bitwise those
-// of the all-resident persistent kernel.
+// Streaming stacks of a few tokens run as one persistent launch per call: the
+// kernel publishes every layer's routing and waits only at a layer with an
+// absent expert, for the host's answer and then for each missing blob's
+// arrival (see serve_layer).  Results are bitwise those of the all-resident
+// persistent kernel.
 bool stream_stack_ok(const moe_ctx* c, int B) {
-    return !c->resident && !c->mixed && B <= moe::kStackPreferMaxB && moe::stack_supported(c->sh, c->stack, B);
+    return !c->resident && !c->mixed && c->write_value && B <= moe::kStackPreferMaxB &&
+           c->active_slots >= B * c->cfg.top_k && moe::stack_supported(c->sh, c->stack, B);
 }
 
-int enq_stack_from(moe_ctx* c, int l, int lend, bool first, const float* x, int B, float eps, float* y,
-                   cudaStream_t st) {
+int enq_stack_streaming(moe_ctx* c, int l, int lend, const float* x, int B, float eps, float* y, uint32_t epoch,
+                        cudaStream_t st) {
     moe::StackArgs a{};
     a.layer0 = l;
     a.n_layers = lend - l;
     a.B = B;
     a.eps = eps;
-    a.x = first ? x : c->xbuf;  // a stopped launch leaves the layer's x in xbuf
+    a.x = x;
     a.y = y;
     a.router_w = c->router_w;
     a.router_bias = c->router_bias;
@@ -448,16 +524,10 @@ int enq_stack_from(moe_ctx* c, int l, int lend, bool first, const float* x, int 
     a.dir = c->dir;
     a.shared_pool = c->cfg.shared_inter > 0 ? c->shared_pool : nullptr;
     a.shared_stride = c->shared_stride;
-    a.rin_idx = first ? c->idx : c->sr_idx;
-    a.rin_w = first ? c->w : c->sr_w;
-    a.rin_sig = first ? c->sigma : c->sr_sig;
-    // the launch reads x and rin_* in its first layer and writes these only
-    // at a later layer's stop, after every CTA has passed its first layer
-    a.x_out = c->xbuf;
-    a.rout_idx = c->sr_idx;
-    a.rout_w = c->sr_w;
-    a.rout_sig = c->sr_sig;
     a.pub = &c->gate_dev;
+    a.dir_patch = c->dir;
+    a.arrive = c->arrive;
+    a.epoch = epoch;
     const cudaError_t e = moe::launch_stack(c->sh, c->stack, a, st);
     if (e != cudaSuccess) return fail(c, MOE_ECUDA, "decode stack launch failed: %s", cudaGetErrorString(e));
     c->launches += 1;
@@ -523,16 +593,16 @@ int stream_layers(moe_ctx* c, int layer0, int n, const float* x, int B, float* y
     std::atomic_thread_fence(std::memory_order_seq_cst);
     const bool plain = !x_trace && !idx_trace && !y_trace && !uidx && !uw;
     if (plain && stream_stack_ok(c, B)) {
-        // route the first layer, serve it, then one persistent launch that the
-        // host relaunches only from layers that miss
-        c->launches += route_launches(B);
-        int rc = enq_route(c, layer0, x, B, nullptr, nullptr, st);
-        if (!rc) rc = serve_layer(c, layer0, B, epoch, st, nullptr);
-        if (!rc) rc = enq_stack_from(c, layer0, layer0 + n, true, x, B, eps, y, st);
-        for (int l = layer0 + 1; l < layer0 + n && !rc; ++l) {
-            bool stopped = false;
-            rc = serve_layer(c, l, B, epoch, st, &stopped);
-            if (!rc && stopped) rc = enq_stack_from(c, l, layer0 + n, false, x, B, eps, y, st);
+        // one persistent launch; the host answers each layer as it is published
+        if (moe::stack_last_status(c->stack))
+            return fail(c, MOE_ETIMEOUT, "a device-side wait of an earlier decode-stack launch ran out (status %d)",
+                        moe::stack_last_status(c->stack)) == MOE_ETIMEOUT
+                       ? (c->poisoned = true, MOE_ETIMEOUT)
+                       : MOE_ETIMEOUT;
+        int rc = enq_stack_streaming(c, layer0, layer0 + n, x, B, eps, y, epoch, st);
+        for (int l = layer0; l < layer0 + n && !rc; ++l) {
+            rc = serve_layer(c, l, B, epoch, st, true);
+            if (rc) abandon_layers(c, l, layer0 + n, epoch, st);
         }
         return rc;
     }
@@ -552,7 +622,7 @@ int stream_layers(moe_ctx* c, int layer0, int n, const float* x, int B, float* y
         CUDA_TRY(c, cudaGraphLaunch(c->graphs[0], st));
         c->launches += route_launches(B);
         for (int l = 0; l < n; ++l) {
-            int rc = serve_layer(c, l, B, epoch, st, nullptr);
+            int rc = serve_layer(c, l, B, epoch, st, false);
             if (rc) return rc;
             CUDA_TRY(c, cudaGraphLaunch(c->graphs[1 + l], st));
             c->launches += 4 + (l == L - 1 ? 0 : 1 + route_launches(B));  // post, renorm, next routing
@@ -570,7 +640,7 @@ int stream_layers(moe_ctx* c, int layer0, int n, const float* x, int B, float* y
     int rc = route(0);
     for (int i = 0; i < n && !rc; ++i) {
         const int l = layer0 + i;
-        if ((rc = serve_layer(c, l, B, epoch, st, nullptr))) break;
+        if ((rc = serve_layer(c, l, B, epoch, st, false))) break;
         const bool last = i == n - 1;
         float* yl = last ? y : (y_trace ? y_trace + i * tok : c->ybuf);
         if ((rc = enq_post(c, l, xin, B, yl, st))) break;
@@ -638,9 +708,7 @@ extern "C" void moe_destroy(moe_ctx* c) {
     cudaFree(c->part);
     cudaFree(c->xbuf);
     cudaFree(c->ybuf);
-    cudaFree(c->sr_idx);
-    cudaFree(c->sr_w);
-    cudaFree(c->sr_sig);
+    cudaFree(c->arrive);
     for (cudaGraphExec_t g : c->graphs)
         if (g) cudaGraphExecDestroy(g);
     cudaFree(c->xring);
@@ -662,11 +730,12 @@ extern "C" void moe_destroy(moe_ctx* c) {
     if (c->gate_mem) cudaFreeHost(c->gate_mem);
     for (auto* p : c->pools) moe_slotpool_destroy(p);
     if (c->side) cudaStreamDestroy(c->side);
-    if (c->ev_copy0) cudaEventDestroy(c->ev_copy0);
+    for (auto& pr : c->tev)
+        for (cudaEvent_t e : pr)
+            if (e) cudaEventDestroy(e);
     for (cudaEvent_t e : c->bias_ev)
         if (e) cudaEventDestroy(e);
     if (c->bias_stage) cudaFreeHost(c->bias_stage);
-    if (c->ev_copy1) cudaEventDestroy(c->ev_copy1);
     cudaGetLastError();
     delete c;
 }
@@ -741,9 +810,6 @@ extern "C" int moe_create(const moe_config* cfg, moe_ctx** out) {
         (rc = dev_alloc(c, &c->part, (size_t)s.max_pairs * H, "down partials")) ||
         (rc = dev_alloc(c, &c->xbuf, (size_t)2 * Bm * H, "xbuf")) ||
         (rc = dev_alloc(c, &c->ybuf, (size_t)Bm * H, "ybuf")) ||
-        (rc = dev_alloc(c, &c->sr_idx, (size_t)2 * Bm * k, "streamed routing")) ||
-        (rc = dev_alloc(c, &c->sr_w, (size_t)2 * Bm * k, "streamed routing weights")) ||
-        (rc = dev_alloc(c, &c->sr_sig, (size_t)2 * Bm, "streamed shared gates")) ||
         (rc = dev_alloc(c, &c->xd.words, (size_t)Bm * H * 3 / 4, "token digits")) ||
         (rc = dev_alloc(c, &c->xd.sums, (size_t)Bm * H / 16, "token digit sums")) ||
         (rc = dev_alloc(c, &c->xd.exps, (size_t)Bm, "token exponents")))
@@ -840,7 +906,10 @@ extern "C" int moe_create(const moe_config* cfg, moe_ctx** out) {
                 return bail(MOE_ENOMEM);
             }
         }
-        const size_t gate_bytes = sizeof(uint32_t) * (2 * (size_t)L + 1) + sizeof(int32_t) * (size_t)L * Bm * k;
+        // ready, epoch, gated, served, serve_n, idx; then the answer table (16-byte entries)
+        const size_t words = 4 * (size_t)L + 1 + (size_t)L * Bm * k;
+        const size_t tab_off = (words * 4 + 15) / 16 * 16, tab_stride = 2 * (size_t)Bm * k;
+        const size_t gate_bytes = tab_off + sizeof(moe::ServeEntry) * (size_t)L * tab_stride;
         if (cudaHostAlloc(reinterpret_cast<void**>(&c->dir_host), sizeof(void*) * (size_t)L * E,
                           cudaHostAllocDefault) != cudaSuccess ||
             cudaHostAlloc(&c->gate_mem, gate_bytes, cudaHostAllocMapped) != cudaSuccess) {
@@ -860,9 +929,13 @@ extern "C" int moe_create(const moe_config* cfg, moe_ctx** out) {
             uint32_t* w = static_cast<uint32_t*>(base);
             g.ready = w;
             g.epoch = w + L;
-            g.stop = w + L + 1;
-            g.idx = reinterpret_cast<int32_t*>(w + 2 * L + 1);
+            g.gated = w + L + 1;
+            g.served = w + 2 * L + 1;
+            g.serve_n = reinterpret_cast<int32_t*>(w + 3 * L + 1);
+            g.idx = reinterpret_cast<int32_t*>(w + 4 * L + 1);
             g.idx_stride = Bm * k;
+            g.serve_tab = reinterpret_cast<moe::ServeEntry*>(static_cast<uint8_t*>(base) + tab_off);
+            g.serve_stride = (int)tab_stride;
         };
         carve(c->gate_mem, c->gate_host);
         carve(gate_dev, c->gate_dev);
@@ -879,13 +952,28 @@ extern "C" int moe_create(const moe_config* cfg, moe_ctx** out) {
             return bail(MOE_ECUDA);
         }
         if ((rc = dev_alloc(c, &c->xring, (size_t)L * Bm * H, "xring")) ||
-            (rc = dev_alloc(c, &c->yout, (size_t)Bm * H, "yout")))
+            (rc = dev_alloc(c, &c->yout, (size_t)Bm * H, "yout")) ||
+            (rc = dev_alloc(c, &c->arrive, (size_t)L * E, "arrival words")))
             return bail(rc);
+        if (cudaMemset(c->arrive, 0, sizeof(uint32_t) * (size_t)L * E) != cudaSuccess) {
+            c->err = "cudaMemset failed";
+            return bail(MOE_ECUDA);
+        }
+        // stream memory writes mark each miss copy's arrival for the persistent kernel
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuStreamWriteValue32", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess && fn)
+            c->write_value = reinterpret_cast<CUresult (*)(CUstream, CUdeviceptr, cuuint32_t, unsigned int)>(fn);
+        cudaGetLastError();
     }
-    if (cudaEventCreate(&c->ev_copy0) != cudaSuccess || cudaEventCreate(&c->ev_copy1) != cudaSuccess) {
-        c->err = "cudaEventCreate failed";
-        return bail(MOE_ECUDA);
-    }
+    for (auto& pr : c->tev)
+        for (cudaEvent_t& e : pr)
+            if (cudaEventCreate(&e) != cudaSuccess) {
+                c->err = "cudaEventCreate failed";
+                return bail(MOE_ECUDA);
+            }
     *out = c;
     return MOE_OK;
 }
@@ -1174,7 +1262,7 @@ extern "C" int moe_pool_stats(moe_ctx* c, int32_t layer, moe_pool_stats_t* out) 
     }
     if (!c->resident && c->side && !c->poisoned) {
         CUDA_TRY(c, cudaStreamSynchronize(c->side));
-        harvest_copy_timing(c);
+        harvest_copy_timing(c, true);
     }
     for (int l = 0; l < g.n_layers; ++l) {
         if (layer >= 0 && l != layer) continue;
@@ -1202,7 +1290,7 @@ extern "C" int moe_pool_reset(moe_ctx* c, int32_t slots, int32_t policy, int32_t
     CUDA_TRY(c, cudaSetDevice(g.device));
     CUDA_TRY(c, cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
     CUDA_TRY(c, cudaStreamSynchronize(c->side));
-    harvest_copy_timing(c);
+    harvest_copy_timing(c, true);
     const int L = g.n_layers, E = g.n_experts;
     std::vector<moe_slotpool*> fresh(L, nullptr);
     for (int l = 0; l < L; ++l) {

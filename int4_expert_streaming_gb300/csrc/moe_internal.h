@@ -65,15 +65,33 @@ struct Dispatch {
     int32_t* n_work;       // [1]
 };
 
-// Publication of a streaming layer's routing to the host (device aliases of
-// mapped pinned host memory): the host polls ready[layer] for the call's epoch,
-// runs the slot pool on idx, and launches the layer's dispatch afterwards.
+// One entry of the host's answer to a streaming layer with absent experts:
+// a missed expert (expert >= 0) with the slot its blob is being copied to and
+// the sequence number the copy's arrival word will carry, or an evicted one
+// (expert = -1 - id, blob null).
+struct ServeEntry {
+    int32_t expert;
+    uint32_t seq;
+    const uint8_t* blob;
+};
+
+// Publication of a streaming layer's routing to the host and the host's
+// answer (device aliases of mapped pinned host memory).  The device writes
+// idx, then ready[layer] = the call's epoch (and gated[layer] first when some
+// expert of the layer is absent); the host runs the slot pool on idx.  For a
+// gated layer it writes the layer's entries (misses first), serve_n[layer] =
+// misses | evictions << 16 (or -1: the call is abandoned), then
+// served[layer] = epoch.
 struct HostGate {
     volatile uint32_t* ready;        // [n_layers] epoch of the last routing published per layer
     const volatile uint32_t* epoch;  // [1] the epoch of the current call, written by the host
-    volatile uint32_t* stop;         // [n_layers] epoch of the call whose persistent launch stopped there
+    volatile uint32_t* gated;        // [n_layers] epoch of the call whose persistent launch waits at the layer
     int32_t* idx;                    // [n_layers][idx_stride] the published routing of each layer
     int idx_stride;                  // max_batch * top_k
+    volatile uint32_t* served;       // [n_layers] epoch of the call whose layer has been answered
+    volatile int32_t* serve_n;       // [n_layers]
+    ServeEntry* serve_tab;           // [n_layers][serve_stride]
+    int serve_stride;                // 2 * max_batch * top_k
 };
 
 struct Shapes {

@@ -1,5 +1,5 @@
 // stack.h -- the persistent decode-stack kernel (all-resident stacks, and
-// streaming stacks that stop for the host only at layers that miss).
+// streaming stacks that wait for the host only at layers that miss).
 #pragma once
 
 #include <string>
@@ -35,18 +35,14 @@ struct StackArgs {
     const uint8_t* const* dir;
     const uint8_t* shared_pool;
     size_t shared_stride;
-    // streaming: the first layer's routing is given (idx and w [B*k], shared
-    // gate [B]); later layers publish their routing through `pub` and run on
-    // while their experts are resident; the launch stops at the first layer
-    // that is not, leaving that layer's x and routing in x_out / rout_*
-    const int32_t* rin_idx;
-    const float* rin_w;
-    const float* rin_sig;
-    float* x_out;
-    int32_t* rout_idx;
-    float* rout_w;
-    float* rout_sig;
+    // streaming: every layer's routing is published through `pub`; a layer
+    // with an absent expert waits for the host's answer (the slots of its
+    // missing experts, then each blob's arrival word), patches the device
+    // directory `dir_patch` (the array `dir` points to) and runs on
     const HostGate* pub;
+    const uint8_t** dir_patch;
+    const uint32_t* arrive;  // [n_layers][n_experts] sequence number of the last copy into each expert's slot
+    uint32_t epoch;          // the call's epoch (what ready/gated/served carry)
     // tests: one CTA withholds its outputs of the launch's first layer and every
     // device-side wait is bounded by 1 ms, so the others' waits run out
     int fault;
@@ -54,6 +50,8 @@ struct StackArgs {
 
 // largest batch the decode stack sends to the persistent kernel (measured crossover)
 constexpr int kStackPreferMaxB = 3;
+// missed experts per layer a streaming launch can wait for (kStackPreferMaxB tokens x top_k <= 16)
+constexpr int kMaxMiss = 48;
 
 int stack_alloc(StackScratch& s, const Shapes& sh, int n_layers, int max_batch, int device, std::string& err);
 void stack_free(StackScratch& s);
@@ -61,6 +59,9 @@ bool stack_supported(const Shapes& sh, const StackScratch& s, int B);
 // Status of the last finished launch (read from mapped host memory, no sync):
 // 0 = ok, otherwise a device-side wait ran out.
 int stack_last_status(const StackScratch& s);
+// After a finished launch that the host abandoned (and nothing worse): clears
+// the device and host status words so that later launches run.
+cudaError_t stack_clear_abandoned(StackScratch& s);
 cudaError_t launch_stack(const Shapes& sh, StackScratch& s, const StackArgs& a, cudaStream_t st);
 
 }  // namespace moe

@@ -36,16 +36,17 @@
 // section "Capability boundaries", README introduction) and keeps HBM busy
 // with bulk copies issued as soon as routing is known.
 //
-// Streaming contexts use it with the host's slot pool behind it.  A launch's
-// first layer takes its routing from a buffer (rin_*: written by the route
-// kernels or by the launch before) instead of computing it.  Every later
-// layer publishes its routing to mapped host memory, where the host runs the
-// pool's bookkeeping in order, and then checks its experts against the
-// device directory: when all are resident the launch simply goes on; at the
-// first layer with an absent expert it leaves that layer's x and routing for
-// the next launch, marks the layer as stopped and exits.  The host copies the
-// missing experts on its side stream and launches again from that layer, so
-// it is on the critical path only for layers that miss.
+// Streaming contexts use it with the host's slot pool behind it.  Every layer
+// publishes its routing to mapped host memory, where the host runs the pool's
+// bookkeeping in order, and checks its experts against the device directory:
+// when all are resident the launch simply goes on.  At a layer with an absent
+// expert every CTA waits for the host's answer (which slot each missing blob
+// is being copied to, and the sequence number that the copy's arrival word
+// will carry), and then goes on as well: rows of resident experts are fetched
+// and used at once, and each missing expert's rows are fetched only after its
+// own arrival word shows the copy done (the host's copy stream sets it right
+// behind the copy).  The copies thus overlap the layer's other work, and one
+// launch still runs the whole call.
 //
 // Every wait is bounded (%globaltimer): a poll or an mbarrier wait that does
 // not complete within wait_ns sets the status word; every CTA then stops at
@@ -70,6 +71,7 @@ constexpr int kNB = kMbP + 2;
 constexpr unsigned long long kWaitNs = 1000000000ull;  // 1 s
 constexpr unsigned long long kFaultWaitNs = 1000000ull;  // 1 ms (the test-only fault mode)
 constexpr int kStatusTimeout = 2;
+constexpr int kStatusAbandoned = 3;  // the host abandoned the call at a gated layer
 
 static_assert(kST == kRenormThreads, "the renormalisation order is defined for kRenormThreads threads");
 
@@ -97,25 +99,24 @@ struct Params {
     int* status_host;
     unsigned long long wait_ns;  // bound of every device-side wait
     int fault_cta;               // tests: this CTA withholds its y words of the launch's first layer (-1: none)
-    // streaming launch (rin_idx non-null): the first layer's routing is given
-    // (idx, w [B*k], sigma [B]); every later layer's routing is published to
-    // mapped host memory (pub_idx row l, then pub_ready[l] = *pub_epoch).  A
+    // streaming launch (pub_idx non-null): every layer's routing is published
+    // to mapped host memory (pub_idx row l, then pub_ready[l] = epoch).  A
     // layer whose experts are all resident (non-null directory entries) runs
-    // on; at the first one that is not, the launch writes that layer's x and
-    // routing for the next launch (x_out [B*H], rout_* like rin_*), sets
-    // pub_stop[l] = *pub_epoch before the ready word, and stops.
-    const int32_t* rin_idx;
-    const float* rin_w;
-    const float* rin_sig;
-    float* x_out;
-    int32_t* rout_idx;
-    float* rout_w;
-    float* rout_sig;
+    // on; one that is not sets pub_gated[l] = epoch before the ready word and
+    // waits for served[l] = epoch; serve_n[l] and the layer's serve_tab row
+    // then give the missed experts (slot blob, arrival sequence number) and the
+    // evicted ones.  CTA 0 patches the device directory (dir_patch) with them.
     int32_t* pub_idx;
     int pub_stride;
     volatile uint32_t* pub_ready;
-    volatile uint32_t* pub_stop;
-    const volatile uint32_t* pub_epoch;
+    volatile uint32_t* pub_gated;
+    const uint32_t* served;
+    const int32_t* serve_n;
+    const ServeEntry* serve_tab;
+    int serve_stride;
+    const uint8_t** dir_patch;
+    const uint32_t* arrive;  // [n_layers][E]
+    uint32_t epoch;
     // shared-memory plan
     int rE, rS, jn;
     int p_bytes, off_sg;  // prefetch buffer size; offset of w_sg in it
@@ -260,6 +261,36 @@ __device__ __forceinline__ bool warp_wait(uint64_t* m, uint32_t parity, const Pa
     }
 }
 
+__device__ __forceinline__ uint32_t ld_acquire_sys(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.sys.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ int32_t ld_relaxed_sys(const int32_t* p) {
+    int32_t v;
+    asm volatile("ld.relaxed.sys.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_sys64(const void* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.sys.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
+
+// streaming: the host's answer for layer l (served[l] = the call's epoch);
+// one thread; false on timeout or abort
+__device__ __forceinline__ bool served_wait(const Params& p, int l) {
+    unsigned spins = 0;
+    const unsigned long long t0 = gtime();
+#pragma unroll 1
+    while (ld_acquire_sys(p.served + l) != p.epoch) {
+        if (spin_abort(p, spins, t0)) return false;
+        __nanosleep(128);
+    }
+    return true;
+}
+
 // ---------------------------------------------------------------------------
 // shared-memory state of one CTA
 // ---------------------------------------------------------------------------
@@ -272,7 +303,12 @@ struct Disp {
     int xe[kMaxB];      // block-fixed-point exponent of each token's x
     float xmax[kMaxB];  // max |x| of each token
     float red[kMaxB][2][kSW];
-    int n_act, n_routed, n_pairs, pad;
+    int n_act, n_routed, n_pairs, n_miss;
+    int serve_n, pad2;  // streaming, a gated layer: the host's answer word, read once per CTA
+    // the missed experts' slots and arrival sequence numbers
+    const uint8_t* miss_blob[kMaxMiss];
+    uint32_t miss_seq[kMaxMiss];
+    int32_t miss_e[kMaxMiss];
 };
 
 struct Lists {
@@ -357,6 +393,39 @@ __device__ bool stage_wait(uint64_t* mb, int i, Waits& w, const Params& p) {
     return __syncthreads_and(ok ? 1 : 0) != 0;
 }
 
+// streaming: a directory entry with bit 0 set is a missed expert's slot whose
+// copy may still be in flight.  Strips the tag and, if it was set, waits until
+// the expert's arrival word carries the copy's sequence number.  One thread;
+// false on timeout or when the host abandons the call.
+__device__ __forceinline__ bool arrival_wait(const Params& p, const Disp* ds, int l, const uint8_t*& blob) {
+    const uintptr_t b = reinterpret_cast<uintptr_t>(blob);
+    if (!(b & 1u)) return true;
+    blob = reinterpret_cast<const uint8_t*>(b & ~(uintptr_t)1);
+    int e = -1;
+    uint32_t seq = 0;
+#pragma unroll 1
+    for (int i = 0; i < ds->n_miss; ++i)
+        if (ds->miss_blob[i] == blob) e = ds->miss_e[i], seq = ds->miss_seq[i];
+    if (e < 0) {  // every tagged entry is in the table
+        atomicCAS(p.status, 0, kStatusAbandoned);
+        return false;
+    }
+    const uint32_t* w = p.arrive + (size_t)l * p.E + e;
+    unsigned spins = 0;
+    const unsigned long long t0 = gtime();
+#pragma unroll 1
+    while ((int32_t)(ld_acquire_sys(w) - seq) < 0) {
+        if (spin_abort(p, spins, t0)) return false;
+        if ((spins & 255u) == 0u && ld_relaxed_sys(p.serve_n + l) < 0) {
+            atomicCAS(p.status, 0, kStatusAbandoned);
+            return false;
+        }
+        __nanosleep(64);
+    }
+    fence_proxy_async_all();  // the copy engine's bytes, read next by the bulk-copy (async) proxy
+    return true;
+}
+
 // ---------------------------------------------------------------------------
 // copies (each issued by one lane)
 // ---------------------------------------------------------------------------
@@ -413,7 +482,7 @@ __device__ __forceinline__ void issue_down(const Params& p, const Lists& D, int 
         const int cols = D.act_expert[a] < 0 ? p.Is : p.I;
         const uint32_t rb = (uint32_t)cols * p.bits / 8, sbb = (uint32_t)cols / 16;
         const BlobLayout L = blob_layout(p.H, cols, p.bits);
-        const uint8_t* blob = D.act_blob[a];
+        const uint8_t* blob = reinterpret_cast<const uint8_t*>(reinterpret_cast<uintptr_t>(D.act_blob[a]) & ~(uintptr_t)1);
         uint8_t* u = stage + (size_t)(a - aa) * p.d_unit;
         bulk_load(u, blob + L.down_q + (size_t)j0 * rb, jn * rb, mb);
         const uint32_t s_lo = (j0 * sbb) & ~15u, s_hi = ((j0 + jn) * sbb + 15u) & ~15u;
@@ -652,8 +721,7 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const __grid_constant__ P
     for (int l = p.layer0; l < lend && ok; ++l) {
         const int li = l - p.layer0, par = l & 1;
         const uint32_t ep = ep0 + (uint32_t)li;
-        const bool given = l == p.layer0 && p.rin_idx != nullptr;    // routing from rin_*
-        const bool streamed = l > p.layer0 && p.rin_idx != nullptr;  // routing published, residency checked
+        const bool streamed = p.pub_idx != nullptr;  // routing published, residency checked
         uint8_t* Pbuf = Pb + par * p.p_bytes;
         unsigned long long* hll = p.h_ll + par * h_par;
         // the next layer's router rows, shared rows and directory row do not
@@ -728,7 +796,7 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const __grid_constant__ P
         // exchange while the other warps make the digits (which only the
         // expert rows need) and these warps the shared gate.
         {
-            const int na = given ? 0 : ne * B, ng = given || p.Is == 0 ? 0 : B;
+            const int na = ne * B, ng = p.Is == 0 ? 0 : B;
             const int nr = min(kSW / 2, max(1, na + ng));  // router warps
             if (warp >= kSW - nr) {
                 unsigned long long* lgx = p.lg_ll + (size_t)par * kMaxB * E;
@@ -753,14 +821,7 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const __grid_constant__ P
         }
         __syncthreads();
         // ------------------------------------------------------------ phase B
-        if (given) {
-#pragma unroll 1
-            for (int i = tid; i < B * k; i += kST) {
-                ds->idx[i / k][i % k] = p.rin_idx[i];
-                ds->w[i / k][i % k] = p.rin_w[i];
-            }
-            if (tid < B) ds->sig[tid] = p.Is > 0 ? p.rin_sig[tid] : 0.0f;
-        } else {
+        {
             const bool okl = topk_lists(p, p.lg_ll + (size_t)par * kMaxB * E, ep, TT, M, nlist);
             if (!__syncthreads_and(okl ? 1 : 0)) {
                 ok = false;
@@ -770,34 +831,66 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const __grid_constant__ P
         }
         fence_proxy_async();  // the top-k scratch shares the area the copies below write
         __syncthreads();
+        bool gated = false;
         if (streamed) {
             // residency of the layer's experts: the same answer in every CTA
             const bool absent = tid < B * k && dirs[(l & 1) * E + ds->idx[tid / k][tid % k]] == nullptr;
-            const bool stop = __syncthreads_or(absent ? 1 : 0) != 0;
-            if (c == 0) {
+            gated = __syncthreads_or(absent ? 1 : 0) != 0;
+            // the routing goes to the host from one warp of CTA 0 (the others go on)
+            if (c == 0 && warp == kSW - 1) {
                 int32_t* row = p.pub_idx + (size_t)l * p.pub_stride;
 #pragma unroll 1
-                for (int i = tid; i < B * k; i += kST) row[i] = ds->idx[i / k][i % k];
-                if (stop) {
-#pragma unroll 1
-                    for (int i = tid; i < B * H; i += kST) p.x_out[i] = xs[i];
-#pragma unroll 1
-                    for (int i = tid; i < B * k; i += kST) {
-                        p.rout_idx[i] = ds->idx[i / k][i % k];
-                        p.rout_w[i] = ds->w[i / k][i % k];
-                    }
-                    if (tid < B) p.rout_sig[tid] = ds->sig[tid];
-                }
+                for (int i = lane; i < B * k; i += 32) row[i] = ds->idx[i / k][i % k];
                 __threadfence_system();
-                __syncthreads();
-                if (tid == 0) {
-                    const uint32_t e = *p.pub_epoch;
-                    if (stop) p.pub_stop[l] = e;
+                __syncwarp();
+                if (lane == 0) {
+                    if (gated) p.pub_gated[l] = p.epoch;
                     __threadfence_system();
-                    p.pub_ready[l] = e;
+                    p.pub_ready[l] = p.epoch;
                 }
             }
-            if (stop) break;  // the host fetches the missing experts and launches again from this layer
+            if (gated) {
+                // the host's answer: the missed experts' slots enter this CTA's
+                // directory row tagged (bit 0) until their copies have landed
+                // (one thread reads the answer word: the host may overwrite it
+                // with -1 at any time, and every thread must take the same branch)
+                bool okg = true;
+                if (tid == 0) {
+                    okg = served_wait(p, l);
+                    ds->serve_n = okg ? ld_relaxed_sys(p.serve_n + l) : -1;
+                }
+                if (!__syncthreads_and(okg ? 1 : 0)) {
+                    ok = false;
+                    break;
+                }
+                const int sn = ds->serve_n;
+                const int nm = sn & 0xffff, nv = (sn >> 16) & 0x7fff;
+                if (sn < 0 || nm > kMaxMiss || nm + nv > p.serve_stride) {
+                    if (tid == 0) atomicCAS(p.status, 0, kStatusAbandoned);
+                    ok = false;
+                    break;
+                }
+                if (tid < nm + nv) (void)ld_acquire_sys(p.served + l);  // this thread's own acquire of the answer
+#pragma unroll 1
+                for (int i = tid; i < nm + nv; i += kST) {
+                    const ServeEntry* en = p.serve_tab + (size_t)l * p.serve_stride + i;
+                    const int e = ld_relaxed_sys(&en->expert), ee = e < 0 ? -1 - e : e;
+                    if (ee >= E) {
+                        atomicCAS(p.status, 0, kStatusAbandoned);
+                    } else if (i < nm) {
+                        const uint8_t* blob = reinterpret_cast<const uint8_t*>(ld_relaxed_sys64(&en->blob));
+                        ds->miss_blob[i] = blob;
+                        ds->miss_seq[i] = (uint32_t)ld_relaxed_sys(reinterpret_cast<const int32_t*>(&en->seq));
+                        ds->miss_e[i] = e;
+                        dirs[(l & 1) * E + e] = reinterpret_cast<const uint8_t*>(reinterpret_cast<uintptr_t>(blob) | 1u);
+                        if (c == 0) p.dir_patch[(size_t)l * E + e] = blob;  // for later launches
+                    } else if (c == 0) {
+                        p.dir_patch[(size_t)l * E + ee] = nullptr;
+                    }
+                }
+                if (tid == 0) ds->n_miss = nm;
+                __syncthreads();
+            }
         }
         if (p.idx_trace && c == 0 && tid < B * k) p.idx_trace[(size_t)li * B * k + tid] = ds->idx[tid / k][tid % k];
         const uint8_t* const* dir_l = dirs + (l & 1) * E;
@@ -849,7 +942,12 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const __grid_constant__ P
             for (int j = 0; j < min(R, wn); ++j) {
                 const int u = wu0 + j, a = u / p.I;
                 const uint8_t* blob = blob_of(a);
-                if (lane == 0) issue_unit(p, blob, u - a * p.I, wslots + (size_t)j * p.g_unit, &mbar[warp * kRing + j]);
+                bool okb = true;
+                if (lane == 0) {
+                    okb = arrival_wait(p, ds, l, blob);
+                    if (okb) issue_unit(p, blob, u - a * p.I, wslots + (size_t)j * p.g_unit, &mbar[warp * kRing + j]);
+                }
+                if (!__shfl_sync(kFullMask, okb, 0)) break;  // the waits below then abort
                 warm |= 1u << j;
             }
         } else {
@@ -859,15 +957,20 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const __grid_constant__ P
             const int U = n_routed * p.I, u0 = U * c / G, u1 = U * (c + 1) / G;  // U <= 129 * 4096
             const int mine = u1 - u0;
             const int wu0 = u0 + mine * warp / kSW, wn = u0 + mine * (warp + 1) / kSW - wu0;
+            int nis = 0;  // units issued (fewer only when a wait gave up)
             if (lane == 0) {
 #pragma unroll 1
                 for (int j = 0; j < min(R, wn); ++j) {
                     const int u = wu0 + j, a = u / p.I;
-                    issue_unit(p, D.act_blob[a], u - a * p.I, wslots + (size_t)j * p.g_unit, &mbar[warp * kRing + j]);
+                    const uint8_t* blob = D.act_blob[a];
+                    if (!arrival_wait(p, ds, l, blob)) break;
+                    issue_unit(p, blob, u - a * p.I, wslots + (size_t)j * p.g_unit, &mbar[warp * kRing + j]);
+                    ++nis;
                 }
             }
+            nis = __shfl_sync(kFullMask, nis, 0);
 #pragma unroll 1
-            for (int j = 0; j < min(R, wn); ++j) warm |= 1u << j;
+            for (int j = 0; j < nis; ++j) warm |= 1u << j;
         }
         const int U = n_routed * p.I, u0 = U * c / G, u1 = U * (c + 1) / G;
         const int mine = u1 - u0;
@@ -915,8 +1018,12 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const __grid_constant__ P
                     const uint8_t* blob = blob_of(an);
                     fence_proxy_async();
                     __syncwarp();
-                    if (lane == 0) issue_unit(p, blob, un - an * p.I, wslots + (size_t)s * p.g_unit, &mbar[warp * kRing + s]);
-                    warm |= 1u << s;
+                    bool okb = true;
+                    if (lane == 0) {
+                        okb = arrival_wait(p, ds, l, blob);
+                        if (okb) issue_unit(p, blob, un - an * p.I, wslots + (size_t)s * p.g_unit, &mbar[warp * kRing + s]);
+                    }
+                    if (__shfl_sync(kFullMask, okb, 0)) warm |= 1u << s;
                 }
             }
             if (!__syncthreads_and(okw ? 1 : 0)) {
@@ -932,6 +1039,17 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const __grid_constant__ P
         // stages are used in rounds of kNSD (one round when every active
         // expert fits).
         {
+            if (gated) {  // every missed expert's down rows are read below
+                bool oka = true;
+                if (tid < ds->n_miss) {
+                    const uint8_t* b = reinterpret_cast<const uint8_t*>(reinterpret_cast<uintptr_t>(ds->miss_blob[tid]) | 1u);
+                    oka = arrival_wait(p, ds, l, b);
+                }
+                if (!__syncthreads_and(oka ? 1 : 0)) {
+                    ok = false;
+                    break;
+                }
+            }
             if (lane == 0) {
                 const int s = kSW - 1 - warp;
                 if (s < min(n_dch, kNSD))
@@ -1234,6 +1352,13 @@ bool stack_supported(const Shapes& sh, const StackScratch& s, int B) {
 
 int stack_last_status(const StackScratch& s) { return s.status_host ? *(volatile int*)s.status_host : 0; }
 
+cudaError_t stack_clear_abandoned(StackScratch& s) {
+    if (!s.status_host || *(volatile int*)s.status_host != kStatusAbandoned) return cudaSuccess;
+    const cudaError_t e = cudaMemset(s.status, 0, sizeof(int));
+    if (e == cudaSuccess) *(volatile int*)s.status_host = 0;
+    return e;
+}
+
 cudaError_t launch_stack(const Shapes& sh, StackScratch& s, const StackArgs& a, cudaStream_t st) {
     Params p{};
     if (!plan(sh, a.B, s.grid, s.max_smem, p)) return cudaErrorInvalidValue;
@@ -1247,13 +1372,14 @@ cudaError_t launch_stack(const Shapes& sh, StackScratch& s, const StackArgs& a, 
     p.sync = s.sync, p.status = s.status, p.status_host = s.status_host_dev;
     p.wait_ns = a.fault ? kFaultWaitNs : kWaitNs;
     p.fault_cta = a.fault ? s.grid - 1 : -1;
-    if (a.rin_idx) {
-        if (!a.rin_w || !a.rin_sig || !a.pub || !a.x_out || !a.rout_idx || !a.rout_w || !a.rout_sig)
-            return cudaErrorInvalidValue;
-        p.rin_idx = a.rin_idx, p.rin_w = a.rin_w, p.rin_sig = a.rin_sig;
-        p.x_out = a.x_out, p.rout_idx = a.rout_idx, p.rout_w = a.rout_w, p.rout_sig = a.rout_sig;
+    if (a.pub) {
+        if (!a.dir_patch || !a.arrive || a.B * sh.top_k > kMaxMiss) return cudaErrorInvalidValue;
         p.pub_idx = a.pub->idx, p.pub_stride = a.pub->idx_stride;
-        p.pub_ready = a.pub->ready, p.pub_stop = a.pub->stop, p.pub_epoch = a.pub->epoch;
+        p.pub_ready = a.pub->ready, p.pub_gated = a.pub->gated;
+        p.served = const_cast<const uint32_t*>(a.pub->served);
+        p.serve_n = const_cast<const int32_t*>(a.pub->serve_n);
+        p.serve_tab = a.pub->serve_tab, p.serve_stride = a.pub->serve_stride;
+        p.dir_patch = a.dir_patch, p.arrive = a.arrive, p.epoch = a.epoch;
     }
     void* f = select_kernel(sh.bits, a.B == 1);
     void* args[] = {&p};

@@ -169,21 +169,35 @@ def test_streaming_pool_trace_and_placement_invariance():
 @pytest.mark.parametrize("B,L,max_batch,slots", [(3, 2, 3, 6), (1, 4, 1, 6), (2, 3, 8, 6), (5, 2, 8, 12)])
 def test_streaming_stack_matches_resident_stack(B, L, max_batch, slots):
     """Whole-stack calls of a streaming context equal the resident context's
-    bitwise: up to 3 tokens through the persistent kernel one layer per launch
-    (routing handed between launches), more through the per-layer kernels."""
+    bitwise: up to 3 tokens (pool >= B * top_k slots) through one persistent
+    launch per call that waits at layers with a miss, more through the
+    per-layer kernels.  The pool events of every (call, layer) equal the
+    oracle simulator fed the resident context's routing."""
     w = dataclasses.replace(TINY, n_layers=L)
     res = _ctx(w, max_batch=max_batch)
     st = _ctx(w, max_batch=max_batch, pool_slots=slots, policy=moe.MOE_EVICT_LRU)
+    sims = [oracle.PoolSim(slots, w.n_experts, moe.MOE_EVICT_LRU) for _ in range(L)]
+    one_launch = B <= 3
     try:
+        idx_tr = torch.empty((L, B, w.top_k), dtype=torch.int32, device="cuda")
         for step in range(6):
             x = torch.from_numpy(synth.tokens(w.seed, 7 + step, B, w.hidden)).cuda()
             ya, yb = torch.empty_like(x), torch.empty_like(x)
-            moe.moe_forward_decode_stack(res, 0, L, x, B, ya)
+            moe.moe_forward_decode_stack(res, 0, L, x, B, ya, 1e-6, None, idx_tr, None)
+            n0 = moe.moe_launch_count(st)
             moe.moe_forward_decode_stack(st, 0, L, x, B, yb)
             torch.cuda.synchronize()
             assert torch.equal(ya, yb), step
+            if one_launch:
+                assert moe.moe_launch_count(st) - n0 == 1, step
+            tr = moe.moe_pool_trace(st)
+            for l in range(L):
+                want = sims[l].request(idx_tr[l].cpu().numpy().reshape(-1))
+                got = [tuple(int(v) for v in r[2:]) for r in tr if r[0] == step and r[1] == l]
+                assert got == want, (step, l)
         s = moe.moe_pool_stats(st)
         assert s["misses"] > 0 and s["calls"] == 6 * L
+        assert s["h2d_ms"] > 0.0  # the copies' event timing is harvested
         # a call over the upper layers only
         x = torch.from_numpy(synth.tokens(w.seed, 99, B, w.hidden)).cuda()
         ya, yb = torch.empty_like(x), torch.empty_like(x)
@@ -384,6 +398,33 @@ def test_injected_faults_fail_cleanly():
         assert e.value.code == moe.MOE_ESTATE  # poisoned
     finally:
         moe.moe_destroy(ctx)
+
+
+def test_streaming_stack_abandoned_by_a_failed_copy_ends_cleanly():
+    """A miss copy that fails (injected) while the persistent kernel waits at
+    the layer: the call returns MOE_ECUDA, the host marks the layer abandoned,
+    the kernel sees it and ends at once (the stream synchronises well before
+    any device-side wait could run out), and the context is poisoned."""
+    import time
+    w = dataclasses.replace(TINY, n_layers=3)
+    x = torch.from_numpy(synth.tokens(w.seed, 5, 1, w.hidden)).cuda()
+    y = torch.empty_like(x)
+    ctx = _ctx(w, max_batch=1, pool_slots=6, fault_flags=moe.MOE_FAULT_MISS_COPY, fault_arg=1)
+    try:
+        n0 = moe.moe_launch_count(ctx)
+        t0 = time.perf_counter()
+        with pytest.raises(moe.MoeError) as e:
+            moe.moe_forward_decode_stack(ctx, 0, 3, x, 1, y)
+        assert e.value.code == moe.MOE_ECUDA
+        torch.cuda.synchronize()
+        assert time.perf_counter() - t0 < 0.5
+        assert moe.moe_launch_count(ctx) - n0 == 1  # it was the persistent kernel
+        with pytest.raises(moe.MoeError) as e:
+            moe.moe_forward_decode_stack(ctx, 0, 3, x, 1, y)
+        assert e.value.code == moe.MOE_ESTATE
+    finally:
+        moe.moe_destroy(ctx)
+    torch.cuda.synchronize()
 
 
 def test_device_wait_runs_out_and_reports_timeout():
