@@ -243,13 +243,15 @@ int moe_forward_decode(moe_ctx* ctx, int32_t layer, const float* x_dev, int32_t 
  * All-resident contexts run the whole stack as one persistent kernel.
  * Streaming contexts run up to 3 tokens on the same kernel (when the pool has
  * at least B x top_k slots), one launch per call: it publishes each layer's
- * routing to the host and goes on through layers whose experts are all
- * resident; at a layer with an absent expert it waits for the host's slot
- * assignment, uses the resident experts at once and each missing expert as
- * soon as its own copy has landed [Swiftlet article, section 3: misses hidden
- * behind compute].  The call returns once the host has served every layer;
- * if the host has to give up mid-call (an I/O error, a failed copy) the
- * kernel ends early and the context is poisoned.  Calls with traces use the
+ * routing to the host, which runs the slot pool on it, and never stops.  A
+ * missing expert's rows are read straight from the pinned store in host
+ * memory (or from the staging buffer the host reads it into from an expert
+ * container) and written into the slot the pool chose by the CTAs that read
+ * them, so misses cost link bandwidth inside the layer rather than a copy and
+ * a relaunch [Swiftlet article, section 3: misses hidden behind compute].
+ * The call returns once the host has served every layer; if the host has to
+ * give up mid-call (an I/O error, an injected fault) the kernel ends early
+ * and the context is poisoned.  Calls with traces use the
  * per-layer kernels.  From 4 tokens on: per-layer kernels with the host's pool
  * decision between routing and dispatch of every layer.  All paths give the
  * same bits.

@@ -14,11 +14,12 @@
 // stream -- the CUDA counterpart of Swiftlet's one pread per expert from the
 // fixed-stride container (article section 2; explainer "Flujo de Inferencia"
 // steps 3-6).  Behind the per-layer kernels the compute stream waits on an
-// event recorded after the copies; behind the persistent decode kernel each
-// copy is followed on the side stream by a stream memory write of the
-// expert's arrival word, which the running kernel waits for before it reads
-// that expert's rows (and only those).  That is this library's explicit
-// hazard management between slot refills and the kernels that read them.  A streaming context can instead take its
+// event recorded after the copies, which is this library's explicit hazard
+// management between slot refills and the kernels that read them.  Behind the
+// persistent decode kernel (a few tokens) there is no copy at all: the store
+// is mapped pinned memory, the kernel reads a missing expert's rows straight
+// from it over the host-device link and writes them into the slot the pool
+// chose, which the host names in mapped memory while the rows are in flight.  A streaming context can instead take its
 // routed blobs from an expert container on disk (store.cpp): a miss is then
 // one positioned read of the blob into a pinned staging buffer followed by the
 // same copy, which is Swiftlet's own fetch path.
@@ -33,8 +34,6 @@
 #include <string>
 #include <thread>
 #include <vector>
-
-#include <cuda.h>
 
 #include "moe_internal.h"
 #include "store.h"
@@ -83,9 +82,6 @@ struct moe_ctx {
     float* part = nullptr;  // [max_pairs][H] weighted down rows of each pair
     float* xbuf = nullptr;  // [2][max_batch][H]
     float* ybuf = nullptr;  // [max_batch][H]
-    // streaming through the persistent kernel: the sequence number of the last
-    // copy into each expert's slot [n_layers][E], set by the side stream
-    uint32_t* arrive = nullptr;
     // streaming, whole-stack calls: each layer's input [n_layers][max_batch][H],
     // the last layer's output, and one CUDA graph per layer (and one for the
     // first routing) for the call's batch size
@@ -109,15 +105,21 @@ struct moe_ctx {
     double prof_ms[moe::kPrefillKernels] = {};
 
     // host
-    uint8_t* store = nullptr;
+    uint8_t* store = nullptr;      // mapped pinned store [n_layers][E][stride]
+    uint8_t* store_dev = nullptr;  // its device alias
     // streaming from an expert container: the open file and a pinned staging
     // ring, each buffer reused only after its copy to the slot has run
     moe::StoreFile file{};
     std::string store_path;
-    static constexpr int kStage = 16;
+    // (mapped: the persistent kernel reads a staged blob during its layer, so a
+    // buffer is reused within a call only for a later layer; kStage > kMaxMiss)
+    static constexpr int kStage = 64;
     uint8_t* stage = nullptr;  // [kStage][stride]
-    cudaEvent_t stage_ev[kStage] = {};
+    uint8_t* stage_dev = nullptr;
+    cudaEvent_t stage_ev[kStage] = {};  // completes when the buffer's last reader has
     bool stage_used[kStage] = {};
+    uint32_t stage_epoch[kStage] = {};  // call (epoch) and layer of a persistent launch's read, 0: none
+    int stage_layer[kStage] = {};
     int stage_next = 0;
     const uint8_t** dir_host = nullptr;  // streaming: the host's directory (pinned), copied to dir on misses
     // streaming: mapped pinned block: ready [n_layers] (uint32, written by the
@@ -144,9 +146,6 @@ struct moe_ctx {
     std::vector<int32_t> trace;
     cudaStream_t side = nullptr;
     int64_t miss_copies = 0;
-    uint32_t copy_seq = 0;  // sequence number of the last miss copy (never 0)
-    // cuStreamWriteValue32 (driver entry point); null: the persistent kernel does not stream
-    CUresult (*write_value)(CUstream, CUdeviceptr, cuuint32_t, unsigned int) = nullptr;
     bool fault_timeout_armed = false;
     bool fault_device_armed = false;  // MOE_FAULT_DEVICE_WAIT, not yet spent
     uint64_t launches = 0;
@@ -276,12 +275,6 @@ void harvest_copy_timing(moe_ctx* c, bool wait) {
     }
 }
 
-// the next miss copy's sequence number (never 0: arrival words start at 0)
-uint32_t next_seq(moe_ctx* c) {
-    if (++c->copy_seq == 0u) ++c->copy_seq;
-    return c->copy_seq;
-}
-
 // Streaming through the persistent kernel: the host gives up the call from
 // layer l on.  A layer the kernel waits at (now or later) reads serve_n < 0
 // and the kernel ends within microseconds; the host waits for that (bounded).
@@ -309,15 +302,16 @@ void abandon_layers(moe_ctx* c, int l, int lend, uint32_t epoch, cudaStream_t st
 }
 
 // Streaming, host side of one layer: wait until the layer's routing has been
-// published (mapped memory, polled), run the slot pool policy on it and copy
-// each missed expert's blob into its slot with cudaMemcpyAsync on the side
-// stream.  Behind the per-layer kernels (gated_launch false) the compute stream
-// then waits on an event after the copies and the layer's device directory is
-// rewritten before the dispatch enqueued next.  Behind the persistent kernel
-// (gated_launch true) the kernel is waiting at the layer when it found an
-// absent expert: it gets the slots and sequence numbers of the misses at once
-// (before any copy is issued), and each copy is followed by the stream write
-// of the expert's arrival word; the kernel patches the device directory.
+// published (mapped memory, polled) and run the slot pool policy on it.
+// Behind the per-layer kernels (gated_launch false) each missed expert's blob
+// is copied into its slot with cudaMemcpyAsync on the side stream, the compute
+// stream waits on an event after the copies, and the layer's device directory
+// is rewritten before the dispatch enqueued next.  Behind the persistent
+// kernel (gated_launch true) nothing is copied: the kernel, which found the
+// same experts absent, reads their rows from host memory (the mapped store,
+// or a staging buffer that the blob is first read into from the container)
+// and needs only the answer -- slots, staging buffers, evictions -- to fill
+// the slots and patch the device directory itself.
 int serve_layer(moe_ctx* c, int layer, int B, uint32_t epoch, cudaStream_t st, bool gated_launch) {
     const int k = c->cfg.top_k, E = c->cfg.n_experts;
     if (c->fault_timeout_armed) {
@@ -358,11 +352,10 @@ int serve_layer(moe_ctx* c, int layer, int B, uint32_t epoch, cudaStream_t st, b
         c->poisoned = true;
         return MOE_ESTATE;
     }
-    // slots, sequence numbers and the directory first (the pool has decided them)
+    // the pool has decided the slots: the host directory first
     struct Miss {
         int32_t e;
         uint8_t* dst;
-        uint32_t seq;
     };
     std::vector<Miss> miss;
     std::vector<int32_t> evicted;
@@ -380,18 +373,52 @@ int serve_layer(moe_ctx* c, int layer, int B, uint32_t epoch, cudaStream_t st, b
             evicted.push_back(out);
         }
         uint8_t* dst = c->pool + ((size_t)layer * c->cfg.pool_slots + slot) * c->stride;
-        miss.push_back({e, dst, gated ? next_seq(c) : 0u});
+        miss.push_back({e, dst});
         dirh[e] = dst;
     }
-    if (gated) {
+    if (gated_launch) {
         moe::ServeEntry* tab = c->gate_host.serve_tab + (size_t)layer * c->gate_host.serve_stride;
         size_t n = 0;
-        for (const Miss& m : miss) tab[n++] = moe::ServeEntry{m.e, m.seq, m.dst};
-        for (int32_t o : evicted) tab[n++] = moe::ServeEntry{-1 - o, 0u, nullptr};
-        c->gate_host.serve_n[layer] = (int32_t)(miss.size() | evicted.size() << 16);
-        std::atomic_thread_fence(std::memory_order_seq_cst);
-        c->gate_host.served[layer] = epoch;
-        std::atomic_thread_fence(std::memory_order_seq_cst);
+        for (const Miss& m : miss) {
+            const uint8_t* src = nullptr;  // the kernel reads the mapped store itself
+            if (!c->store) {               // expert container: one positioned read into a staging buffer
+                const int si = c->stage_next;
+                c->stage_next = (si + 1) % moe_ctx::kStage;
+                if (c->stage_used[si] && !(c->stage_epoch[si] == epoch && c->stage_layer[si] < layer)) {
+                    if (c->stage_epoch[si] == epoch)  // (kStage > misses of one layer)
+                        return fail(c, MOE_ESTATE, "staging ring overrun at layer %d", layer);
+                    CUDA_TRY(c, cudaEventSynchronize(c->stage_ev[si]));  // an earlier call's reader
+                }
+                uint8_t* buf = c->stage + (size_t)si * c->stride;
+                if (moe::store_read_blob(c->file, layer, m.e, buf) != MOE_OK) {
+                    fail(c, MOE_EIO, "reading expert %d of layer %d from %s failed", m.e, layer,
+                         c->store_path.c_str());
+                    c->poisoned = true;  // the pool already counts the expert as resident
+                    return MOE_EIO;
+                }
+                CUDA_TRY(c, cudaEventRecord(c->stage_ev[si], st));  // completes with the kernel reading it
+                c->stage_used[si] = true;
+                c->stage_epoch[si] = epoch;
+                c->stage_layer[si] = layer;
+                src = c->stage_dev + (size_t)si * c->stride;
+            }
+            if ((c->cfg.fault_flags & MOE_FAULT_MISS_COPY) && c->miss_copies == c->cfg.fault_arg) {
+                c->miss_copies++;
+                return fail(c, MOE_ECUDA, "miss copy %d failed (injected)", c->cfg.fault_arg);
+            }
+            c->miss_copies++;
+            tab[n++] = moe::ServeEntry{m.e, 0, m.dst, src};
+            S.h2d_bytes += c->lstride[layer];  // the blob crosses the link once, read by the kernel
+        }
+        for (int32_t o : evicted) tab[n++] = moe::ServeEntry{-1 - o, 0, nullptr, nullptr};
+        if (gated) {
+            c->gate_host.serve_n[layer] = (int32_t)(miss.size() | evicted.size() << 16);
+            std::atomic_thread_fence(std::memory_order_seq_cst);
+            c->gate_host.served[layer] = epoch;
+            std::atomic_thread_fence(std::memory_order_seq_cst);
+        }
+        S.calls++;
+        return MOE_OK;
     }
     if (miss.empty()) {
         S.calls++;
@@ -422,26 +449,21 @@ int serve_layer(moe_ctx* c, int layer, int B, uint32_t epoch, cudaStream_t st, b
         c->miss_copies++;
         // the slot's previous expert was last read before this routing was published
         CUDA_TRY(c, cudaMemcpyAsync(m.dst, src, c->lstride[layer], cudaMemcpyHostToDevice, c->side));
-        if (gated) {
-            const CUresult r = c->write_value(c->side, (CUdeviceptr)(c->arrive + (size_t)layer * E + m.e), m.seq, 0);
-            if (r != CUDA_SUCCESS) return fail(c, MOE_ECUDA, "cuStreamWriteValue32 failed (%d)", (int)r);
-        }
         if (stage_i >= 0) {
             CUDA_TRY(c, cudaEventRecord(c->stage_ev[stage_i], c->side));
             c->stage_used[stage_i] = true;
+            c->stage_epoch[stage_i] = 0;
         }
         S.h2d_bytes += c->lstride[layer];
     }
     CUDA_TRY(c, cudaEventRecord(c->tev[ti][1], c->side));
     c->tlayer[ti] = layer;
     c->t_rec++;
-    if (!gated_launch) {
-        CUDA_TRY(c, cudaStreamWaitEvent(st, c->tev[ti][1], 0));
-        // the layer's device directory, read by the dispatch enqueued next (the
-        // source is pinned; the host rewrites it only after a later routing of
-        // this layer has been published, i.e. after this copy has run)
-        CUDA_TRY(c, cudaMemcpyAsync(c->dir + (size_t)layer * E, dirh, sizeof(void*) * E, cudaMemcpyHostToDevice, st));
-    }
+    CUDA_TRY(c, cudaStreamWaitEvent(st, c->tev[ti][1], 0));
+    // the layer's device directory, read by the dispatch enqueued next (the
+    // source is pinned; the host rewrites it only after a later routing of
+    // this layer has been published, i.e. after this copy has run)
+    CUDA_TRY(c, cudaMemcpyAsync(c->dir + (size_t)layer * E, dirh, sizeof(void*) * E, cudaMemcpyHostToDevice, st));
     std::atomic_thread_fence(std::memory_order_release);
     S.calls++;
     return MOE_OK;
@@ -505,7 +527,7 @@ int enq_post(moe_ctx* c, int l, const float* xin, int B, float* yl, cudaStream_t
 // arrival (see serve_layer).  Results are bitwise those of the all-resident
 // persistent kernel.
 bool stream_stack_ok(const moe_ctx* c, int B) {
-    return !c->resident && !c->mixed && c->write_value && B <= moe::kStackPreferMaxB &&
+    return !c->resident && !c->mixed && B <= moe::kStackPreferMaxB &&
            c->active_slots >= B * c->cfg.top_k && moe::stack_supported(c->sh, c->stack, B);
 }
 
@@ -526,7 +548,8 @@ int enq_stack_streaming(moe_ctx* c, int l, int lend, const float* x, int B, floa
     a.shared_stride = c->shared_stride;
     a.pub = &c->gate_dev;
     a.dir_patch = c->dir;
-    a.arrive = c->arrive;
+    a.store = c->store ? c->store_dev : nullptr;
+    a.store_stride = c->stride;
     a.epoch = epoch;
     const cudaError_t e = moe::launch_stack(c->sh, c->stack, a, st);
     if (e != cudaSuccess) return fail(c, MOE_ECUDA, "decode stack launch failed: %s", cudaGetErrorString(e));
@@ -708,7 +731,6 @@ extern "C" void moe_destroy(moe_ctx* c) {
     cudaFree(c->part);
     cudaFree(c->xbuf);
     cudaFree(c->ybuf);
-    cudaFree(c->arrive);
     for (cudaGraphExec_t g : c->graphs)
         if (g) cudaGraphExecDestroy(g);
     cudaFree(c->xring);
@@ -876,8 +898,10 @@ extern "C" int moe_create(const moe_config* cfg, moe_ctx** out) {
                 return bail(MOE_EIO);
             }
             if (cudaHostAlloc(reinterpret_cast<void**>(&c->stage), (size_t)moe_ctx::kStage * c->stride,
-                              cudaHostAllocDefault) != cudaSuccess) {
+                              cudaHostAllocMapped) != cudaSuccess ||
+                cudaHostGetDevicePointer(reinterpret_cast<void**>(&c->stage_dev), c->stage, 0) != cudaSuccess) {
                 cudaGetLastError();
+                if (c->stage) cudaFreeHost(c->stage);
                 c->stage = nullptr;
                 c->err = "cudaHostAlloc of the staging ring failed";
                 return bail(MOE_ENOMEM);
@@ -896,9 +920,10 @@ extern "C" int moe_create(const moe_config* cfg, moe_ctx** out) {
                 }
         } else {
             const size_t store_bytes = (size_t)L * E * c->stride;
-            if (cudaHostAlloc(reinterpret_cast<void**>(&c->store), store_bytes, cudaHostAllocDefault) !=
-                cudaSuccess) {
+            if (cudaHostAlloc(reinterpret_cast<void**>(&c->store), store_bytes, cudaHostAllocMapped) != cudaSuccess ||
+                cudaHostGetDevicePointer(reinterpret_cast<void**>(&c->store_dev), c->store, 0) != cudaSuccess) {
                 cudaGetLastError();
+                if (c->store) cudaFreeHost(c->store);
                 c->store = nullptr;
                 char buf[160];
                 snprintf(buf, sizeof buf, "cudaHostAlloc of the %zu-byte pinned store failed", store_bytes);
@@ -952,21 +977,8 @@ extern "C" int moe_create(const moe_config* cfg, moe_ctx** out) {
             return bail(MOE_ECUDA);
         }
         if ((rc = dev_alloc(c, &c->xring, (size_t)L * Bm * H, "xring")) ||
-            (rc = dev_alloc(c, &c->yout, (size_t)Bm * H, "yout")) ||
-            (rc = dev_alloc(c, &c->arrive, (size_t)L * E, "arrival words")))
+            (rc = dev_alloc(c, &c->yout, (size_t)Bm * H, "yout")))
             return bail(rc);
-        if (cudaMemset(c->arrive, 0, sizeof(uint32_t) * (size_t)L * E) != cudaSuccess) {
-            c->err = "cudaMemset failed";
-            return bail(MOE_ECUDA);
-        }
-        // stream memory writes mark each miss copy's arrival for the persistent kernel
-        void* fn = nullptr;
-        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-        if (cudaGetDriverEntryPointByVersion("cuStreamWriteValue32", &fn, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess && fn)
-            c->write_value = reinterpret_cast<CUresult (*)(CUstream, CUdeviceptr, cuuint32_t, unsigned int)>(fn);
-        cudaGetLastError();
     }
     for (auto& pr : c->tev)
         for (cudaEvent_t& e : pr)

@@ -66,13 +66,15 @@ struct Dispatch {
 };
 
 // One entry of the host's answer to a streaming layer with absent experts:
-// a missed expert (expert >= 0) with the slot its blob is being copied to and
-// the sequence number the copy's arrival word will carry, or an evicted one
-// (expert = -1 - id, blob null).
+// a missed expert (expert >= 0) with the slot the pool gave it and, for an
+// expert container, the pinned staging buffer its blob has been read into
+// (null when the whole store is in pinned host memory), or an evicted one
+// (expert = -1 - id, slot null).
 struct ServeEntry {
     int32_t expert;
-    uint32_t seq;
-    const uint8_t* blob;
+    int32_t pad;
+    const uint8_t* slot;
+    const uint8_t* src;
 };
 
 // Publication of a streaming layer's routing to the host and the host's
@@ -85,7 +87,7 @@ struct ServeEntry {
 struct HostGate {
     volatile uint32_t* ready;        // [n_layers] epoch of the last routing published per layer
     const volatile uint32_t* epoch;  // [1] the epoch of the current call, written by the host
-    volatile uint32_t* gated;        // [n_layers] epoch of the call whose persistent launch waits at the layer
+    volatile uint32_t* gated;        // [n_layers] epoch of the call whose persistent launch found an absent expert there
     int32_t* idx;                    // [n_layers][idx_stride] the published routing of each layer
     int idx_stride;                  // max_batch * top_k
     volatile uint32_t* served;       // [n_layers] epoch of the call whose layer has been answered

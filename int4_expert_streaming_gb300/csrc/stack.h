@@ -35,14 +35,17 @@ struct StackArgs {
     const uint8_t* const* dir;
     const uint8_t* shared_pool;
     size_t shared_stride;
-    // streaming: every layer's routing is published through `pub`; a layer
-    // with an absent expert waits for the host's answer (the slots of its
-    // missing experts, then each blob's arrival word), patches the device
-    // directory `dir_patch` (the array `dir` points to) and runs on
+    // streaming: every layer's routing is published through `pub`.  A layer
+    // with absent experts reads their rows straight from host memory (the
+    // pinned store `store`, blob stride store_stride, or, when store is null,
+    // the staging buffers named in the host's answer), and each CTA writes
+    // the rows it read into the slots of the host's answer; CTA 0 patches the
+    // device directory `dir_patch` (the array `dir` points to).
     const HostGate* pub;
     const uint8_t** dir_patch;
-    const uint32_t* arrive;  // [n_layers][n_experts] sequence number of the last copy into each expert's slot
-    uint32_t epoch;          // the call's epoch (what ready/gated/served carry)
+    const uint8_t* store;
+    size_t store_stride;
+    uint32_t epoch;  // the call's epoch (what ready/gated/served carry)
     // tests: one CTA withholds its outputs of the launch's first layer and every
     // device-side wait is bounded by 1 ms, so the others' waits run out
     int fault;
@@ -50,7 +53,7 @@ struct StackArgs {
 
 // largest batch the decode stack sends to the persistent kernel (measured crossover)
 constexpr int kStackPreferMaxB = 3;
-// missed experts per layer a streaming launch can wait for (kStackPreferMaxB tokens x top_k <= 16)
+// missed experts per layer of a streaming launch (kStackPreferMaxB tokens x top_k <= 16)
 constexpr int kMaxMiss = 48;
 
 int stack_alloc(StackScratch& s, const Shapes& sh, int n_layers, int max_batch, int device, std::string& err);

@@ -39,14 +39,17 @@
 // Streaming contexts use it with the host's slot pool behind it.  Every layer
 // publishes its routing to mapped host memory, where the host runs the pool's
 // bookkeeping in order, and checks its experts against the device directory:
-// when all are resident the launch simply goes on.  At a layer with an absent
-// expert every CTA waits for the host's answer (which slot each missing blob
-// is being copied to, and the sequence number that the copy's arrival word
-// will carry), and then goes on as well: rows of resident experts are fetched
-// and used at once, and each missing expert's rows are fetched only after its
-// own arrival word shows the copy done (the host's copy stream sets it right
-// behind the copy).  The copies thus overlap the layer's other work, and one
-// launch still runs the whole call.
+// when all are resident the launch simply goes on.  A missing expert's rows
+// are read straight from pinned host memory (the store, over the
+// host-device link) by the same bulk copies that read resident rows from
+// HBM, and used at once; no copy engine and no host call sits between the
+// routing and the compute.  The CTA that read a row also writes it from
+// shared memory into the HBM slot that the host's pool chose (the answer
+// arrives in mapped memory while the rows are in flight), so the blob
+// crosses the link once and the slot is filled when the launch ends.  With an
+// expert container on disk the host first reads each missing blob into a
+// pinned staging buffer and names it in the answer, which the layer then
+// waits for.  One launch runs the whole call either way.
 //
 // Every wait is bounded (%globaltimer): a poll or an mbarrier wait that does
 // not complete within wait_ns sets the status word; every CTA then stops at
@@ -102,10 +105,12 @@ struct Params {
     // streaming launch (pub_idx non-null): every layer's routing is published
     // to mapped host memory (pub_idx row l, then pub_ready[l] = epoch).  A
     // layer whose experts are all resident (non-null directory entries) runs
-    // on; one that is not sets pub_gated[l] = epoch before the ready word and
-    // waits for served[l] = epoch; serve_n[l] and the layer's serve_tab row
-    // then give the missed experts (slot blob, arrival sequence number) and the
-    // evicted ones.  CTA 0 patches the device directory (dir_patch) with them.
+    // on; one that is not sets pub_gated[l] = epoch before the ready word,
+    // reads the missing experts' rows from host memory (store + (l E + e)
+    // store_stride, or with a null store the staging buffer of the answer)
+    // and, once served[l] = epoch, serve_n[l] and the layer's serve_tab row
+    // give the missed experts' slots and the evicted experts, writes those
+    // rows into the slots.  CTA 0 patches the device directory (dir_patch).
     int32_t* pub_idx;
     int pub_stride;
     volatile uint32_t* pub_ready;
@@ -115,7 +120,8 @@ struct Params {
     const ServeEntry* serve_tab;
     int serve_stride;
     const uint8_t** dir_patch;
-    const uint32_t* arrive;  // [n_layers][E]
+    const uint8_t* store;
+    unsigned long long store_stride;
     uint32_t epoch;
     // shared-memory plan
     int rE, rS, jn;
@@ -276,7 +282,6 @@ __device__ __forceinline__ unsigned long long ld_relaxed_sys64(const void* p) {
     asm volatile("ld.relaxed.sys.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
-__device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
 
 // streaming: the host's answer for layer l (served[l] = the call's epoch);
 // one thread; false on timeout or abort
@@ -304,10 +309,10 @@ struct Disp {
     float xmax[kMaxB];  // max |x| of each token
     float red[kMaxB][2][kSW];
     int n_act, n_routed, n_pairs, n_miss;
-    int serve_n, pad2;  // streaming, a gated layer: the host's answer word, read once per CTA
-    // the missed experts' slots and arrival sequence numbers
-    const uint8_t* miss_blob[kMaxMiss];
-    uint32_t miss_seq[kMaxMiss];
+    // streaming, a gated layer: the missing experts and (once the host's
+    // answer is in: ans = 2; 1 while a warp fetches it, 3 if it failed) their slots
+    int ans, pad2;
+    const uint8_t* miss_slot[kMaxMiss];
     int32_t miss_e[kMaxMiss];
 };
 
@@ -393,37 +398,130 @@ __device__ bool stage_wait(uint64_t* mb, int i, Waits& w, const Params& p) {
     return __syncthreads_and(ok ? 1 : 0) != 0;
 }
 
-// streaming: a directory entry with bit 0 set is a missed expert's slot whose
-// copy may still be in flight.  Strips the tag and, if it was set, waits until
-// the expert's arrival word carries the copy's sequence number.  One thread;
-// false on timeout or when the host abandons the call.
-__device__ __forceinline__ bool arrival_wait(const Params& p, const Disp* ds, int l, const uint8_t*& blob) {
-    const uintptr_t b = reinterpret_cast<uintptr_t>(blob);
-    if (!(b & 1u)) return true;
-    blob = reinterpret_cast<const uint8_t*>(b & ~(uintptr_t)1);
-    int e = -1;
-    uint32_t seq = 0;
+// This CTA's down rows j0 .. j0+jn-1 of a routed expert (H x I), as staged in
+// shared memory ([jn rows of rb bytes][scale/bias words from the 16-byte
+// boundary below row j0's]), into the expert's slot blob; one warp.
+__device__ __forceinline__ void store_down(uint8_t* slot, const uint8_t* unit, int j0, int jn, int H, int I, int bits,
+                                          uint32_t rb, uint32_t dsb, int rows_bytes, int lane) {
+    const size_t q = (size_t)I * H * bits / 8, sq = (size_t)I * H / 16;  // down q at 2q, down sb at 3q + 2sq
+    uint4* dq = reinterpret_cast<uint4*>(slot + 2 * q + (size_t)j0 * rb);
 #pragma unroll 1
-    for (int i = 0; i < ds->n_miss; ++i)
-        if (ds->miss_blob[i] == blob) e = ds->miss_e[i], seq = ds->miss_seq[i];
-    if (e < 0) {  // every tagged entry is in the table
-        atomicCAS(p.status, 0, kStatusAbandoned);
-        return false;
+    for (int i = lane; i < (int)(jn * rb / 16); i += 32) dq[i] = reinterpret_cast<const uint4*>(unit)[i];
+    const uint32_t* ss = reinterpret_cast<const uint32_t*>(unit + rows_bytes + ((j0 * dsb) & 15u));
+    uint32_t* ds = reinterpret_cast<uint32_t*>(slot + 3 * q + 2 * sq + (size_t)j0 * dsb);
+#pragma unroll 1
+    for (int i = lane; i < (int)(jn * dsb / 4); i += 32) ds[i] = ss[i];
+}
+
+// streaming: the host's answer for gated layer l, fetched by the first warp
+// of the CTA that needs it (the others wait for that warp): the missed
+// experts' slots (and, without a store in host memory, their staging buffers,
+// entered tagged into the CTA's directory row); CTA 0 also patches the device
+// directory.  Warp-collective; false (in every lane) on timeout or abort.
+__device__ __forceinline__ bool answer_wait(const Params& p, Disp* ds, int l, const uint8_t** dir_row, int lane) {
+    volatile int* ans = &ds->ans;
+    int s = 0;
+    if (lane == 0) {
+        s = *ans;
+        if (s == 0) s = atomicCAS(&ds->ans, 0, 1) == 0 ? -1 : 1;
     }
-    const uint32_t* w = p.arrive + (size_t)l * p.E + e;
-    unsigned spins = 0;
-    const unsigned long long t0 = gtime();
-#pragma unroll 1
-    while ((int32_t)(ld_acquire_sys(w) - seq) < 0) {
-        if (spin_abort(p, spins, t0)) return false;
-        if ((spins & 255u) == 0u && ld_relaxed_sys(p.serve_n + l) < 0) {
-            atomicCAS(p.status, 0, kStatusAbandoned);
-            return false;
+    s = __shfl_sync(kFullMask, s, 0);
+    if (s == 2) return true;
+    if (s == 3) return false;
+    bool ok = true;
+    if (s == -1) {  // this warp fetches
+        int sn = -1;
+        if (lane == 0) {
+            ok = served_wait(p, l);
+            sn = ok ? ld_relaxed_sys(p.serve_n + l) : -1;
         }
-        __nanosleep(64);
+        sn = __shfl_sync(kFullMask, sn, 0);
+        const int nm = sn & 0xffff, nv = (sn >> 16) & 0x7fff;
+        ok = sn >= 0 && nm == ds->n_miss && nm + nv <= p.serve_stride;
+        bool bad = false;
+        if (ok) {
+            (void)ld_acquire_sys(p.served + l);  // this lane's own acquire of the answer
+#pragma unroll 1
+            for (int i = lane; i < nm + nv; i += 32) {
+                const ServeEntry* en = p.serve_tab + (size_t)l * p.serve_stride + i;
+                const int e = ld_relaxed_sys(&en->expert), ee = e < 0 ? -1 - e : e;
+                if (ee >= p.E) {
+                    bad = true;
+                } else if (i < nm) {
+                    const uint8_t* slot = reinterpret_cast<const uint8_t*>(ld_relaxed_sys64(&en->slot));
+                    int j = -1;
+#pragma unroll 1
+                    for (int q = 0; q < nm; ++q)
+                        if (ds->miss_e[q] == e) j = q;
+                    if (j < 0 || !slot) {
+                        bad = true;
+                    } else {
+                        ds->miss_slot[j] = slot;
+                        if (!p.store) {
+                            const uintptr_t src = (uintptr_t)ld_relaxed_sys64(&en->src);
+                            dir_row[e] = reinterpret_cast<const uint8_t*>(src | 1u);
+                        }
+                        if (blockIdx.x == 0) p.dir_patch[(size_t)l * p.E + e] = slot;  // for later launches
+                    }
+                } else if (blockIdx.x == 0) {
+                    p.dir_patch[(size_t)l * p.E + ee] = nullptr;
+                }
+            }
+            ok = !__any_sync(kFullMask, bad);
+        }
+        __syncwarp();
+        __threadfence_block();
+        if (lane == 0) {
+            if (!ok) atomicCAS(p.status, 0, kStatusAbandoned);
+            *ans = ok ? 2 : 3;
+        }
+        return ok;
     }
-    fence_proxy_async_all();  // the copy engine's bytes, read next by the bulk-copy (async) proxy
-    return true;
+    if (lane == 0) {  // another warp fetches
+        unsigned spins = 0;
+        const unsigned long long t0 = gtime();
+#pragma unroll 1
+        for (;;) {
+            const int v = *ans;
+            if (v == 2) break;
+            if (v == 3 || spin_abort(p, spins, t0)) {
+                ok = false;
+                break;
+            }
+            __nanosleep(32);
+        }
+        __threadfence_block();
+    }
+    return __shfl_sync(kFullMask, ok ? 1 : 0, 0) != 0;
+}
+
+// the slot of missing expert e (after answer_wait); lane-parallel search
+__device__ __forceinline__ uint8_t* miss_slot_of(const Disp* ds, int e, int lane) {
+    const int n = ds->n_miss;
+    int j = -1;
+#pragma unroll 1
+    for (int q = lane; q < n; q += 32)
+        if (ds->miss_e[q] == e) j = q;
+    const unsigned b = __ballot_sync(kFullMask, j >= 0);
+    j = __shfl_sync(kFullMask, j, b ? __ffs(b) - 1 : 0);
+    return j >= 0 ? const_cast<uint8_t*>(ds->miss_slot[j]) : nullptr;
+}
+
+// One gate/up unit in shared memory ([gate q][up q][gate sb][up sb], row r of
+// an expert with I rows) into the expert's slot blob, in 16-byte pieces by one warp.
+__device__ __forceinline__ void store_unit(uint8_t* slot, const uint8_t* unit, int r, int I, uint32_t qb, uint32_t sbb,
+                                           int lane) {
+    const int nq = (int)(qb / 16), ns = (int)(sbb / 16);
+    const size_t q = (size_t)I * qb, sq = (size_t)I * sbb;  // blob layout: gate q, up q, down q, gate sb, up sb, down sb
+#pragma unroll 1
+    for (int i = lane; i < 2 * (nq + ns); i += 32) {
+        size_t off;
+        if (i < 2 * nq)
+            off = (i < nq ? 0 : q) + (size_t)r * qb + 16 * (i < nq ? i : i - nq);
+        else
+            off = 3 * q + (i < 2 * nq + ns ? 0 : sq) + (size_t)r * sbb + 16 * (i < 2 * nq + ns ? i - 2 * nq : i - 2 * nq - ns);
+        *reinterpret_cast<uint4*>(slot + off) = reinterpret_cast<const uint4*>(unit)[i];
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -670,7 +768,7 @@ __device__ __forceinline__ float swiglu_row(const uint8_t* gq, const uint8_t* uq
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <int BITS, bool ONE>
+template <int BITS, bool ONE, bool STREAM>
 __global__ void __launch_bounds__(kST, 1) stack_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ uint64_t mbar[kNB];
@@ -721,7 +819,7 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const __grid_constant__ P
     for (int l = p.layer0; l < lend && ok; ++l) {
         const int li = l - p.layer0, par = l & 1;
         const uint32_t ep = ep0 + (uint32_t)li;
-        const bool streamed = p.pub_idx != nullptr;  // routing published, residency checked
+        const bool streamed = STREAM && p.pub_idx != nullptr;  // routing published, residency checked
         uint8_t* Pbuf = Pb + par * p.p_bytes;
         unsigned long long* hll = p.h_ll + par * h_par;
         // the next layer's router rows, shared rows and directory row do not
@@ -850,59 +948,69 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const __grid_constant__ P
                 }
             }
             if (gated) {
-                // the host's answer: the missed experts' slots enter this CTA's
-                // directory row tagged (bit 0) until their copies have landed
-                // (one thread reads the answer word: the host may overwrite it
-                // with -1 at any time, and every thread must take the same branch)
-                bool okg = true;
-                if (tid == 0) {
-                    okg = served_wait(p, l);
-                    ds->serve_n = okg ? ld_relaxed_sys(p.serve_n + l) : -1;
-                }
-                if (!__syncthreads_and(okg ? 1 : 0)) {
-                    ok = false;
-                    break;
-                }
-                const int sn = ds->serve_n;
-                const int nm = sn & 0xffff, nv = (sn >> 16) & 0x7fff;
-                if (sn < 0 || nm > kMaxMiss || nm + nv > p.serve_stride) {
-                    if (tid == 0) atomicCAS(p.status, 0, kStatusAbandoned);
-                    ok = false;
-                    break;
-                }
-                if (tid < nm + nv) (void)ld_acquire_sys(p.served + l);  // this thread's own acquire of the answer
+                // the layer's missing experts (the same list in every CTA);
+                // their rows are read from host memory, through directory
+                // entries tagged in bit 0 (blob addresses are 4096-aligned)
+                if (warp == 0) {
+                    int n = 0;
 #pragma unroll 1
-                for (int i = tid; i < nm + nv; i += kST) {
-                    const ServeEntry* en = p.serve_tab + (size_t)l * p.serve_stride + i;
-                    const int e = ld_relaxed_sys(&en->expert), ee = e < 0 ? -1 - e : e;
-                    if (ee >= E) {
-                        atomicCAS(p.status, 0, kStatusAbandoned);
-                    } else if (i < nm) {
-                        const uint8_t* blob = reinterpret_cast<const uint8_t*>(ld_relaxed_sys64(&en->blob));
-                        ds->miss_blob[i] = blob;
-                        ds->miss_seq[i] = (uint32_t)ld_relaxed_sys(reinterpret_cast<const int32_t*>(&en->seq));
-                        ds->miss_e[i] = e;
-                        dirs[(l & 1) * E + e] = reinterpret_cast<const uint8_t*>(reinterpret_cast<uintptr_t>(blob) | 1u);
-                        if (c == 0) p.dir_patch[(size_t)l * E + e] = blob;  // for later launches
-                    } else if (c == 0) {
-                        p.dir_patch[(size_t)l * E + ee] = nullptr;
+                    for (int q0 = 0; q0 < B * k; q0 += 32) {
+                        const int q = q0 + lane;
+                        int e = -1;
+                        if (q < B * k) {
+                            e = ds->idx[q / k][q % k];
+                            if (dirs[(l & 1) * E + e] != nullptr) e = -1;
+#pragma unroll 1
+                            for (int q2 = 0; q2 < q && e >= 0; ++q2)
+                                if (ds->idx[q2 / k][q2 % k] == e) e = -1;
+                        }
+                        const unsigned bal = __ballot_sync(kFullMask, e >= 0);
+                        if (e >= 0) ds->miss_e[n + __popc(bal & ((1u << lane) - 1u))] = e;
+                        n += __popc(bal);
+                    }
+                    if (lane == 0) {
+                        ds->n_miss = n;
+                        ds->ans = 0;
                     }
                 }
-                if (tid == 0) ds->n_miss = nm;
+                __syncthreads();
+                if (p.store) {  // the pinned store
+                    if (tid < ds->n_miss) {
+                        const int e = ds->miss_e[tid];
+                        dirs[(l & 1) * E + e] = reinterpret_cast<const uint8_t*>(
+                            reinterpret_cast<uintptr_t>(p.store + ((size_t)l * E + e) * p.store_stride) | 1u);
+                    }
+                } else {  // staging buffers named in the host's answer
+                    bool oka = true;
+                    if (warp == 0) oka = answer_wait(p, ds, l, dirs + (l & 1) * E, lane);
+                    if (!__syncthreads_and(oka ? 1 : 0)) {
+                        ok = false;
+                        break;
+                    }
+                }
                 __syncthreads();
             }
         }
         if (p.idx_trace && c == 0 && tid < B * k) p.idx_trace[(size_t)li * B * k + tid] = ds->idx[tid / k][tid % k];
         const uint8_t* const* dir_l = dirs + (l & 1) * E;
+        const uint8_t** dir_l_w = dirs + (l & 1) * E;
         int n_act, n_pairs, n_routed;
         int el = 0x7fffffff, rk = 0;  // one token: this lane's expert (lanes < k) and its rank among the k
-        // blob of active expert a (every lane calls it; ONE: from the ranks, before the lists are visible)
+        // blob of active expert a (every lane calls it; ONE: from the ranks, before
+        // the lists are visible), tagged in bit 0 when it is read from host memory
         auto blob_of = [&](int a) -> const uint8_t* {
             if (ONE) {
                 const int src = __ffs(__ballot_sync(kFullMask, rk == a && lane < k)) - 1;
                 return dir_l[__shfl_sync(kFullMask, el, src)];
             }
             return D.act_blob[a];
+        };
+        auto expert_of = [&](int a) -> int {
+            if (ONE) return __shfl_sync(kFullMask, el, __ffs(__ballot_sync(kFullMask, rk == a && lane < k)) - 1);
+            return D.act_expert[a];
+        };
+        auto untag = [](const uint8_t* b) {
+            return reinterpret_cast<const uint8_t*>(reinterpret_cast<uintptr_t>(b) & ~(uintptr_t)1);
         };
         if (ONE) {
             // one token: the active experts are its k experts in ascending id
@@ -941,13 +1049,8 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const __grid_constant__ P
 #pragma unroll 1
             for (int j = 0; j < min(R, wn); ++j) {
                 const int u = wu0 + j, a = u / p.I;
-                const uint8_t* blob = blob_of(a);
-                bool okb = true;
-                if (lane == 0) {
-                    okb = arrival_wait(p, ds, l, blob);
-                    if (okb) issue_unit(p, blob, u - a * p.I, wslots + (size_t)j * p.g_unit, &mbar[warp * kRing + j]);
-                }
-                if (!__shfl_sync(kFullMask, okb, 0)) break;  // the waits below then abort
+                const uint8_t* blob = untag(blob_of(a));
+                if (lane == 0) issue_unit(p, blob, u - a * p.I, wslots + (size_t)j * p.g_unit, &mbar[warp * kRing + j]);
                 warm |= 1u << j;
             }
         } else {
@@ -957,20 +1060,15 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const __grid_constant__ P
             const int U = n_routed * p.I, u0 = U * c / G, u1 = U * (c + 1) / G;  // U <= 129 * 4096
             const int mine = u1 - u0;
             const int wu0 = u0 + mine * warp / kSW, wn = u0 + mine * (warp + 1) / kSW - wu0;
-            int nis = 0;  // units issued (fewer only when a wait gave up)
             if (lane == 0) {
 #pragma unroll 1
                 for (int j = 0; j < min(R, wn); ++j) {
                     const int u = wu0 + j, a = u / p.I;
-                    const uint8_t* blob = D.act_blob[a];
-                    if (!arrival_wait(p, ds, l, blob)) break;
-                    issue_unit(p, blob, u - a * p.I, wslots + (size_t)j * p.g_unit, &mbar[warp * kRing + j]);
-                    ++nis;
+                    issue_unit(p, untag(D.act_blob[a]), u - a * p.I, wslots + (size_t)j * p.g_unit, &mbar[warp * kRing + j]);
                 }
             }
-            nis = __shfl_sync(kFullMask, nis, 0);
 #pragma unroll 1
-            for (int j = 0; j < nis; ++j) warm |= 1u << j;
+            for (int j = 0; j < min(R, wn); ++j) warm |= 1u << j;
         }
         const int U = n_routed * p.I, u0 = U * c / G, u1 = U * (c + 1) / G;
         const int mine = u1 - u0;
@@ -1013,17 +1111,23 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const __grid_constant__ P
                                                      xdw + (size_t)t * nc * DW, xS + t * nc, ds->xe[t], nc);
                     if (lane == 0) ll_store(hll + (size_t)pr * p.h_stride + r, h, ep);
                 }
+                if (gated && (reinterpret_cast<uintptr_t>(blob_of(a)) & 1u)) {
+                    // a row read from host memory: into the expert's new slot
+                    const int e = expert_of(a);
+                    uint8_t* slot = answer_wait(p, ds, l, dir_l_w, lane) ? miss_slot_of(ds, e, lane) : nullptr;
+                    if (!slot) {
+                        okw = false;
+                        break;
+                    }
+                    store_unit(slot, st, r, p.I, qb, sbb, lane);
+                }
                 if (j + R < wn) {
                     const int un = wu0 + j + R, an = un / p.I;
-                    const uint8_t* blob = blob_of(an);
+                    const uint8_t* blob = untag(blob_of(an));
                     fence_proxy_async();
                     __syncwarp();
-                    bool okb = true;
-                    if (lane == 0) {
-                        okb = arrival_wait(p, ds, l, blob);
-                        if (okb) issue_unit(p, blob, un - an * p.I, wslots + (size_t)s * p.g_unit, &mbar[warp * kRing + s]);
-                    }
-                    if (__shfl_sync(kFullMask, okb, 0)) warm |= 1u << s;
+                    if (lane == 0) issue_unit(p, blob, un - an * p.I, wslots + (size_t)s * p.g_unit, &mbar[warp * kRing + s]);
+                    warm |= 1u << s;
                 }
             }
             if (!__syncthreads_and(okw ? 1 : 0)) {
@@ -1039,17 +1143,6 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const __grid_constant__ P
         // stages are used in rounds of kNSD (one round when every active
         // expert fits).
         {
-            if (gated) {  // every missed expert's down rows are read below
-                bool oka = true;
-                if (tid < ds->n_miss) {
-                    const uint8_t* b = reinterpret_cast<const uint8_t*>(reinterpret_cast<uintptr_t>(ds->miss_blob[tid]) | 1u);
-                    oka = arrival_wait(p, ds, l, b);
-                }
-                if (!__syncthreads_and(oka ? 1 : 0)) {
-                    ok = false;
-                    break;
-                }
-            }
             if (lane == 0) {
                 const int s = kSW - 1 - warp;
                 if (s < min(n_dch, kNSD))
@@ -1139,6 +1232,15 @@ __global__ void __launch_bounds__(kST, 1) stack_kernel(const __grid_constant__ P
                                                             hd, cols, lane);
                             if (lane == 0) part[(size_t)pr * p.jn + jj] = __fmul_rn(wp, v);
                         }
+                    }
+                    if (gated && pr == D.act_off[a] && (reinterpret_cast<uintptr_t>(D.act_blob[a]) & 1u)) {
+                        // an expert read from host memory: this CTA's down rows of it into its new slot
+                        uint8_t* slot = answer_wait(p, ds, l, dir_l_w, lane) ? miss_slot_of(ds, D.act_expert[a], lane) : nullptr;
+                        if (!slot) {
+                            okc = false;
+                            break;
+                        }
+                        store_down(slot, unit, j0, jn, H, p.I, BITS, rb, dsb, p.d_rows_bytes, lane);
                     }
                 }
                 fence_proxy_async();
@@ -1273,9 +1375,23 @@ bool plan(const Shapes& sh, int B, int grid, int max_smem, Params& p) {
     return off <= budget;
 }
 
-void* select_kernel(int bits, bool one) {
-    if (bits == 4) return one ? reinterpret_cast<void*>(&stack_kernel<4, true>) : reinterpret_cast<void*>(&stack_kernel<4, false>);
-    if (bits == 8) return one ? reinterpret_cast<void*>(&stack_kernel<8, true>) : reinterpret_cast<void*>(&stack_kernel<8, false>);
+// ONE: the batch-1 instance; STREAM: the instance of streaming contexts (all
+// the residency and slot-filling code lives only there)
+void* select_kernel(int bits, bool one, bool stream) {
+    if (bits == 4) {
+        if (stream)
+            return one ? reinterpret_cast<void*>(&stack_kernel<4, true, true>)
+                       : reinterpret_cast<void*>(&stack_kernel<4, false, true>);
+        return one ? reinterpret_cast<void*>(&stack_kernel<4, true, false>)
+                   : reinterpret_cast<void*>(&stack_kernel<4, false, false>);
+    }
+    if (bits == 8) {
+        if (stream)
+            return one ? reinterpret_cast<void*>(&stack_kernel<8, true, true>)
+                       : reinterpret_cast<void*>(&stack_kernel<8, false, true>);
+        return one ? reinterpret_cast<void*>(&stack_kernel<8, true, false>)
+                   : reinterpret_cast<void*>(&stack_kernel<8, false, false>);
+    }
     return nullptr;
 }
 
@@ -1319,8 +1435,8 @@ int stack_alloc(StackScratch& s, const Shapes& sh, int n_layers, int max_batch, 
         err = "stack scratch initialisation failed";
         return MOE_ECUDA;
     }
-    for (int one = 0; one < 2; ++one)
-        if (void* f = select_kernel(sh.bits, one != 0)) {
+    for (int v = 0; v < 4; ++v)
+        if (void* f = select_kernel(sh.bits, (v & 1) != 0, (v & 2) != 0)) {
             if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, s.max_smem - 1024) != cudaSuccess) {
                 cudaGetLastError();
                 s.grid = 0;  // persistent kernel unavailable; per-layer kernels serve the stack
@@ -1343,7 +1459,7 @@ bool stack_supported(const Shapes& sh, const StackScratch& s, int B) {
     if (s.grid <= 0 || !s.lg_ll || B < 1 || B > kMaxB || sh.hidden > 2048 || sh.top_k > 16) return false;
     if (sh.n_experts > 2 * kST) return false;  // two keys per lane in the first top-k level
     if (sh.n_experts % 2) return false;        // directory rows are bulk-copied: 16-byte aligned rows
-    if (!select_kernel(sh.bits, B == 1)) return false;
+    if (!select_kernel(sh.bits, B == 1, false)) return false;
     const int cmax = std::max(sh.inter, sh.shared_inter);
     if (cmax * sh.bits / 128 > 32) return false;  // one chunk per lane on down rows
     Params p{};
@@ -1373,15 +1489,15 @@ cudaError_t launch_stack(const Shapes& sh, StackScratch& s, const StackArgs& a, 
     p.wait_ns = a.fault ? kFaultWaitNs : kWaitNs;
     p.fault_cta = a.fault ? s.grid - 1 : -1;
     if (a.pub) {
-        if (!a.dir_patch || !a.arrive || a.B * sh.top_k > kMaxMiss) return cudaErrorInvalidValue;
+        if (!a.dir_patch || a.B * sh.top_k > kMaxMiss) return cudaErrorInvalidValue;
         p.pub_idx = a.pub->idx, p.pub_stride = a.pub->idx_stride;
         p.pub_ready = a.pub->ready, p.pub_gated = a.pub->gated;
         p.served = const_cast<const uint32_t*>(a.pub->served);
         p.serve_n = const_cast<const int32_t*>(a.pub->serve_n);
         p.serve_tab = a.pub->serve_tab, p.serve_stride = a.pub->serve_stride;
-        p.dir_patch = a.dir_patch, p.arrive = a.arrive, p.epoch = a.epoch;
+        p.dir_patch = a.dir_patch, p.store = a.store, p.store_stride = a.store_stride, p.epoch = a.epoch;
     }
-    void* f = select_kernel(sh.bits, a.B == 1);
+    void* f = select_kernel(sh.bits, a.B == 1, a.pub != nullptr);
     void* args[] = {&p};
     return cudaLaunchCooperativeKernel(f, dim3(s.grid), dim3(kST), args, (size_t)p.smem_bytes, st);
 }
