@@ -32,9 +32,9 @@ import synth  # noqa: E402
 METRIC = "MoE-stack decode tok/s; expert-weight HBM GB/s as fraction of GB300 peak"
 FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) of one decode-stack launch per layer: an ncu capture
-# of the 35B-shaped int4 stack at batch 1 (4 layers, 68.027136 + 0.643328 MB),
+# of the 35B-shaped int4 stack at batch 1 (4 layers, 68.025344 + 0.380160 MB),
 # scaled by the layer count; valid for that workload and the current kernel
-STACK_35B_DRAM_BYTES_PER_LAYER = 68.670464e6 / 4
+STACK_35B_DRAM_BYTES_PER_LAYER = 68.405504e6 / 4
 FALLBACK_BF16_TFLOPS = 1700.0
 PREFILL_METRIC = "MoE prefill tok/s; grouped-GEMM bf16 TFLOP/s as fraction of GB300 dense peak"
 
