@@ -25,7 +25,10 @@
  * reads"].  A bounded per-layer slot pool in HBM caches experts and evicts by
  * use count with recency as the tie-break [article, section 3 "Expert cache
  * pool and LFU+LRU eviction"; README, "How it works": "LFU plus recency"].
- * Misses are copied from a pinned host store on a side stream.
+ * A miss is served from a mapped pinned host store (or from an expert
+ * container on disk through pinned staging buffers): the persistent decode
+ * kernel reads the missing rows over the host link itself and fills the
+ * slot; the per-layer kernels get the blob by one copy on a side stream.
  *
  * Blob layout v1 (little-endian; offsets in bytes, rows x cols per matrix):
  *   gate.q  [inter  x hidden*bits/32] u32   element c of a row in word
@@ -162,7 +165,7 @@ int moe_pack_expert(int32_t hidden, int32_t inter, int32_t bits, const uint8_t* 
  * cache pool and LFU+LRU eviction": a bounded pool of experts in memory.]
  * Validate cfg, allocate the HBM slot pool (n_layers x pool_slots x stride,
  * 64-bit offsets), the device directory, scratch and, when streaming, the
- * pinned host store (n_layers x n_experts x stride) and the side stream.
+ * mapped pinned host store (n_layers x n_experts x stride) and the side stream.
  * Errors: MOE_EINVAL (bad config, nothing allocated), MOE_ENOMEM, MOE_ECUDA,
  * MOE_EIO (store_path cannot be opened, or its header does not match the
  * config's n_layers, n_experts, hidden, inter and bits).
@@ -221,9 +224,12 @@ int moe_set_router_bias_all(moe_ctx* ctx, const float* router_bias_host, void* s
  *   x_dev   fp32 [B x hidden] in, y_dev fp32 [B x hidden] out (may not alias x).
  *   topk_idx_dev int32 [B x top_k] / topk_w_dev fp32 [B x top_k]: the chosen
  *   experts in descending-logit order and their weights, or NULL.
- * Asynchronous on `stream` when all experts are resident; otherwise it reads
- * the routing back once, fetches missed blobs on the side stream and orders
- * `stream` after them.  Errors: MOE_EINVAL, MOE_ESTATE (layer not loaded),
+ * Asynchronous on `stream` when all experts are resident.  A streaming context
+ * reads the routing back once per call: with topk_idx_dev and topk_w_dev NULL
+ * and B <= 3 the layer runs on the persistent kernel, which reads missed
+ * blobs from host memory itself (see moe_forward_decode_stack); otherwise the
+ * missed blobs are copied on the side stream and `stream` is ordered after
+ * them.  Errors: MOE_EINVAL, MOE_ESTATE (layer not loaded),
  * MOE_EPOOL, MOE_ETIMEOUT, MOE_ECUDA.
  */
 int moe_forward_decode(moe_ctx* ctx, int32_t layer, const float* x_dev, int32_t B, float* y_dev,
