@@ -522,10 +522,10 @@ int enq_post(moe_ctx* c, int l, const float* xin, int B, float* yl, cudaStream_t
 }
 
 // Streaming stacks of a few tokens run as one persistent launch per call: the
-// kernel publishes every layer's routing and waits only at a layer with an
-// absent expert, for the host's answer and then for each missing blob's
-// arrival (see serve_layer).  Results are bitwise those of the all-resident
-// persistent kernel.
+// kernel publishes every layer's routing, reads a missing expert's rows from
+// host memory itself and needs the host's answer only to fill the slots (see
+// serve_layer).  Results are bitwise those of the all-resident persistent
+// kernel.
 bool stream_stack_ok(const moe_ctx* c, int B) {
     return !c->resident && !c->mixed && B <= moe::kStackPreferMaxB &&
            c->active_slots >= B * c->cfg.top_k && moe::stack_supported(c->sh, c->stack, B);
